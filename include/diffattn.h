@@ -1,0 +1,156 @@
+/*
+ * diffattn.h -- C ABI of the GB300 (sm_103a) differential-attention forward.
+ *
+ * Per diff head h, for query row i of a sequence (positions from 0), the
+ * library computes
+ *
+ *   out[i] = RMSNorm( softmax(s Q1 K1^T)[i] V  -  lambda_h softmax(s Q2 K2^T)[i] V ) * w
+ *            * (1 - lambda_init)
+ *
+ * with s = d^-0.5 on the component dim d, keys j <= i when causal, RMSNorm
+ * over the dv = 2d values of one (token, head) with eps, and
+ *   lambda = exp(lambda_q1 . lambda_k1) - exp(lambda_q2 . lambda_k2) + lambda_init,
+ *   lambda_init(l) = 0.8 - 0.6 exp(-0.3 (l - 1)).
+ * Sources: "DiffTransformer.py" (MultiHeadDifferentialAttention.forward: the
+ * lambda reparameterisation, the causal mask, the two softmax maps and their
+ * difference, the per-head RMSNorm and the (1 - lambda_init) scale;
+ * DiffTransformer.__init__: the lambda_init schedule) and
+ * "LlamaDiffSdpaAttention.py" (forward: the two attention calls combined as
+ * attn1 - lambda_full * attn2, grouped key/value heads via repeat_kv on k1, k2
+ * and v, the component-dim scale).
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller; the library never
+ *    frees or retains them past the call's completion on `stream`.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Work is enqueued asynchronously; nothing synchronises except
+ *    diffattn_get_device_status().
+ *  - Argument errors are detected on the host and returned synchronously; in
+ *    that case NOTHING is launched. Problems only a kernel can see (bad
+ *    cu_seqlens contents, a pipeline wait that ran out of time) are recorded
+ *    in a per-device error word read by diffattn_get_device_status(); kernels
+ *    never trap or assert.
+ *  - The library owns, per device, one small error word and cached launch
+ *    state; it allocates nothing per call.
+ */
+#ifndef DIFFATTN_H_
+#define DIFFATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DIFFATTN_OK = 0,
+    DIFFATTN_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer      */
+    DIFFATTN_ERR_UNSUPPORTED = 2,   /* valid request outside the built kernels' shapes */
+    DIFFATTN_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed             */
+    DIFFATTN_ERR_TIMEOUT = 4,       /* a kernel pipeline wait gave up (device status)  */
+    DIFFATTN_ERR_BAD_SEQLENS = 5    /* cu_seqlens not monotone / out of range (device) */
+} diffattn_status;
+
+typedef enum {
+    DIFFATTN_DTYPE_F32 = 0,         /* q, k, v, out in fp32 (CUDA-core kernel)          */
+    DIFFATTN_DTYPE_BF16 = 1         /* q, k, v, out in bf16 (tcgen05 tensor-core kernel) */
+} diffattn_dtype;
+
+/*
+ * Problem shape.
+ *  Dense mode (cu_seqlens == NULL): `batch` sequences of `seqlen` tokens each,
+ *    packed back to back (token index = b * seqlen + position).
+ *  Packed mode (cu_seqlens != NULL): `num_seqs` sequences; sequence s holds
+ *    tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of `total_tokens`; `max_seqlen`
+ *    must be >= every length (it sizes the launch; longer sequences are
+ *    reported as DIFFATTN_ERR_BAD_SEQLENS by the kernel, not processed).
+ *  num_heads = H diff heads; num_kv_heads = Hkv key/value diff heads, H % Hkv == 0;
+ *    diff head h reads key/value head h / (H / Hkv) for both components.
+ *  d = component dim (Q1, Q2, K1, K2); dv = value dim per diff head (must be 2d).
+ *  eps = RMSNorm epsilon (1e-5 on the pages).
+ */
+typedef struct {
+    int batch;
+    int seqlen;
+    int num_seqs;
+    int max_seqlen;
+    int total_tokens;
+    int num_heads;
+    int num_kv_heads;
+    int d;
+    int dv;
+    diffattn_dtype dtype;
+    float eps;
+} diffattn_desc;
+
+/*
+ * lambda_init for layer `depth` (counted from 1): 0.8 - 0.6 * exp(-0.3 * (depth - 1)).
+ * Source: "DiffTransformer.py", DiffTransformer.__init__ (decaying lambda_init).
+ * Host-only, pure; returns NaN for depth < 1.
+ */
+float diffattn_lambda_init(int depth);
+
+/*
+ * lambda reparameterisation, one value per parameter set:
+ *   lambda_out[i] = exp(sum_e lq1[i*d+e] * lk1[i*d+e]) - exp(sum_e lq2[i*d+e] * lk2[i*d+e])
+ *                   + lambda_init
+ * Source: "DiffTransformer.py", MultiHeadDifferentialAttention.forward,
+ * "Compute lambda using reparameterization" (the Llama gist computes the same).
+ *  lq1, lk1, lq2, lk2: device fp32 [n_sets][d], contiguous.
+ *  lambda_out: device fp32 [n_sets]. n_sets = 1 for lambdas shared by all
+ *  heads, H for per-head lambdas. Computed in fp32, not rounded further.
+ * Errors: INVALID_ARG for null pointers, n_sets < 1, d < 1 or d > 1024.
+ */
+diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float* lq2,
+                                const float* lk2, int n_sets, int d, float lambda_init,
+                                float* lambda_out, void* stream);
+
+/*
+ * Differential-attention forward (one launch of the fused kernel).
+ * Source: as in the file header; the output-difference form
+ * O1/l1 - lambda O2/l2 of "LlamaDiffSdpaAttention.py", forward, with the
+ * per-head RMSNorm of "DiffTransformer.py", forward.
+ *  q   : [tokens][H][2d]   Q1 = q[..., :d], Q2 = q[..., d:]     (dtype of desc)
+ *  k   : [tokens][Hkv][2d] K1 = k[..., :d], K2 = k[..., d:]
+ *  v   : [tokens][Hkv][dv]
+ *  out : [tokens][H][dv]   written for every token of every sequence
+ *  lambda : device fp32, lambda_per_head ? [H] : [1] (e.g. from diffattn_lambda)
+ *  lambda_init : the scalar of the (1 - lambda_init) output scale
+ *  subln_w : device fp32 [dv], the RMSNorm weight shared by all heads
+ *  causal : nonzero -> key j takes part in row i iff j <= i (same sequence)
+ *  cu_seqlens : NULL (dense mode) or device int32 [num_seqs + 1], cu[0] = 0,
+ *               nondecreasing, cu[num_seqs] = total_tokens
+ *  All tensors contiguous; q, k, v, out 16-byte aligned. For bf16 the
+ *  output is rounded to nearest even.
+ * Supported: bf16 with d = 64, dv = 128 (tcgen05 kernel); fp32 with
+ *  d in {16, 32, 64}, dv = 2d (CUDA-core kernel). Otherwise UNSUPPORTED.
+ * Errors: INVALID_ARG (null pointer, non-positive sizes, H % Hkv != 0,
+ *  dv != 2d, misalignment, tokens or indices beyond 2^31); UNSUPPORTED;
+ *  CUDA (launch failure). An empty problem (no tokens) returns OK with
+ *  nothing launched.
+ */
+diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k,
+                             const void* v, const float* lambda, int lambda_per_head,
+                             float lambda_init, const float* subln_w, int causal,
+                             const int* cu_seqlens, void* out, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns OK, TIMEOUT, BAD_SEQLENS (first error recorded since the last read),
+ * or CUDA if the synchronisation itself failed.
+ */
+diffattn_status diffattn_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* diffattn_status_string(diffattn_status status);
+
+/*
+ * Test hook (no paper counterpart): sets the limit, in nanoseconds, after
+ * which a kernel pipeline wait gives up and records DIFFATTN_ERR_TIMEOUT.
+ * 0 restores the default (2 s). Affects launches made after the call.
+ */
+void diffattn_set_wait_timeout_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H_ */
