@@ -1,0 +1,411 @@
+"""Benchmark of the causal differential-attention forward on GB300.
+
+One step = the whole path over one batch of the long-context workload
+(B = 1, T = 16384, 16 diff heads, d = 64, dv = 128, no kv grouping, depth 12):
+the lambda kernel, then the fused tcgen05 forward. Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Throughput counts 768 tensor flop per unmasked (query, key) pair per diff head
+(2 components x 2d for the scores + 2 components x 2dv for P V). N > 1 runs
+one rank per GPU under torchrun, each on its own copy of the workload (weak
+scaling, no data-path collective); `value` is all ranks' flop over the
+slowest rank's time. `--impl reference` times the fp64 CPU oracle on bounded
+row samples of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "diff-attn fwd TFLOP/s (causal) & % of GB300 bf16 tensor peak; tokens/s"
+FLOP_PER_PAIR = 768
+WORKLOAD = "long_t16384"
+KERNEL_SRC = os.path.join(ROOT, "differential_attention_diffattn_gb300", "csrc", "fwd_sm103a.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fwd_bf16_sm103a_long_t16384.md")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def causal_pairs(seq_lens, heads):
+    return sum(n * (n + 1) // 2 for n in seq_lens) * heads
+
+
+def kernel_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, only while the
+    kernel source still matches the one that was profiled."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ ours (GPU) ---
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import differential_attention_diffattn_gb300 as da
+    from differential_attention_diffattn_gb300 import workloads as W
+
+    da.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    inp = W.generate(wl, seed=args.seed)
+    tokens = inp.tokens
+    pairs = causal_pairs(inp.seq_lens, wl.num_heads)
+    flops_step = FLOP_PER_PAIR * pairs
+    packed = wl.varlen
+    li = da.diffattn_lambda_init(wl.depth)
+    stream = torch.cuda.current_stream()
+
+    # Two input/output sets, used alternately: each is larger than the 129 MB
+    # L2, so a step never starts on tensors the previous step left in L2.
+    sets = []
+    for _ in range(2):
+        s = dict(q=inp.q.to(dev), k=inp.k.to(dev), v=inp.v.to(dev))
+        s["out"] = torch.empty(tokens, wl.num_heads, wl.dv, dtype=s["q"].dtype, device=dev)
+        sets.append(s)
+    lvec = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    w = inp.subln_w.to(dev)
+    cu = inp.cu_seqlens.to(dev)
+    lam = torch.empty(1 if not wl.lambda_per_head else wl.num_heads, dtype=torch.float32, device=dev)
+
+    def fwd(s):
+        if packed:
+            da.diffattn_fwd(s["q"], s["k"], s["v"], lam, li, w, causal=wl.causal, cu_seqlens=cu,
+                            max_seqlen=inp.max_seqlen, eps=wl.eps, out=s["out"], stream=stream)
+        else:
+            da.diffattn_fwd(s["q"], s["k"], s["v"], lam, li, w, causal=wl.causal, eps=wl.eps, out=s["out"],
+                            stream=stream)
+
+    def step(i):
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        fwd(sets[i % 2])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = None
+    if rank == 0:
+        visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        sampler = ClockSampler(visible[local_rank].strip() if local_rank < len(visible) else str(local_rank))
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        ev[i][0].record(stream)
+        fwd(sets[i % 2])
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = t0.elapsed_time(t1)
+    fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the timed region")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----------------
+    host = {n: getattr(inp, n).pin_memory() for n in ("q", "k", "v", "subln_w", "cu_seqlens")}
+    host_l = [x.pin_memory() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    out_h = torch.empty(tokens, wl.num_heads, wl.dv, dtype=sets[0]["q"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + host_l)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        s = sets[0]
+        for n in ("q", "k", "v"):
+            s[n].copy_(host[n], non_blocking=True)
+        for dst, src in zip(lvec, host_l):
+            dst.copy_(src, non_blocking=True)
+        w.copy_(host["subln_w"], non_blocking=True)
+        cu.copy_(host["cu_seqlens"], non_blocking=True)
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        fwd(s)
+        out_h.copy_(s["out"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops_step * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the end-to-end region")
+    if not torch.isfinite(out_h[:: max(1, tokens // 64)].float()).all():
+        raise RuntimeError("non-finite output")
+
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    achieved = flops_step / (fwd_ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": len(inp.seq_lens) if not packed else None,
+                   "seq_len": inp.max_seqlen, "tokens": tokens, "diff_heads": wl.num_heads,
+                   "kv_heads": wl.num_kv_heads, "d": wl.d, "dv": wl.dv, "depth": wl.depth,
+                   "causal": wl.causal, "flop_per_pair": FLOP_PER_PAIR, "flop_per_step": flops_step,
+                   "l2": "inputs larger than L2: two rotating ~256 MB input/output sets",
+                   "inputs": "seeded N(0,1) q/k/v rounded to bf16, lambda vectors N(0,0.1^2) fp32, subln w = 1"},
+        "tokens_per_s": round(tokens * world * args.steps / (elapsed_ms * 1e-3), 1),
+        "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": round(e2e_ms / args.e2e_steps, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"{pk_kind} bf16 dense burst",
+                     "frac_of_sustained": round(achieved / float(pk["bf16_tflops_sustained"]), 4),
+                     "kernel": "diffattn_fwd_bf16_sm103a_kernel", "launch_ms": round(fwd_ms, 4),
+                     "algorithmic_flop_per_launch": flops_step},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+        "impl": "ours",
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_stride)
+    return line
+
+
+# --------------------------------------------------------- CPU / oracle ---
+
+def oracle_sample(inp, positions):
+    """Oracle rows for the given in-sequence query positions of every sequence
+    and every head; returns (seconds, pairs)."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    wl = inp.wl
+    cu = inp.cu_seqlens.tolist()
+    toks = []
+    for s in range(len(cu) - 1):
+        n = cu[s + 1] - cu[s]
+        toks.extend(cu[s] + p for p in positions if p < n)
+    toks = np.asarray(toks, dtype=np.int32)
+    tt = np.repeat(toks, wl.num_heads)
+    hh = np.tile(np.arange(wl.num_heads, dtype=np.int32), toks.size)
+    keys = [(p + 1 if wl.causal else cu[s + 1] - cu[s]) for s in range(len(cu) - 1) for p in positions
+            if p < cu[s + 1] - cu[s]]
+    pairs = int(sum(keys)) * wl.num_heads
+    li = orc.lambda_init(wl.depth)
+    lam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, li)
+    t = time.perf_counter()
+    orc.forward_rows(inp.cu_seqlens, inp._f64_q, inp._f64_k, inp._f64_v, lam, li, inp.subln_w, wl.eps,
+                     wl.causal, rows=(tt, hh))
+    return time.perf_counter() - t, pairs
+
+
+def _prep_f64(inp):
+    from oracle import oracle as orc
+    if not hasattr(inp, "_f64_q"):
+        inp._f64_q, inp._f64_k, inp._f64_v = orc._f64(inp.q), orc._f64(inp.k), orc._f64(inp.v)
+
+
+def cpu_baseline(inp, stride):
+    from oracle import oracle as orc
+    _prep_f64(inp)
+    positions = list(range(stride // 2, inp.max_seqlen, stride))
+    sec, pairs = oracle_sample(inp, positions)
+    return {"value": round(FLOP_PER_PAIR * pairs / sec / 1e12, 6), "unit": "TFLOP/s", "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(sec, 2),
+            "sample": f"fp64 C oracle (OpenMP) on every {stride}th query row of every head "
+                      f"({len(positions) * inp.wl.num_heads} rows, {pairs} causal pairs) of {inp.wl.name}"}
+
+
+def run_reference(args):
+    from differential_attention_diffattn_gb300 import workloads as W
+    from oracle import oracle as orc
+    wl = W.WORKLOADS[args.workload]
+    inp = W.generate(wl, seed=args.seed)
+    _prep_f64(inp)
+    L = inp.max_seqlen
+    budget_s = args.reference_budget_s
+    # rows per step: start at 64 query positions, shrink so the run fits the budget
+    per_step = 64
+    sec, _ = oracle_sample(inp, list(range(0, L, L // per_step)))
+    est = sec * (args.steps + args.warmup)
+    while est > budget_s and per_step > 2:
+        per_step //= 2
+        est /= 2
+    stride = L // per_step
+    for i in range(args.warmup):
+        oracle_sample(inp, list(range(i % stride, L, stride)))
+    tot_s, tot_pairs = 0.0, 0
+    for i in range(args.steps):
+        s, p = oracle_sample(inp, list(range((i * 37) % stride, L, stride)))
+        tot_s += s
+        tot_pairs += p
+    value = FLOP_PER_PAIR * tot_pairs / tot_s / 1e12
+    sample = (f"fp64 C oracle (OpenMP) per step on {per_step} query positions (stride {stride}, rotating offset) "
+              f"x {wl.num_heads} heads of {wl.name}")
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "seq_len": L, "diff_heads": wl.num_heads, "kv_heads": wl.num_kv_heads,
+                   "d": wl.d, "dv": wl.dv, "depth": wl.depth, "causal": wl.causal, "flop_per_pair": FLOP_PER_PAIR},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "impl": "reference",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-stride", type=int, default=8, help="CPU baseline: every n-th query row")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=150.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        line = run_reference(args)
+        line["n_gpus"] = world
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

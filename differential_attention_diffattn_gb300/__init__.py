@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) differential-attention forward behind a C ABI.
+
+The public functions carry the names of the C entry points in
+include/diffattn.h and take torch tensors for device memory and streams.
+"""
+from ._lib import (  # noqa: F401
+    DTYPE_BF16,
+    DTYPE_F32,
+    DiffAttnDesc,
+    DiffAttnError,
+    diffattn_fwd,
+    diffattn_get_device_status,
+    diffattn_lambda,
+    diffattn_lambda_init,
+    diffattn_set_wait_timeout_ns,
+    diffattn_status_string,
+    load_library,
+)
+from ._build import LIB_PATH, build  # noqa: F401

@@ -1,0 +1,200 @@
+"""ctypes binding of libdiffattn.so (the C ABI of include/diffattn.h).
+
+Argument marshalling only: torch tensors supply device pointers, shapes and
+the current CUDA stream; every step of the computation runs in the library's
+kernels. There is no fallback of any kind: if the library is not built, or a
+call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = range(6)
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+# Names the header declares with external linkage (checked by the ABI tests).
+EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_get_device_status",
+            "diffattn_status_string", "diffattn_set_wait_timeout_ns")
+
+
+class DiffAttnDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("max_seqlen", ctypes.c_int), ("total_tokens", ctypes.c_int), ("num_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("d", ctypes.c_int), ("dv", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libdiffattn.so (built by `_build.build()` / `__graft_entry__.build()`)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libdiffattn.so is not built ({p}); run differential_attention_diffattn_gb300."
+                               "_build.build() first")
+        lib = ctypes.CDLL(p)
+        vp, fp, ip = ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)
+        lib.diffattn_lambda_init.restype = ctypes.c_float
+        lib.diffattn_lambda_init.argtypes = [ctypes.c_int]
+        lib.diffattn_lambda.restype = ctypes.c_int
+        lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp]
+        lib.diffattn_fwd.restype = ctypes.c_int
+        lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
+                                     vp, ctypes.c_int, vp, vp, vp]
+        lib.diffattn_get_device_status.restype = ctypes.c_int
+        lib.diffattn_get_device_status.argtypes = [vp]
+        lib.diffattn_status_string.restype = ctypes.c_char_p
+        lib.diffattn_status_string.argtypes = [ctypes.c_int]
+        lib.diffattn_set_wait_timeout_ns.restype = None
+        lib.diffattn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        del fp, ip
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().diffattn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(t, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------- the ABI ---
+
+def diffattn_lambda_init(depth: int) -> float:
+    """lambda_init of layer `depth` (from 1), computed by the library (host)."""
+    return float(load_library().diffattn_lambda_init(int(depth)))
+
+
+def diffattn_lambda(lq1, lk1, lq2, lk2, lambda_init: float, out=None, stream=None):
+    """lambda per parameter set on the GPU. Vectors fp32 [d] (one set) or
+    [n, d] (n sets, e.g. per head); returns fp32 [n]."""
+    import torch
+    lib = load_library()
+    vs = (lq1, lk1, lq2, lk2)
+    for i, t in enumerate(vs):
+        _check_cuda(t, f"lambda vector {i}")
+        if t.dtype != torch.float32 or t.shape != lq1.shape:
+            raise ValueError("lambda vectors must be fp32 of one shape")
+    d = lq1.shape[-1]
+    n = 1 if lq1.dim() == 1 else lq1.shape[0]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=lq1.device)
+    _check_cuda(out, "out")
+    st = lib.diffattn_lambda(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), n, d, float(lambda_init), _ptr(out),
+                             _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_lambda")
+    return out
+
+
+def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,
+                 max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, stream=None):
+    """Differential-attention forward on the GPU.
+
+    q [B, T, H, 2d] with k [B, T, Hkv, 2d], v [B, T, Hkv, dv] (dense), or
+    q [tokens, H, 2d] with k, v token-major and, for packed sequences,
+    cu_seqlens int32 [num_seqs + 1] on the device plus max_seqlen (host int).
+    lam: fp32 [1] (shared) or [H] (per head). Returns out [..., H, dv] in q's dtype.
+    """
+    import torch
+    lib = load_library()
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (lam, "lambda"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+    if q.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    if lam.dtype != torch.float32 or subln_w.dtype != torch.float32:
+        raise ValueError("lambda and subln_w must be fp32")
+    desc = DiffAttnDesc()
+    if q.dim() == 4:
+        if cu_seqlens is not None:
+            raise ValueError("cu_seqlens goes with token-major [tokens, H, 2d] inputs")
+        B, T, H, two_d = q.shape
+        desc.batch, desc.seqlen = B, T
+        tokens = B * T
+    elif q.dim() == 3:
+        tokens, H, two_d = q.shape
+        if cu_seqlens is None:
+            desc.batch, desc.seqlen = 1, tokens
+        else:
+            _check_cuda(cu_seqlens, "cu_seqlens")
+            if cu_seqlens.dtype != torch.int32:
+                raise ValueError("cu_seqlens must be int32")
+            if max_seqlen is None:
+                raise ValueError("max_seqlen is required with cu_seqlens")
+            desc.num_seqs = cu_seqlens.numel() - 1
+            desc.max_seqlen = int(max_seqlen)
+            desc.total_tokens = tokens
+    else:
+        raise ValueError("q must be [B, T, H, 2d] or [tokens, H, 2d]")
+    Hkv, dv = k.shape[-2], v.shape[-1]
+    desc.num_heads, desc.num_kv_heads = H, Hkv
+    desc.d, desc.dv = two_d // 2, dv
+    desc.dtype = dt
+    desc.eps = float(eps)
+    if k.shape[:-2] != q.shape[:-2] or v.shape[:-2] != q.shape[:-2] or v.shape[-2] != Hkv:
+        raise ValueError("q, k, v token dimensions or kv heads disagree")
+    if lam.numel() not in (1, H):
+        raise ValueError("lambda must hold 1 or H values")
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
+    _check_cuda(out, "out")
+    st = lib.diffattn_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
+                          1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
+                          1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(out),
+                          _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd")
+    return out
+
+
+def diffattn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load_library().diffattn_get_device_status(_stream_handle(stream)))
+
+
+def diffattn_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def diffattn_set_wait_timeout_ns(ns: int) -> None:
+    load_library().diffattn_set_wait_timeout_ns(int(ns))

@@ -1,0 +1,199 @@
+// Host side of the C ABI declared in include/diffattn.h: argument validation,
+// the per-device error word, TMA descriptor encoding and kernel dispatch.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/diffattn.h"
+#include "internal.h"
+
+namespace diffattn {
+namespace {
+
+// Error bits written by kernels; one word per device (a module variable of
+// this library, so nothing is allocated for it).
+__device__ unsigned int g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_error_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_timeout_ns = kDefaultWaitTimeoutNs;
+
+cudaError_t error_word_ptr(unsigned int** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_error_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        err = cudaGetSymbolAddress(&ptr, g_error_word);
+        if (err != cudaSuccess) return err;
+        g_error_ptr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    *out = g_error_ptr[dev];
+    return cudaSuccess;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a [rows][row_elems] row-major tensor; box = 64 elements
+// (128 bytes, 128-byte swizzle) x 128 rows. Rows past the end read as zero.
+bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, uint64_t rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {row_elems, rows};
+    const cuuint64_t strides[1] = {row_elems * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace diffattn
+
+using namespace diffattn;
+
+extern "C" {
+
+float diffattn_lambda_init(int depth) {
+    if (depth < 1) return NAN;
+    return (float)(0.8 - 0.6 * std::exp(-0.3 * (double)(depth - 1)));
+}
+
+diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int n_sets,
+                                int d, float lambda_init, float* lambda_out, void* stream) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out) return DIFFATTN_ERR_INVALID_ARG;
+    if (n_sets < 1 || d < 1 || d > 1024) return DIFFATTN_ERR_INVALID_ARG;
+    if (launch_lambda(lq1, lk1, lq2, lk2, n_sets, d, lambda_init, lambda_out,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+    return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                             const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
+                             int causal, const int* cu_seqlens, void* out, void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_desc& ds = *desc;
+    if (ds.num_heads <= 0 || ds.num_kv_heads <= 0 || ds.num_heads % ds.num_kv_heads != 0 || ds.num_heads > 65535)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.d <= 0 || ds.dv != 2 * ds.d) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lambda) & 3u) || (reinterpret_cast<uintptr_t>(subln_w) & 3u))
+        return DIFFATTN_ERR_INVALID_ARG;
+
+    FwdParams p{};
+    if (cu_seqlens == nullptr) {
+        if (ds.batch < 0 || ds.seqlen < 0) return DIFFATTN_ERR_INVALID_ARG;
+        const long long tokens = (long long)ds.batch * ds.seqlen;
+        if (tokens > INT32_MAX) return DIFFATTN_ERR_INVALID_ARG;
+        p.num_seqs = ds.batch;
+        p.seqlen = ds.seqlen;
+        p.max_seqlen = ds.seqlen;
+        p.total_tokens = (int)tokens;
+    } else {
+        if (ds.num_seqs < 0 || ds.max_seqlen < 0 || ds.total_tokens < 0) return DIFFATTN_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return DIFFATTN_ERR_INVALID_ARG;
+        p.num_seqs = ds.num_seqs;
+        p.seqlen = 0;
+        p.max_seqlen = ds.max_seqlen;
+        p.total_tokens = ds.total_tokens;
+    }
+    if (p.num_seqs > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    // rows of q / out as 32-bit TMA coordinates and element offsets
+    if ((long long)p.total_tokens * ds.num_heads * ds.dv >= (1LL << 40)) return DIFFATTN_ERR_INVALID_ARG;
+
+    const bool bf16_tc = ds.dtype == DIFFATTN_DTYPE_BF16 && ds.d == 64;
+    const bool f32_simt = ds.dtype == DIFFATTN_DTYPE_F32 && (ds.d == 16 || ds.d == 32 || ds.d == 64);
+    if (!bf16_tc && !f32_simt) return DIFFATTN_ERR_UNSUPPORTED;
+    if (bf16_tc && (p.max_seqlen + 127) / 128 > 65535) return DIFFATTN_ERR_INVALID_ARG;
+
+    // An empty problem launches nothing; its tensor pointers may be NULL.
+    if (p.total_tokens == 0 || p.num_seqs == 0 || p.max_seqlen == 0) return DIFFATTN_OK;
+    if (!q || !k || !v || !lambda || !subln_w || !out) return DIFFATTN_ERR_INVALID_ARG;
+
+    unsigned int* err_word = nullptr;
+    if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.lambda = lambda;
+    p.subln_w = subln_w;
+    p.cu_seqlens = cu_seqlens;
+    p.error_word = err_word;
+    p.H = ds.num_heads;
+    p.Hkv = ds.num_kv_heads;
+    p.d = ds.d;
+    p.dv = ds.dv;
+    p.lambda_stride = lambda_per_head ? 1 : 0;
+    p.causal = causal ? 1 : 0;
+    p.lambda_init = lambda_init;
+    p.eps = ds.eps;
+    p.scale = (float)(1.0 / std::sqrt((double)ds.d));
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
+    p.timeout_ns = g_timeout_ns;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+
+    FwdTensorMaps maps;
+    if (!encode_bf16_rows(&maps.q, q, (uint64_t)ds.num_heads * 2 * ds.d, (uint64_t)p.total_tokens) ||
+        !encode_bf16_rows(&maps.k, k, (uint64_t)ds.num_kv_heads * 2 * ds.d, (uint64_t)p.total_tokens) ||
+        !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens))
+        return DIFFATTN_ERR_CUDA;
+    return launch_fwd_bf16_sm103a(p, maps, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+diffattn_status diffattn_get_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    }
+    if (word & kErrBadSeqlens) return DIFFATTN_ERR_BAD_SEQLENS;
+    if (word & kErrTimeout) return DIFFATTN_ERR_TIMEOUT;
+    return DIFFATTN_OK;
+}
+
+const char* diffattn_status_string(diffattn_status s) {
+    switch (s) {
+        case DIFFATTN_OK: return "ok";
+        case DIFFATTN_ERR_INVALID_ARG: return "invalid argument";
+        case DIFFATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case DIFFATTN_ERR_CUDA: return "CUDA error";
+        case DIFFATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+        case DIFFATTN_ERR_BAD_SEQLENS: return "invalid cu_seqlens";
+    }
+    return "unknown status";
+}
+
+void diffattn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : kDefaultWaitTimeoutNs; }
+
+}  // extern "C"

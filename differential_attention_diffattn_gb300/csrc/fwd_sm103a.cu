@@ -1,0 +1,420 @@
+// Fused differential-attention forward for sm_103a (bf16 in, fp32 accumulate,
+// bf16 out), d = 64, dv = 128.
+//
+// One CTA owns 128 query rows of one diff head of one sequence and walks the
+// visible 128-key tiles. Per tile it computes, on the tensor cores,
+//   S1 = Q1 K1^T, S2 = Q2 K2^T           ("DiffTransformer.py", forward,
+//                                          "Compute attention scores")
+// keeps two online-softmax states (running max m_c, running sum l_c), writes
+// the unnormalised probabilities P_c back to tensor memory as bf16 and
+// accumulates O_c += P_c V with the SAME value tile for both components
+// ("LlamaDiffSdpaAttention.py", forward: two attention calls over one
+// value_states). The epilogue forms O1/l1 - lambda O2/l2 (the output-difference
+// form attn1 - lambda_full * attn2), applies the per-head RMSNorm over dv, the
+// weight and (1 - lambda_init) ("DiffTransformer.py", forward, "Normalize each
+// head independently using RMSNorm", "Scale the normalized output") and stores
+// bf16.
+//
+// Roles (320 threads):
+//   warps 0-3  softmax of component 1 (TMEM lanes 0-127 = query rows), then
+//              the epilogue;
+//   warps 4-7  softmax of component 2;
+//   warp  8    TMA producer (Q once, K1|K2 and V per tile into a STAGES ring);
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer.
+// Tensor memory (512 columns of 128 lanes x 32 bit):
+//   [0,128) S1 / P1 (bf16 pairs in the first 64 columns), [128,256) S2 / P2,
+//   [256,384) O1, [384,512) O2.
+// Shared memory: Q1|Q2 (32 KB) + STAGES x (K1|K2 32 KB + V 32 KB), all
+// 128-byte swizzled boxes of [128 rows x 64 bf16] as written by TMA.
+//
+// Every wait is bounded (see sm103a_ptx.cuh); on a timeout the CTA records the
+// error, lets its copies and MMAs in flight finish, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace diffattn {
+namespace {
+
+constexpr int BM = 128;                 // query rows per CTA
+constexpr int BN = 128;                 // keys per tile
+constexpr int HD = 64;                  // component dim d
+constexpr int DV = 128;                 // value dim
+constexpr int STAGES = 3;               // K/V ring depth
+constexpr int NUM_THREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t BOX_BYTES = BM * HD * 2;          // one [128 x 64] bf16 box: 16 KB
+constexpr uint32_t Q_BYTES = 2 * BOX_BYTES;
+constexpr uint32_t K_BYTES = 2 * BOX_BYTES;
+constexpr uint32_t V_BYTES = 2 * BOX_BYTES;
+constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_STAGE0 = Q_BYTES;
+constexpr uint32_t OFF_MISC = OFF_STAGE0 + STAGES * STAGE_BYTES;
+constexpr uint32_t MISC_BYTES = 1024;
+constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + OFF_MISC + MISC_BYTES;
+static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared memory limit");
+
+constexpr uint32_t TMEM_COLS = 512;
+__device__ __forceinline__ uint32_t col_s(int c) { return (uint32_t)c * 128u; }        // S_c / P_c
+__device__ __forceinline__ uint32_t col_o(int c) { return 256u + (uint32_t)c * 128u; } // O_c
+
+// Rescale the running output only when the row maximum grew by more than 2^8
+// (in log2 units); otherwise keep the stale maximum, which bounds P by 256.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+struct Misc {  // lives at OFF_MISC
+    uint64_t q_full;
+    uint64_t k_full[STAGES];
+    uint64_t v_full[STAGES];
+    uint64_t kv_empty[STAGES];
+    uint64_t s_full[2];
+    uint64_t p_ready[2];
+    uint64_t o_full;
+    uint64_t l2_ready;
+    uint32_t tmem_base;
+    int abort_flag;
+    float inv_l2[BM];
+};
+static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
+
+// K-major operand (rows of 64 bf16 = 128 B, 8-row groups 1024 B apart).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
+// MN-major value operand: 64-column halves 16 KB apart, 8-key groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_value(uint32_t saddr) { return smem_desc_sw128(saddr, BOX_BYTES, 1024); }
+
+// True on every lane iff `pred` holds on every lane of the warp.
+__device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffffffu, pred); }
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.x;
+    const int seq = blockIdx.z;
+    const int qt = gridDim.y - 1 - blockIdx.y;  // longest query tiles are scheduled first
+
+    // ---- sequence bounds; uniform over the CTA -----------------------------
+    int start, len;
+    if (p.cu_seqlens != nullptr) {
+        start = p.cu_seqlens[seq];
+        const int end = p.cu_seqlens[seq + 1];
+        const bool bad = start < 0 || end < start || end > p.total_tokens || end - start > p.max_seqlen ||
+                         (seq == 0 && start != 0) || (seq == p.num_seqs - 1 && end != p.total_tokens);
+        if (bad) {
+            if (threadIdx.x == 0) atomicOr(p.error_word, kErrBadSeqlens);
+            return;
+        }
+        len = end - start;
+    } else {
+        start = seq * p.seqlen;
+        len = p.seqlen;
+    }
+    if (qt * BM >= len) return;
+    const int n_kv = p.causal ? qt + 1 : (len + BN - 1) / BN;
+    const int g = h / (p.H / p.Hkv);
+
+    const uint32_t bar_q_full = smem_u32(&ms.q_full);
+    auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
+    auto bar_v_full = [&](int s) { return smem_u32(&ms.v_full[s]); };
+    auto bar_kv_empty = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
+    auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
+    const uint32_t bar_o_full = smem_u32(&ms.o_full);
+    const uint32_t bar_l2_ready = smem_u32(&ms.l2_ready);
+    const uint32_t sq = sbase + OFF_Q;
+    auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
+    auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
+
+    // ---- setup --------------------------------------------------------------
+    if (warp == PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_init(bar_q_full, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_k_full(s), 1);
+            mbar_init(bar_v_full(s), 1);
+            mbar_init(bar_kv_empty(s), 1);
+        }
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(bar_s_full(c), 1);
+            mbar_init(bar_p_ready(c), 128);
+        }
+        mbar_init(bar_o_full, 1);
+        mbar_init(bar_l2_ready, 128);
+        ms.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem_base;
+    const AbortState ab{&ms.abort_flag, p.error_word, p.timeout_ns};
+
+    if (warp == PRODUCER_WARP) {
+        // ================================================= TMA producer ===
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            const int row_q = start + qt * BM;
+            mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
+            tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
+            tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
+            int issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % STAGES;
+                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+                if (!mbar_wait(bar_kv_empty(s), ph ^ 1u, ab)) break;
+                const int row = start + j * BN;
+                mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
+                tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
+                tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
+                mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
+                tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
+                tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+                issued = j + 1;
+            }
+            // Let every copy this CTA started land before shared memory goes away.
+            mbar_wait_drain(bar_q_full, 0, p.timeout_ns);
+            for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
+                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+                mbar_wait_drain(bar_k_full(j % STAGES), ph, p.timeout_ns);
+                mbar_wait_drain(bar_v_full(j % STAGES), ph, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ==================================================== MMA issuer ===
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
+            auto issue_s = [&](int c, int j) {  // S_c = Q_c K_c^T over d = 64 (4 x K16)
+                const uint32_t qa = sq + (uint32_t)c * BOX_BYTES;
+                const uint32_t ka = sk(j % STAGES) + (uint32_t)c * BOX_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    mma_ss(tmem + col_s(c), desc_kmajor(qa + kk * 32), desc_kmajor(ka + kk * 32), idesc_s,
+                           kk > 0 ? 1u : 0u);
+                mma_commit(bar_s_full(c));
+            };
+            auto issue_pv = [&](int c, int j) {  // O_c += P_c V over 128 keys (8 x K16)
+                const uint32_t va = sv(j % STAGES);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(tmem + col_o(c), tmem + col_s(c) + kk * 8, desc_value(va + kk * 2048), idesc_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bar_q_full, 0, ab) && mbar_wait(bar_k_full(0), 0, ab);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int s = j % STAGES;
+                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+                const bool has_next = j + 1 < n_kv;
+                const int s1 = (j + 1) % STAGES;
+                const uint32_t ph1 = (uint32_t)((j + 1) / STAGES) & 1u;
+                if (!(ok = mbar_wait(bar_v_full(s), ph, ab))) break;
+                if (!(ok = mbar_wait(bar_p_ready(0), (uint32_t)j & 1u, ab))) break;
+                tc_fence_after();
+                issue_pv(0, j);
+                if (has_next) {
+                    if (!(ok = mbar_wait(bar_k_full(s1), ph1, ab))) break;
+                    tc_fence_after();
+                    issue_s(0, j + 1);
+                }
+                if (!(ok = mbar_wait(bar_p_ready(1), (uint32_t)j & 1u, ab))) break;
+                tc_fence_after();
+                issue_pv(1, j);
+                mma_commit(bar_kv_empty(s));
+                if (has_next) issue_s(1, j + 1);
+            }
+            // Completes once every MMA issued above has finished (also after an abort).
+            mma_commit(bar_o_full);
+            mbar_wait_drain(bar_o_full, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else {
+        // ======================================== softmax (warps 0-7) ===
+        const int c = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;  // query row in the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + col_s(c);
+        const uint32_t t_o = tmem + lane_off + col_o(c);
+        const int qi = qt * BM + r;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY;  // running max of scores * scale * log2(e)
+        float l = 0.f;        // running sum of 2^(x - m)
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = warp_all(mbar_wait(bar_s_full(c), (uint32_t)j & 1u, ab)))) break;
+            tc_fence_after();
+            float x[BN];
+            {
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) tmem_ld32(t_s + ch * 32, sr[ch]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
+            }
+            const int kbase = j * BN;
+            if ((p.causal && j == qt) || kbase + BN > len) {
+                int lim = p.causal ? min(qi + 1, len) : len;  // keys < lim are visible
+                lim -= kbase;
+#pragma unroll
+                for (int e = 0; e < BN; ++e)
+                    if (e >= lim) x[e] = -INFINITY;
+            }
+            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+            for (int e = 4; e < BN; e += 4) {
+                mx0 = fmaxf(mx0, x[e]);
+                mx1 = fmaxf(mx1, x[e + 1]);
+                mx2 = fmaxf(mx2, x[e + 2]);
+                mx3 = fmaxf(mx3, x[e + 3]);
+            }
+            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            float alpha = 1.f;
+            if (m_tile > m + RESCALE_THRESHOLD) {
+                alpha = ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
+                m = m_tile;
+            }
+            const float neg_m = -m;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int e = 0; e < BN; e += 4) {
+                x[e] = ex2_approx(fmaf(x[e], sl2, neg_m));
+                x[e + 1] = ex2_approx(fmaf(x[e + 1], sl2, neg_m));
+                x[e + 2] = ex2_approx(fmaf(x[e + 2], sl2, neg_m));
+                x[e + 3] = ex2_approx(fmaf(x[e + 3], sl2, neg_m));
+                s0 += x[e];
+                s1 += x[e + 1];
+                s2 += x[e + 2];
+                s3 += x[e + 3];
+            }
+            l = l * alpha + ((s0 + s1) + (s2 + s3));
+            // P_c (bf16 pairs: column i holds keys 2i (low half) and 2i+1) over S_c.
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[half * 64 + 2 * i], x[half * 64 + 2 * i + 1]);
+                tmem_st32(t_s + half * 32, pk);
+            }
+            // O_c holds the sum through tile j-1 here: S_c(j) was issued after PV_c(j-1).
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int ch = 0; ch < DV / 32; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + ch * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_o + ch * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_p_ready(c));
+        }
+
+        if (c == 1) {
+            ms.inv_l2[r] = 1.f / l;
+            mbar_arrive(bar_l2_ready);
+        } else {
+            ok = ok && warp_all(mbar_wait(bar_o_full, 0, ab)) && warp_all(mbar_wait(bar_l2_ready, 0, ab));
+            if (ok) {
+                tc_fence_after();
+                const float lam = p.lambda[h * p.lambda_stride];
+                const float il1 = 1.f / l;
+                const float il2 = ms.inv_l2[r];
+                const uint32_t t_o1 = tmem + lane_off + col_o(0);
+                const uint32_t t_o2 = tmem + lane_off + col_o(1);
+                // pass 1: mean square of D = O1/l1 - lambda O2/l2 over the dv values of the row
+                float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < DV / 32; ++ch) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(t_o1 + ch * 32, o1);
+                    tmem_ld32(t_o2 + ch * 32, o2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float a0 = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                        const float a1 = __uint_as_float(o1[i + 1]) * il1 - lam * (__uint_as_float(o2[i + 1]) * il2);
+                        ss0 = fmaf(a0, a0, ss0);
+                        ss1 = fmaf(a1, a1, ss1);
+                    }
+                }
+                const float rinv = 1.f / sqrtf((ss0 + ss1) / (float)DV + p.eps);
+                const float post = (1.f - p.lambda_init) * rinv;
+                const bool store = qi < len;
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                      ((size_t)(start + (store ? qi : 0)) * p.H + h) * DV);
+                // pass 2: recompute D, normalise, weight, scale, round to bf16 and store
+#pragma unroll
+                for (int ch = 0; ch < DV / 32; ++ch) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(t_o1 + ch * 32, o1);
+                    tmem_ld32(t_o2 + ch * 32, o2);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int e = ch * 32 + i;
+                        const float a0 = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                        const float a1 = __uint_as_float(o1[i + 1]) * il1 - lam * (__uint_as_float(o2[i + 1]) * il2);
+                        pk[i / 2] = pack_bf16x2(a0 * post * __ldg(p.subln_w + e), a1 * post * __ldg(p.subln_w + e + 1));
+                    }
+                    if (store) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: all TMEM traffic of this CTA is complete -----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream) {
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !attr_done[dev]) {
+        err = cudaFuncSetAttribute(diffattn_fwd_bf16_sm103a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        attr_done[dev] = true;
+    }
+    const int n_qt = (p.max_seqlen + BM - 1) / BM;
+    dim3 grid((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
+    diffattn_fwd_bf16_sm103a_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace diffattn

@@ -1,0 +1,54 @@
+// Launch parameters shared by the host C-ABI layer and the kernel translation
+// units of the library. Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace diffattn {
+
+// Bits of the per-device error word written by kernels.
+enum : uint32_t { kErrTimeout = 1u, kErrBadSeqlens = 2u };
+
+// Default limit of every bounded pipeline wait inside a kernel.
+constexpr unsigned long long kDefaultWaitTimeoutNs = 2000000000ull;
+
+// One forward problem after host validation. Sequence s covers tokens
+// [seq_start(s), seq_start(s) + seq_len(s)): dense mode (cu_seqlens == nullptr)
+// uses s * seqlen and seqlen; packed mode reads cu_seqlens on the device.
+struct FwdParams {
+    const void* q;            // [tokens][H][2d]
+    const void* k;            // [tokens][Hkv][2d]
+    const void* v;            // [tokens][Hkv][dv]
+    void* out;                // [tokens][H][dv]
+    const float* lambda;      // [H] or [1]
+    const float* subln_w;     // [dv]
+    const int* cu_seqlens;    // nullptr (dense) or [num_seqs + 1]
+    unsigned int* error_word; // per-device error bits
+    int num_seqs;             // dense: batch
+    int seqlen;               // dense: tokens per sequence
+    int max_seqlen;           // sizes the grid; packed sequences longer are errors
+    int total_tokens;
+    int H, Hkv, d, dv;
+    int lambda_stride;        // 1: per head, 0: shared
+    int causal;
+    float lambda_init;
+    float eps;
+    float scale_log2;         // d^-0.5 * log2(e)
+    float scale;              // d^-0.5
+    unsigned long long timeout_ns;
+};
+
+// TMA descriptors of the bf16 operands, built on the host per call.
+struct FwdTensorMaps {
+    CUtensorMap q, k, v;
+};
+
+// Kernel launchers (each defined in its own translation unit). They return the
+// cudaError_t of the launch.
+cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                          int n_sets, int d, float lambda_init, float* out, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
+
+}  // namespace diffattn

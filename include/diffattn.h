@@ -124,8 +124,9 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  *  d in {16, 32, 64}, dv = 2d (CUDA-core kernel). Otherwise UNSUPPORTED.
  * Errors: INVALID_ARG (null pointer, non-positive sizes, H % Hkv != 0,
  *  dv != 2d, misalignment, tokens or indices beyond 2^31); UNSUPPORTED;
- *  CUDA (launch failure). An empty problem (no tokens) returns OK with
- *  nothing launched.
+ *  CUDA (launch failure). An empty problem (no tokens, no sequences or
+ *  max_seqlen 0) returns OK with nothing launched; its tensor pointers may
+ *  then be NULL.
  */
 diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k,
                              const void* v, const float* lambda, int lambda_per_head,

@@ -40,6 +40,18 @@
  */
 #include <math.h>
 #include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads an OpenMP parallel region of the oracle uses (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 double oracle_lambda_init(int depth) {
     return 0.8 - 0.6 * exp(-0.3 * (double)(depth - 1));

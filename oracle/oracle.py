@@ -54,6 +54,8 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 def _bind(lib):
     dp = ctypes.POINTER(ctypes.c_double)
     ip = ctypes.POINTER(ctypes.c_int)
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
     lib.oracle_lambda_init.restype = ctypes.c_double
     lib.oracle_lambda_init.argtypes = [ctypes.c_int]
     lib.oracle_lambda.restype = None
@@ -98,6 +100,11 @@ def _dp(a: np.ndarray):
 
 def _ip(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def num_threads() -> int:
+    """Host threads the oracle's parallel loops run on."""
+    return int(_load().oracle_num_threads())
 
 
 def lambda_init(depth: int, lib=None) -> float:

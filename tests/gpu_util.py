@@ -1,0 +1,108 @@
+"""Shared helpers of the GPU parity tests: run the library on a generated
+workload, compute the oracle on the same inputs, compare with the stated
+tolerances."""
+import numpy as np
+import torch
+
+import differential_attention_diffattn_gb300 as da
+from oracle import oracle as orc
+
+# Acceptance: fp32 max-abs <= 1e-5; bf16 max-abs <= 2e-2 and normalised L1
+# (sum |y - y_ref| / sum |y_ref|) <= 5e-3, against the fp64 oracle before any
+# output rounding.
+TOL_F32_MAX = 1e-5
+TOL_BF16_MAX = 2e-2
+TOL_BF16_REL = 5e-3
+
+
+def to_dev(inp, dev="cuda"):
+    return {name: getattr(inp, name).to(dev) for name in
+            ("q", "k", "v", "lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2", "subln_w", "cu_seqlens")}
+
+
+def run_gpu(inp, dev="cuda", packed=True, lam_value=None, lambda_init=None, out=None):
+    """The library's forward on `inp`: lambda_init from diffattn_lambda_init,
+    lambda from diffattn_lambda (unless `lam_value` forces it)."""
+    t = to_dev(inp, dev)
+    li = da.diffattn_lambda_init(inp.wl.depth) if lambda_init is None else float(lambda_init)
+    if lam_value is None:
+        lam = da.diffattn_lambda(t["lambda_q1"], t["lambda_k1"], t["lambda_q2"], t["lambda_k2"], li)
+    else:
+        lam = torch.as_tensor(np.atleast_1d(lam_value), dtype=torch.float32, device=dev)
+    if packed:
+        y = da.diffattn_fwd(t["q"], t["k"], t["v"], lam, li, t["subln_w"], causal=inp.wl.causal,
+                            cu_seqlens=t["cu_seqlens"], max_seqlen=inp.max_seqlen, eps=inp.wl.eps, out=out)
+    else:
+        B, T = len(inp.seq_lens), inp.seq_lens[0]
+        sh = lambda x: x.view(B, T, *x.shape[1:])  # noqa: E731
+        y = da.diffattn_fwd(sh(t["q"]), sh(t["k"]), sh(t["v"]), lam, li, t["subln_w"], causal=inp.wl.causal,
+                            eps=inp.wl.eps, out=out)
+        y = y.view(B * T, *y.shape[2:])
+    st = da.diffattn_get_device_status()
+    assert st == 0, da.diffattn_status_string(st)
+    return y
+
+
+def oracle_out(inp, rows=None, lam_value=None, lambda_init=None):
+    li = orc.lambda_init(inp.wl.depth) if lambda_init is None else float(lambda_init)
+    lam = (orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, li)
+           if lam_value is None else lam_value)
+    return orc.forward_rows(inp.cu_seqlens, inp.q, inp.k, inp.v, lam, li, inp.subln_w, inp.wl.eps,
+                            inp.wl.causal, rows)
+
+
+def sample_rows(inp, every=61, edge=128):
+    """Every `every`-th query row of every head plus the first and last `edge`
+    rows of every sequence (rows are independent, so sampling is exact)."""
+    toks = set()
+    cu = inp.cu_seqlens.tolist()
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        toks.update(range(a, min(b, a + edge)))
+        toks.update(range(max(a, b - edge), b))
+        toks.update(range(a, b, every))
+    toks = np.array(sorted(toks), dtype=np.int32)
+    H = inp.wl.num_heads
+    tt = np.repeat(toks, H)
+    hh = np.tile(np.arange(H, dtype=np.int32), toks.size)
+    return tt, hh
+
+
+def row_condition(inp, lam_value):
+    """kappa per (token, head) row: rms(attn1) / rms(D), D = attn1 - lambda attn2
+    before the norm. Both come from the oracle alone: with w = 1, lambda_init = 0
+    and a huge eps E the oracle returns D / sqrt(mean D^2 + E), i.e. D / sqrt(E)
+    to a relative 1e-12. The norm turns an absolute error e in D into e / rms(D),
+    so bf16 rounding of the probabilities (relative to attn1, attn2) is amplified
+    by kappa in rows where the two maps nearly cancel."""
+    E = 1e12
+    ones = np.ones(inp.wl.dv)
+    d_ = orc.forward_rows(inp.cu_seqlens, inp.q, inp.k, inp.v, lam_value, 0.0, ones, E, inp.wl.causal)
+    a1 = orc.forward_rows(inp.cu_seqlens, inp.q, inp.k, inp.v, 0.0, 0.0, ones, E, inp.wl.causal)
+    rms = lambda x: np.sqrt(np.mean(x ** 2, axis=-1))  # noqa: E731
+    return rms(a1) / np.maximum(rms(d_), 1e-300)
+
+
+def compare(got, want, dtype, kappa=None):
+    """got: [..., dv] from the GPU; want: fp64 oracle of the same rows. With
+    `kappa` (per row), the bf16 max-abs bound of each row is scaled by
+    max(1, kappa); the normalised L1 bound is unchanged."""
+    g = got.detach().float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all(), "non-finite output"
+    err = np.abs(g - want)
+    stats = dict(max_abs=float(err.max()) if err.size else 0.0,
+                 rel_l1=float(err.sum() / max(np.abs(want).sum(), 1e-300)))
+    if dtype == "f32":
+        assert stats["max_abs"] <= TOL_F32_MAX, stats
+    else:
+        if kappa is None:
+            assert stats["max_abs"] <= TOL_BF16_MAX, stats
+        else:
+            row_err = err.max(axis=-1)
+            bound = TOL_BF16_MAX * np.maximum(1.0, kappa)
+            worst = np.unravel_index(np.argmax(row_err / bound), row_err.shape)
+            stats.update(worst_row=[int(x) for x in worst], worst_kappa=float(kappa[worst]),
+                         worst_err=float(row_err[worst]))
+            assert (row_err <= bound).all(), stats
+        assert stats["rel_l1"] <= TOL_BF16_REL, stats
+    return stats

@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/diffattn.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import differential_attention_diffattn_gb300 as da
+from differential_attention_diffattn_gb300 import _lib
+from oracle import oracle as orc
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "diffattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    da.build()
+    return da.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(diffattn_[a-z0-9_]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTED), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_lambda_init_host(lib):
+    for depth in (1, 2, 8, 12, 24, 100):
+        assert abs(da.diffattn_lambda_init(depth) - orc.lambda_init(depth)) < 1e-7
+    assert da.diffattn_lambda_init(0) != da.diffattn_lambda_init(0)  # NaN
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert da.diffattn_status_string(s)
+    assert da.diffattn_status_string(99) == "unknown status"
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every case below fails validation first
+
+
+def _desc(**kw):
+    d = _lib.DiffAttnDesc()
+    base = dict(batch=1, seqlen=16, num_heads=4, num_kv_heads=2, d=64, dv=128, dtype=_lib.DTYPE_BF16, eps=1e-5)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+def _fwd(lib, desc, q=FAKE, k=FAKE, v=FAKE, lam=FAKE, w=FAKE, out=FAKE, cu=None):
+    vp = ctypes.c_void_p
+    return lib.diffattn_fwd(ctypes.byref(desc), vp(q), vp(k), vp(v), vp(lam), 0, 0.2, vp(w), 1,
+                            vp(cu) if cu else None, vp(out), None)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(num_heads=3), {}, 1),                 # H % Hkv != 0
+    (dict(dv=64), {}, 1),                       # dv != 2d
+    (dict(num_heads=0), {}, 1),
+    (dict(batch=-1), {}, 1),
+    (dict(eps=-1.0), {}, 1),
+    (dict(dtype=7), {}, 1),
+    ({}, dict(q=0), 1),                         # null pointer
+    ({}, dict(out=0), 1),
+    ({}, dict(q=FAKE + 8), 1),                  # not 16-byte aligned
+    (dict(d=32, dv=64), {}, 2),                 # bf16 only with d = 64
+    (dict(d=128, dv=256, dtype=_lib.DTYPE_F32), {}, 2),
+    (dict(batch=0), {}, 0),                     # empty: nothing to launch
+])
+def test_fwd_rejects_on_host(lib, kw, ptrs, want):
+    assert _fwd(lib, _desc(**kw), **ptrs) == want
+
+
+def test_varlen_argument_checks(lib):
+    d = _desc(num_seqs=-1, max_seqlen=16, total_tokens=16)
+    assert _fwd(lib, d, cu=FAKE) == 1
+    d = _desc(num_seqs=2, max_seqlen=16, total_tokens=16)
+    assert _fwd(lib, d, cu=FAKE + 2) == 1       # misaligned cu_seqlens
+    d = _desc(num_seqs=0, max_seqlen=0, total_tokens=0)
+    assert _fwd(lib, d, cu=FAKE) == 0
+
+
+def test_lambda_rejects_on_host(lib):
+    vp = ctypes.c_void_p
+    assert lib.diffattn_lambda(vp(FAKE), vp(FAKE), vp(FAKE), None, 1, 16, 0.2, vp(FAKE), None) == 1
+    assert lib.diffattn_lambda(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0, 16, 0.2, vp(FAKE), None) == 1
+    assert lib.diffattn_lambda(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 1, 0, 0.2, vp(FAKE), None) == 1
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        _lib.load_library(str(tmp_path / "missing.so"))

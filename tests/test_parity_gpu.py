@@ -1,0 +1,192 @@
+"""GPU parity of the C-ABI path against the fp64 oracle (element by element).
+
+Sizes the oracle finishes in seconds are compared in full; the two largest
+workloads (T = 16384 and the 32k-token packed batch) are compared on sampled
+rows, launched exactly as the benchmark launches them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_diffattn_gb300 as da
+from differential_attention_diffattn_gb300 import workloads as W
+from oracle import oracle as orc
+
+from gpu_util import compare, oracle_out, row_condition, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    da.build()
+    da.load_library()
+    torch.cuda.set_device(0)
+
+
+# -------------------------------------------------------------- lambda ---
+
+@pytest.mark.parametrize("shape", [(16,), (64,), (16, 64), (3, 1000)])
+def test_lambda_kernel(shape):
+    g = torch.Generator().manual_seed(3)
+    vs = [torch.randn(shape, generator=g) * 0.3 for _ in range(4)]
+    li = da.diffattn_lambda_init(7)
+    got = da.diffattn_lambda(*[x.cuda() for x in vs], li).cpu().numpy()
+    want = orc.lambda_values(*vs, orc.lambda_init(7))
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-6)
+
+
+def test_lambda_zero_vectors_give_lambda_init():
+    z = torch.zeros(64, device="cuda")
+    li = da.diffattn_lambda_init(12)
+    got = da.diffattn_lambda(z, z, z, z, li).item()
+    assert got == li
+
+
+# ---------------------------------------------------------- workloads ---
+
+@pytest.mark.parametrize("name", ["tiny_f32", "b2_t512_gqa", "llama1b_b4_t2048"])
+def test_workload_full(name):
+    inp = W.generate(W.WORKLOADS[name], seed=0)
+    got = run_gpu(inp, packed=False)
+    compare(got, oracle_out(inp), inp.wl.dtype)
+
+
+@pytest.mark.parametrize("name", ["long_t16384", "varlen_32k"])
+def test_workload_sampled(name):
+    inp = W.generate(W.WORKLOADS[name], seed=0)
+    got = run_gpu(inp, packed=name == "varlen_32k")
+    assert torch.isfinite(got).all()
+    tt, hh = sample_rows(inp)
+    compare(got[torch.as_tensor(tt).long(), torch.as_tensor(hh).long()], oracle_out(inp, rows=(tt, hh)),
+            inp.wl.dtype)
+
+
+# ---------------------------------------------------------- edge cases ---
+
+BF = W.WORKLOADS["b2_t512_gqa"]
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 255, 1000])
+def test_bf16_ragged_lengths(T):
+    inp = W.generate(BF, seed=T, seq_lens=[T])
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+@pytest.mark.parametrize("lens", [[1, 130, 7, 256, 3], [640, 1], [129, 129, 129], [4096, 33]])
+def test_bf16_packed(lens):
+    inp = W.generate(BF, seed=len(lens), seq_lens=lens)
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+@pytest.mark.parametrize("T", [1, 100, 300])
+def test_bf16_non_causal(T):
+    inp = W.generate(W.with_overrides(BF, causal=False), seed=5, seq_lens=[T, 77])
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+@pytest.mark.parametrize("H,Hkv", [(16, 1), (16, 2), (16, 16), (3, 3), (8, 4)])
+def test_bf16_head_groups(H, Hkv):
+    inp = W.generate(W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv), seed=H * 10 + Hkv, seq_lens=[300])
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+def test_bf16_per_head_lambda_and_random_weight():
+    wl = W.with_overrides(BF, lambda_per_head=True, random_subln=True)
+    inp = W.generate(wl, seed=11, seq_lens=[257, 190])
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+@pytest.mark.parametrize("lam", [0.0, 1.0, 1.9, -0.5])
+def test_bf16_forced_lambda(lam):
+    """lambda = 0 (plain attention), lambda = 1, lambda > 1, lambda < 0. Rows
+    whose two maps nearly cancel are ill-conditioned, so the max-abs bound of
+    each row scales with its kappa (see gpu_util.row_condition)."""
+    inp = W.generate(BF, seed=21, seq_lens=[333])
+    compare(run_gpu(inp, lam_value=lam), oracle_out(inp, lam_value=lam), "bf16",
+            kappa=row_condition(inp, lam))
+
+
+def test_bf16_large_scores():
+    """Scores of a few hundred: exercises the deferred-rescale threshold."""
+    inp = W.generate(BF, seed=22, seq_lens=[700])
+    inp.q = (inp.q.float() * 6).to(torch.bfloat16)
+    inp.k = (inp.k.float() * 6).to(torch.bfloat16)
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+@pytest.mark.parametrize("d,lens", [(16, [64, 3]), (32, [100]), (64, [70, 1])])
+def test_f32_shapes(d, lens):
+    wl = W.with_overrides(W.WORKLOADS["tiny_f32"], d=d, dv=2 * d, num_heads=4, num_kv_heads=2,
+                          random_subln=True)
+    inp = W.generate(wl, seed=d, seq_lens=lens)
+    compare(run_gpu(inp), oracle_out(inp), "f32")
+
+
+def test_f32_non_causal():
+    wl = W.with_overrides(W.WORKLOADS["tiny_f32"], causal=False)
+    inp = W.generate(wl, seed=4, seq_lens=[50, 13])
+    compare(run_gpu(inp), oracle_out(inp), "f32")
+
+
+# ------------------------------------------------------- equivalences ---
+
+def test_batch_equals_separate_calls_bitwise():
+    inp = W.generate(BF, seed=31, seq_lens=[300, 300, 300])
+    full = run_gpu(inp, packed=False)
+    for s in range(3):
+        one = W.generate(BF, seed=31, seq_lens=[300, 300, 300])
+        a, b = s * 300, (s + 1) * 300
+        one.q, one.k, one.v = one.q[a:b], one.k[a:b], one.v[a:b]
+        one.seq_lens, one.cu_seqlens = [300], torch.tensor([0, 300], dtype=torch.int32)
+        assert torch.equal(run_gpu(one), full[a:b])
+
+
+def test_gqa_equals_replicated_bitwise():
+    inp = W.generate(BF, seed=32, seq_lens=[400])
+    a = run_gpu(inp)
+    rep = W.generate(W.with_overrides(BF, num_kv_heads=16), seed=32, seq_lens=[400])
+    rep.q, rep.lambda_q1, rep.lambda_k1 = inp.q, inp.lambda_q1, inp.lambda_k1
+    rep.lambda_q2, rep.lambda_k2, rep.subln_w = inp.lambda_q2, inp.lambda_k2, inp.subln_w
+    rep.k = inp.k.repeat_interleave(4, dim=1)
+    rep.v = inp.v.repeat_interleave(4, dim=1)
+    assert torch.equal(run_gpu(rep), a)
+
+
+def test_deterministic():
+    inp = W.generate(BF, seed=33, seq_lens=[1000, 24])
+    assert torch.equal(run_gpu(inp), run_gpu(inp))
+
+
+# ------------------------------------------------------------- errors ---
+
+def test_bad_cu_seqlens_reported_and_device_usable():
+    inp = W.generate(BF, seed=34, seq_lens=[100, 50])
+    t = {n: getattr(inp, n).cuda() for n in ("q", "k", "v", "subln_w")}
+    lam = torch.tensor([0.3], device="cuda")
+    bad = torch.tensor([0, 120, 150], dtype=torch.int32, device="cuda")  # 120 > max_seqlen 100
+    da.diffattn_fwd(t["q"], t["k"], t["v"], lam, 0.2, t["subln_w"], cu_seqlens=bad, max_seqlen=100)
+    assert da.diffattn_get_device_status() == 5
+    bad2 = torch.tensor([0, 100, 90], dtype=torch.int32, device="cuda")  # not monotone
+    da.diffattn_fwd(t["q"], t["k"], t["v"], lam, 0.2, t["subln_w"], cu_seqlens=bad2, max_seqlen=100)
+    assert da.diffattn_get_device_status() == 5
+    assert da.diffattn_get_device_status() == 0  # cleared by the read
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
+def test_empty_problem_launches_nothing():
+    q = torch.zeros(0, 16, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(0, 4, 128, dtype=torch.bfloat16, device="cuda")
+    lam = torch.tensor([0.3], device="cuda")
+    w = torch.ones(128, device="cuda")
+    out = da.diffattn_fwd(q, k, k, lam, 0.2, w)
+    assert out.shape == (0, 16, 128)
+    assert da.diffattn_get_device_status() == 0
+
+
+def test_unsupported_shape_raises():
+    q = torch.zeros(10, 2, 64, dtype=torch.bfloat16, device="cuda")  # bf16 with d = 32
+    k = torch.zeros(10, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(da.DiffAttnError) as e:
+        da.diffattn_fwd(q, k, k, torch.tensor([0.1], device="cuda"), 0.2, torch.ones(64, device="cuda"))
+    assert e.value.status == 2
