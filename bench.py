@@ -374,7 +374,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-stride", type=int, default=8, help="CPU baseline: every n-th query row")
+    ap.add_argument("--cpu-stride", type=int, default=2, help="CPU baseline: every n-th query row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
     args = ap.parse_args()

@@ -129,7 +129,6 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     const bool bf16_tc = ds.dtype == DIFFATTN_DTYPE_BF16 && ds.d == 64;
     const bool f32_simt = ds.dtype == DIFFATTN_DTYPE_F32 && (ds.d == 16 || ds.d == 32 || ds.d == 64);
     if (!bf16_tc && !f32_simt) return DIFFATTN_ERR_UNSUPPORTED;
-    if (bf16_tc && (p.max_seqlen + 127) / 128 > 65535) return DIFFATTN_ERR_INVALID_ARG;
 
     // An empty problem launches nothing; its tensor pointers may be NULL.
     if (p.total_tokens == 0 || p.num_seqs == 0 || p.max_seqlen == 0) return DIFFATTN_OK;

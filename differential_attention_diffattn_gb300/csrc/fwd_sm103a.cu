@@ -29,6 +29,12 @@
 //
 // Every wait is bounded (see sm103a_ptx.cuh); on a timeout the CTA records the
 // error, lets its copies and MMAs in flight finish, frees TMEM and returns.
+//
+// Per component the tile loop is a chain: softmax(j) -> P_c(j) V and S_c(j+1)
+// on the tensor pipe -> softmax(j+1); the two components' chains interleave on
+// the tensor pipe. (A variant with two 64-key S buffers per component, which
+// breaks the chain, measured slower on GB300: it doubles the MMA instruction
+// and barrier count per key.)
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -195,56 +201,54 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ==================================================== MMA issuer ===
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
-            auto issue_s = [&](int c, int j) {  // S_c = Q_c K_c^T over d = 64 (4 x K16)
-                const uint32_t qa = sq + (uint32_t)c * BOX_BYTES;
-                const uint32_t ka = sk(j % STAGES) + (uint32_t)c * BOX_BYTES;
+        // The whole warp walks the loop with warp-uniform values; one elected
+        // lane issues each tcgen05 instruction. Descriptors are built once and
+        // advanced by constant offsets of their start-address field (16-byte
+        // units): with per-instruction descriptor arithmetic, issue rather than
+        // the tensor pipe limited the MMA rate.
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
+        constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, STG = STAGE_BYTES >> 4, BOX = BOX_BYTES >> 4;
+        const uint64_t qdesc = desc_kmajor(sq), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
+        auto issue_s = [&](int c, int j) {
+            const uint64_t a0 = qdesc + (uint64_t)c * BOX;
+            const uint64_t b0 = kdesc + (uint64_t)(j % STAGES) * STG + (uint64_t)c * BOX;
+            const uint32_t d = tmem + col_s(c);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_ss(tmem + col_s(c), desc_kmajor(qa + kk * 32), desc_kmajor(ka + kk * 32), idesc_s,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(bar_s_full(c));
-            };
-            auto issue_pv = [&](int c, int j) {  // O_c += P_c V over 128 keys (8 x K16)
-                const uint32_t va = sv(j % STAGES);
+            for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a0 + kk * KSTEP, b0 + kk * KSTEP, idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit_elect(bar_s_full(c));
+        };
+        auto issue_pv = [&](int c, int j) {
+            const uint64_t b0 = vdesc + (uint64_t)(j % STAGES) * STG;
+            const uint32_t d = tmem + col_o(c), a = tmem + col_s(c);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + col_o(c), tmem + col_s(c) + kk * 8, desc_value(va + kk * 2048), idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-            };
-            bool ok = mbar_wait(bar_q_full, 0, ab) && mbar_wait(bar_k_full(0), 0, ab);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                issue_s(1, 0);
+            for (int kk = 0; kk < BN / 16; ++kk) mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, kk > 0 ? 1u : acc0);
+        };
+        bool ok = warp_all(mbar_wait(bar_q_full, 0, ab)) && warp_all(mbar_wait(bar_k_full(0), 0, ab));
+        if (ok) { tc_fence_after(); issue_s(0, 0); issue_s(1, 0); }
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int s = j % STAGES;
+            const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+            const bool has_next = j + 1 < n_kv;
+            const int s1 = (j + 1) % STAGES;
+            const uint32_t ph1 = (uint32_t)((j + 1) / STAGES) & 1u;
+            if (!(ok = warp_all(mbar_wait(bar_v_full(s), ph, ab)))) break;
+            if (!(ok = warp_all(mbar_wait(bar_p_ready(0), (uint32_t)j & 1u, ab)))) break;
+            tc_fence_after();
+            issue_pv(0, j);
+            if (has_next) {
+                if (!(ok = warp_all(mbar_wait(bar_k_full(s1), ph1, ab)))) break;
+                issue_s(0, j + 1);
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % STAGES;
-                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-                const bool has_next = j + 1 < n_kv;
-                const int s1 = (j + 1) % STAGES;
-                const uint32_t ph1 = (uint32_t)((j + 1) / STAGES) & 1u;
-                if (!(ok = mbar_wait(bar_v_full(s), ph, ab))) break;
-                if (!(ok = mbar_wait(bar_p_ready(0), (uint32_t)j & 1u, ab))) break;
-                tc_fence_after();
-                issue_pv(0, j);
-                if (has_next) {
-                    if (!(ok = mbar_wait(bar_k_full(s1), ph1, ab))) break;
-                    tc_fence_after();
-                    issue_s(0, j + 1);
-                }
-                if (!(ok = mbar_wait(bar_p_ready(1), (uint32_t)j & 1u, ab))) break;
-                tc_fence_after();
-                issue_pv(1, j);
-                mma_commit(bar_kv_empty(s));
-                if (has_next) issue_s(1, j + 1);
-            }
-            // Completes once every MMA issued above has finished (also after an abort).
-            mma_commit(bar_o_full);
-            mbar_wait_drain(bar_o_full, 0, p.timeout_ns);
+            if (!(ok = warp_all(mbar_wait(bar_p_ready(1), (uint32_t)j & 1u, ab)))) break;
+            tc_fence_after();
+            issue_pv(1, j);
+            mma_commit_elect(bar_kv_empty(s));
+            if (has_next) issue_s(1, j + 1);
         }
+        mma_commit_elect(bar_o_full);
+        mbar_wait_drain(bar_o_full, 0, p.timeout_ns);
         __syncwarp();
     } else {
         // ======================================== softmax (warps 0-7) ===
