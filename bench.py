@@ -128,6 +128,7 @@ def run_ours(args, rank, world, local_rank):
     import torch.distributed as dist
 
     import differential_attention_diffattn_gb300 as da
+    from differential_attention_diffattn_gb300 import shard
     from differential_attention_diffattn_gb300 import workloads as W
 
     da.build()
@@ -197,10 +198,7 @@ def run_ours(args, rank, world, local_rank):
     fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the timed region")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = shard.max_over_ranks(elapsed_ms)
     ms_step = elapsed_ms / args.steps
     value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
@@ -235,10 +233,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = shard.max_over_ranks(e2e_ms)
     e2e_value = flops_step * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the end-to-end region")
