@@ -284,13 +284,13 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             }
             float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-            for (int e = 4; e < BN; e += 4) {
-                mx0 = fmaxf(mx0, x[e]);
-                mx1 = fmaxf(mx1, x[e + 1]);
-                mx2 = fmaxf(mx2, x[e + 2]);
-                mx3 = fmaxf(mx3, x[e + 3]);
+            for (int e = 4; e < BN; e += 8) {
+                mx0 = fmax3(mx0, x[e], x[e + 1]);
+                mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
+                mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
+                mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
             }
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
             float alpha = 1.f;
             if (m_tile > m + RESCALE_THRESHOLD) {
                 alpha = ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
@@ -298,26 +298,27 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             }
             const float neg_m = -m;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            // P_c (bf16 pairs: column i holds keys 2i (low half) and 2i+1) over S_c, stored
+            // 32 keys at a time so the TMEM stores overlap the next chunk's exponentials.
 #pragma unroll
-            for (int e = 0; e < BN; e += 4) {
-                x[e] = ex2_approx(fmaf(x[e], sl2, neg_m));
-                x[e + 1] = ex2_approx(fmaf(x[e + 1], sl2, neg_m));
-                x[e + 2] = ex2_approx(fmaf(x[e + 2], sl2, neg_m));
-                x[e + 3] = ex2_approx(fmaf(x[e + 3], sl2, neg_m));
-                s0 += x[e];
-                s1 += x[e + 1];
-                s2 += x[e + 2];
-                s3 += x[e + 3];
+            for (int ch = 0; ch < BN / 32; ++ch) {
+#pragma unroll
+                for (int e = ch * 32; e < ch * 32 + 32; e += 4) {
+                    x[e] = ex2_approx(fmaf(x[e], sl2, neg_m));
+                    x[e + 1] = ex2_approx(fmaf(x[e + 1], sl2, neg_m));
+                    x[e + 2] = ex2_approx(fmaf(x[e + 2], sl2, neg_m));
+                    x[e + 3] = ex2_approx(fmaf(x[e + 3], sl2, neg_m));
+                    s0 += x[e];
+                    s1 += x[e + 1];
+                    s2 += x[e + 2];
+                    s3 += x[e + 3];
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(x[ch * 32 + 2 * i], x[ch * 32 + 2 * i + 1]);
+                tmem_st16(t_s + ch * 16, pk);
             }
             l = l * alpha + ((s0 + s1) + (s2 + s3));
-            // P_c (bf16 pairs: column i holds keys 2i (low half) and 2i+1) over S_c.
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[half * 64 + 2 * i], x[half * 64 + 2 * i + 1]);
-                tmem_st32(t_s + half * 32, pk);
-            }
             // O_c holds the sum through tile j-1 here: S_c(j) was issued after PV_c(j-1).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
