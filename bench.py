@@ -275,6 +275,91 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------- cache forward (GPU) ---
+
+def run_ours_kv(args, rank, world, local_rank):
+    """Decode / short query block against a key/value cache. HBM-bound: the
+    metric is algorithmic bytes (valid cache rows of K and V read once, q read,
+    out written) per second."""
+    import torch
+
+    import differential_attention_diffattn_gb300 as da
+    from differential_attention_diffattn_gb300 import shard
+    from differential_attention_diffattn_gb300 import workloads as W
+
+    da.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.KV_WORKLOADS[args.workload]
+    inp = W.generate_kv(wl, seed=args.seed)
+    lens = [int(x) for x in inp.cache_seqlens]
+    kv_row_bytes = wl.num_kv_heads * (2 * wl.d + wl.dv) * 2
+    bytes_step = (sum(lens) * kv_row_bytes + wl.batch * wl.q_len * wl.num_heads * (2 * wl.d + wl.dv) * 2)
+    li = da.diffattn_lambda_init(wl.depth)
+    stream = torch.cuda.current_stream()
+    sets = []
+    for _ in range(2):  # two caches used alternately: a step never starts on an L2-resident cache
+        s = dict(q=inp.q.to(dev), k=inp.k_cache.to(dev), v=inp.v_cache.to(dev))
+        s["out"] = torch.empty(inp.q.shape[:-1] + (wl.dv,), dtype=torch.bfloat16, device=dev)
+        sets.append(s)
+    lvec = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    w = inp.subln_w.to(dev)
+    lens_d = inp.cache_seqlens.to(dev)
+    lam = torch.empty(wl.num_heads if wl.lambda_per_head else 1, dtype=torch.float32, device=dev)
+    desc = da.kv_desc(inp.q, inp.k_cache, inp.v_cache, wl.eps)
+    ws = torch.empty(da.diffattn_fwd_kvcache_workspace_size(desc), dtype=torch.uint8, device=dev)
+
+    def fwd(s):
+        da.diffattn_fwd_kvcache(s["q"], s["k"], s["v"], lam, li, w, cache_seqlens=lens_d, causal=wl.causal,
+                                eps=wl.eps, workspace=ws, out=s["out"], stream=stream)
+
+    for i in range(args.warmup):
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        fwd(sets[i % 2])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = None
+    if rank == 0:
+        visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        sampler = ClockSampler(visible[local_rank].strip() if local_rank < len(visible) else str(local_rank))
+        sampler.start()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        ev[i][0].record(stream)
+        fwd(sets[i % 2])
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the timed region")
+    elapsed_ms = shard.max_over_ranks(t0.elapsed_time(t1))
+    fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    value = bytes_step * world * args.steps / (elapsed_ms * 1e-3) / 1e9
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    achieved = bytes_step / (fwd_ms * 1e-3) / 1e9
+    return {
+        "metric": "diff-attn kv-cache fwd HBM GB/s (decode)", "value": round(value, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": wl.batch, "q_len": wl.q_len, "cache_capacity": wl.capacity,
+                   "cache_tokens": sum(lens), "diff_heads": wl.num_heads, "kv_heads": wl.num_kv_heads, "d": wl.d,
+                   "dv": wl.dv, "causal": wl.causal, "bytes_per_step": bytes_step,
+                   "l2": "two rotating caches, each larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                     "frac": round(achieved / float(pk["hbm_gbs"]), 4), "traffic": None,
+                     "peak_kind": f"{pk_kind} HBM copy bandwidth",
+                     "kernel": "diffattn_decode_split_kernel + diffattn_decode_combine_kernel",
+                     "launch_ms": round(fwd_ms, 5)},
+        "clocks": clocks, "gpu_launches": 3 * args.steps, "impl": "ours",
+    }
+
+
 # --------------------------------------------------------- CPU / oracle ---
 
 def oracle_sample(inp, positions):
@@ -393,7 +478,9 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        line = run_ours(args, rank, world, local_rank)
+        from differential_attention_diffattn_gb300 import workloads as W
+        runner = run_ours_kv if args.workload in W.KV_WORKLOADS else run_ours
+        line = runner(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -8,12 +8,16 @@ from ._lib import (  # noqa: F401
     DTYPE_F32,
     DiffAttnDesc,
     DiffAttnError,
+    DiffAttnKvDesc,
     diffattn_fwd,
+    diffattn_fwd_kvcache,
+    diffattn_fwd_kvcache_workspace_size,
     diffattn_get_device_status,
     diffattn_lambda,
     diffattn_lambda_init,
     diffattn_set_wait_timeout_ns,
     diffattn_status_string,
+    kv_desc,
     load_library,
 )
 from ._build import LIB_PATH, build  # noqa: F401

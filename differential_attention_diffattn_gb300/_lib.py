@@ -18,8 +18,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = r
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 # Names the header declares with external linkage (checked by the ABI tests).
-EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_get_device_status",
-            "diffattn_status_string", "diffattn_set_wait_timeout_ns")
+EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_kvcache_workspace_size",
+            "diffattn_fwd_kvcache", "diffattn_get_device_status", "diffattn_status_string",
+            "diffattn_set_wait_timeout_ns")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -27,6 +28,12 @@ class DiffAttnDesc(ctypes.Structure):
                 ("max_seqlen", ctypes.c_int), ("total_tokens", ctypes.c_int), ("num_heads", ctypes.c_int),
                 ("num_kv_heads", ctypes.c_int), ("d", ctypes.c_int), ("dv", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+class DiffAttnKvDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("cache_capacity", ctypes.c_int),
+                ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("d", ctypes.c_int),
+                ("dv", ctypes.c_int), ("dtype", ctypes.c_int), ("eps", ctypes.c_float), ("num_splits", ctypes.c_int)]
 
 
 class DiffAttnError(RuntimeError):
@@ -58,6 +65,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                      vp, ctypes.c_int, vp, vp, vp]
+        lib.diffattn_fwd_kvcache_workspace_size.restype = ctypes.c_ulonglong
+        lib.diffattn_fwd_kvcache_workspace_size.argtypes = [ctypes.POINTER(DiffAttnKvDesc)]
+        lib.diffattn_fwd_kvcache.restype = ctypes.c_int
+        lib.diffattn_fwd_kvcache.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, ctypes.c_int,
+                                             ctypes.c_float, vp, ctypes.c_int, vp, ctypes.c_ulonglong, vp, vp]
         lib.diffattn_get_device_status.restype = ctypes.c_int
         lib.diffattn_get_device_status.argtypes = [vp]
         lib.diffattn_status_string.restype = ctypes.c_char_p
@@ -184,6 +196,59 @@ def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True,
                           _stream_handle(stream))
     if st != OK:
         raise DiffAttnError(st, "diffattn_fwd")
+    return out
+
+
+def kv_desc(q, k_cache, v_cache, eps: float = 1e-5, num_splits: int = 0) -> DiffAttnKvDesc:
+    """Descriptor of a cache forward from tensor shapes (q [B, q_len, H, 2d],
+    k_cache [B, capacity, Hkv, 2d], v_cache [B, capacity, Hkv, dv])."""
+    import torch
+    if q.dim() != 4 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q, k_cache, v_cache must be 4-D")
+    d = DiffAttnKvDesc()
+    d.batch, d.q_len, d.num_heads = q.shape[0], q.shape[1], q.shape[2]
+    d.cache_capacity, d.num_kv_heads = k_cache.shape[1], k_cache.shape[2]
+    d.d, d.dv = q.shape[3] // 2, v_cache.shape[3]
+    d.dtype = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_F32
+    d.eps, d.num_splits = float(eps), int(num_splits)
+    return d
+
+
+def diffattn_fwd_kvcache_workspace_size(desc: DiffAttnKvDesc) -> int:
+    return int(load_library().diffattn_fwd_kvcache_workspace_size(ctypes.byref(desc)))
+
+
+def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, cache_seqlens=None,
+                         causal: bool = True, eps: float = 1e-5, num_splits: int = 0, workspace=None, out=None,
+                         stream=None):
+    """New queries q [B, q_len, H, 2d] against a cache (k_cache [B, capacity,
+    Hkv, 2d], v_cache [B, capacity, Hkv, dv], cache_seqlens int32 [B] on the
+    device or None). The workspace (scratch for the key splits) is a caller
+    buffer; when None the binding allocates one with torch for this call."""
+    import torch
+    lib = load_library()
+    for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (lam, "lambda"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+    if cache_seqlens is not None:
+        _check_cuda(cache_seqlens, "cache_seqlens")
+        if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != q.shape[0]:
+            raise ValueError("cache_seqlens must be int32 [batch]")
+    desc = kv_desc(q, k_cache, v_cache, eps, num_splits)
+    need = int(lib.diffattn_fwd_kvcache_workspace_size(ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda(workspace, "workspace")
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v_cache.shape[-1],), dtype=q.dtype, device=q.device)
+    _check_cuda(out, "out")
+    H = q.shape[2]
+    st = lib.diffattn_fwd_kvcache(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(cache_seqlens) if cache_seqlens is not None else None, _ptr(lam),
+                                  1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
+                                  1 if causal else 0, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _ptr(out), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_kvcache")
     return out
 
 

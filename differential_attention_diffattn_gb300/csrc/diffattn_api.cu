@@ -69,6 +69,38 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Key-split plan of a cache forward: (number of splits, keys per split).
+// Chooses enough (batch x kv head x split) CTAs to keep every SM streaming,
+// with splits of at least 256 keys; deterministic in the shape.
+bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
+    if (d.batch < 0 || d.q_len < 1 || d.cache_capacity < d.q_len || d.num_heads <= 0 || d.num_kv_heads <= 0 ||
+        d.num_heads % d.num_kv_heads != 0 || d.num_splits < 0)
+        return false;
+    const long long cap = d.cache_capacity;
+    long long n = d.num_splits;
+    if (n == 0) {
+        const long long ctas = (long long)d.batch * d.num_kv_heads;
+        const long long target = 4LL * 152;
+        n = ctas > 0 ? (target + ctas - 1) / ctas : 1;
+        const long long max_n = (cap + 255) / 256;
+        if (n > max_n) n = max_n;
+        if (n < 1) n = 1;
+    }
+    long long c = (cap + n - 1) / n;
+    c = (c + 63) / 64 * 64;
+    n = (cap + c - 1) / c;
+    if (n > 65535) return false;
+    *n_splits = (int)n;
+    *chunk = (int)c;
+    return true;
+}
+
+unsigned long long kv_workspace_bytes(const diffattn_kv_desc& d, int n_splits) {
+    const unsigned long long rows = (unsigned long long)d.batch * d.q_len * d.num_heads * n_splits * 2;
+    const unsigned long long o = rows * (unsigned long long)d.dv * 4;
+    return o + rows * 2 * 4;
+}
+
 }  // namespace
 }  // namespace diffattn
 
@@ -166,6 +198,68 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
     return launch_fwd_bf16_sm103a(p, maps, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+unsigned long long diffattn_fwd_kvcache_workspace_size(const diffattn_kv_desc* desc) {
+    int n = 0, c = 0;
+    if (!desc || !kv_plan(*desc, &n, &c)) return 0;
+    return kv_workspace_bytes(*desc, n);
+}
+
+diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                     const void* v_cache, const int* cache_seqlens, const float* lambda,
+                                     int lambda_per_head, float lambda_init, const float* subln_w, int causal,
+                                     void* workspace, unsigned long long workspace_bytes, void* out,
+                                     void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_kv_desc& ds = *desc;
+    int n_splits = 0, chunk = 0;
+    if (!kv_plan(ds, &n_splits, &chunk)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.d <= 0 || ds.dv != 2 * ds.d) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if ((long long)ds.batch * ds.cache_capacity * ds.num_kv_heads * ds.dv >= (1LL << 40) ||
+        (long long)ds.batch * ds.q_len * ds.num_heads > INT32_MAX || ds.batch > 65535 || ds.num_kv_heads > 65535)
+        return DIFFATTN_ERR_INVALID_ARG;
+    const int rows = ds.q_len * (ds.num_heads / ds.num_kv_heads);
+    if (ds.dtype != DIFFATTN_DTYPE_BF16 || ds.d != 64 || !decode_rows_supported(rows))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    if (ds.batch == 0) return DIFFATTN_OK;
+    if (!q || !k_cache || !v_cache || !lambda || !subln_w || !out || !workspace) return DIFFATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(lambda) & 3u) || (reinterpret_cast<uintptr_t>(subln_w) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < kv_workspace_bytes(ds, n_splits)) return DIFFATTN_ERR_INVALID_ARG;
+
+    unsigned int* err_word = nullptr;
+    if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    KvParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.out = out;
+    p.lambda = lambda;
+    p.subln_w = subln_w;
+    p.cache_seqlens = cache_seqlens;
+    p.error_word = err_word;
+    const unsigned long long rows_total = (unsigned long long)ds.batch * ds.q_len * ds.num_heads * n_splits * 2;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = p.ws_o + rows_total * ds.dv;
+    p.batch = ds.batch;
+    p.q_len = ds.q_len;
+    p.capacity = ds.cache_capacity;
+    p.H = ds.num_heads;
+    p.Hkv = ds.num_kv_heads;
+    p.lambda_stride = lambda_per_head ? 1 : 0;
+    p.causal = causal ? 1 : 0;
+    p.num_splits = n_splits;
+    p.chunk = chunk;
+    p.lambda_init = lambda_init;
+    p.eps = ds.eps;
+    p.scale = (float)(1.0 / std::sqrt((double)ds.d));
+    return launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 
 diffattn_status diffattn_get_device_status(void* stream) {

@@ -44,11 +44,36 @@ struct FwdTensorMaps {
     CUtensorMap q, k, v;
 };
 
+// One forward against a key/value cache (decode / short query blocks).
+struct KvParams {
+    const void* q;             // [batch][q_len][H][2d]
+    const void* k;             // [batch][capacity][Hkv][2d]
+    const void* v;             // [batch][capacity][Hkv][dv]
+    void* out;                 // [batch][q_len][H][dv]
+    const float* lambda;       // [H] or [1]
+    const float* subln_w;      // [dv]
+    const int* cache_seqlens;  // nullptr (all = capacity) or [batch]
+    unsigned int* error_word;
+    float* ws_o;               // [batch*q_len*H][num_splits][2][dv]   partial O per split
+    float* ws_ml;              // [batch*q_len*H][num_splits][2][2]    (m, l) per split
+    int batch, q_len, capacity;
+    int H, Hkv;
+    int lambda_stride;
+    int causal;
+    int num_splits;            // key splits per (batch, kv head)
+    int chunk;                 // keys per split (multiple of 64)
+    float lambda_init;
+    float eps;
+    float scale;               // d^-0.5
+};
+
 // Kernel launchers (each defined in its own translation unit). They return the
 // cudaError_t of the launch.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                           int n_sets, int d, float lambda_init, float* out, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
+cudaError_t launch_decode(const KvParams& p, cudaStream_t stream);
+int decode_rows_supported(int rows);
 
 }  // namespace diffattn

@@ -146,3 +146,73 @@ def generate(wl: Workload, seed: int = 0, seq_lens: Optional[List[int]] = None) 
 def with_overrides(wl: Workload, **kw) -> Workload:
     """A copy of `wl` with some fields replaced (edge-case shapes in tests)."""
     return dataclasses.replace(wl, **kw)
+
+
+# ----------------------------------------------------------------- cache ---
+
+@dataclasses.dataclass(frozen=True)
+class KvWorkload:
+    """New queries against a key/value cache (decode or a short query block)."""
+
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    d: int
+    dv: int
+    depth: int
+    batch: int
+    q_len: int            # new query tokens per sequence
+    capacity: int         # cache rows per sequence
+    len_min: int = 0      # valid cache lengths drawn uniformly from [len_min, capacity];
+                          # 0: every sequence holds `capacity` keys
+    causal: bool = True
+    lambda_per_head: bool = False
+    random_subln: bool = False
+    eps: float = 1e-5
+
+
+KV_WORKLOADS = {
+    # one decoded token per sequence, Llama-3.2-1B-shaped heads (16 diff heads
+    # over 4 kv heads), 16k-token caches
+    "decode_b8_c16384": KvWorkload("decode_b8_c16384", num_heads=16, num_kv_heads=4, d=64, dv=128, depth=12,
+                                   batch=8, q_len=1, capacity=16384),
+    # ragged caches, 4 new tokens per sequence (a short speculative block)
+    "decode_b16_q4_ragged": KvWorkload("decode_b16_q4_ragged", num_heads=16, num_kv_heads=4, d=64, dv=128,
+                                       depth=12, batch=16, q_len=4, capacity=8192, len_min=512),
+}
+
+
+@dataclasses.dataclass
+class KvInputs:
+    wl: KvWorkload
+    cache_seqlens: torch.Tensor   # int32 [batch]
+    q: torch.Tensor               # bf16 [batch, q_len, H, 2d]
+    k_cache: torch.Tensor         # bf16 [batch, capacity, Hkv, 2d]
+    v_cache: torch.Tensor         # bf16 [batch, capacity, Hkv, dv]
+    lambda_q1: torch.Tensor
+    lambda_k1: torch.Tensor
+    lambda_q2: torch.Tensor
+    lambda_k2: torch.Tensor
+    subln_w: torch.Tensor
+
+
+def generate_kv(wl: KvWorkload, seed: int = 0, lengths: Optional[List[int]] = None) -> KvInputs:
+    """Seeded cache inputs. Draw order: cache lengths -> q -> k_cache -> v_cache
+    -> lambda_q1, lambda_k1, lambda_q2, lambda_k2 (-> subln weight). Cache rows
+    beyond a sequence's length hold random values too: they must not matter."""
+    gen = torch.Generator().manual_seed(seed)
+    B, H, Hkv, d, dv = wl.batch, wl.num_heads, wl.num_kv_heads, wl.d, wl.dv
+    if lengths is None:
+        if wl.len_min > 0:
+            lengths = [int(torch.randint(max(wl.len_min, wl.q_len), wl.capacity + 1, (1,), generator=gen))
+                       for _ in range(B)]
+        else:
+            lengths = [wl.capacity] * B
+    lens = torch.tensor(lengths, dtype=torch.int32)
+    q = torch.randn(B, wl.q_len, H, 2 * d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, wl.capacity, Hkv, 2 * d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, wl.capacity, Hkv, dv, generator=gen).to(torch.bfloat16)
+    lshape = (H, d) if wl.lambda_per_head else (d,)
+    lam = [torch.randn(lshape, generator=gen, dtype=torch.float32) * 0.1 for _ in range(4)]
+    w = (torch.rand(dv, generator=gen) + 0.5) if wl.random_subln else torch.ones(dv)
+    return KvInputs(wl, lens, q, k, v, lam[0], lam[1], lam[2], lam[3], w.float())

@@ -134,6 +134,65 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
                              const int* cu_seqlens, void* out, void* stream);
 
 /*
+ * Shape of a forward against a key/value cache (decode, or a short block of new
+ * queries appended to a cached sequence).
+ *  batch sequences; each has q_len new query tokens and a cache of
+ *  cache_capacity key/value rows, of which cache_seqlens[b] are valid (the new
+ *  tokens included: they are the last q_len valid rows).
+ *  num_heads, num_kv_heads, d, dv, dtype, eps as in diffattn_desc.
+ *  num_splits: key splits per (sequence, kv head); 0 lets the library choose
+ *  from the shape (the workspace size depends on it).
+ */
+typedef struct {
+    int batch;
+    int q_len;
+    int cache_capacity;
+    int num_heads;
+    int num_kv_heads;
+    int d;
+    int dv;
+    diffattn_dtype dtype;
+    float eps;
+    int num_splits;
+} diffattn_kv_desc;
+
+/*
+ * Bytes of device workspace diffattn_fwd_kvcache needs for `desc` (partial
+ * softmax states of every key split); 0 for an invalid or empty shape.
+ */
+unsigned long long diffattn_fwd_kvcache_workspace_size(const diffattn_kv_desc* desc);
+
+/*
+ * Differential-attention forward of new queries against a key/value cache.
+ * Query t of sequence b sits at position cache_seqlens[b] - q_len + t and, when
+ * causal, sees cached keys j <= that position: the bottom-right aligned mask
+ * triu(-inf, 1 + src_len - tgt_len) of "Add an isolated implementation of
+ * FlashDiffAttention" (review snippet, alternative_forward), on the cache of
+ * "LlamaDiffSdpaAttention.py" (forward, past_key_value.update with k1, k2
+ * stacked). The per-row arithmetic is that of diffattn_fwd.
+ *  q       : [batch][q_len][H][2d]            bf16
+ *  k_cache : [batch][cache_capacity][Hkv][2d] bf16 (K1 | K2 per kv head)
+ *  v_cache : [batch][cache_capacity][Hkv][dv] bf16
+ *  cache_seqlens : NULL (every sequence holds cache_capacity keys) or device
+ *                  int32 [batch], q_len <= cache_seqlens[b] <= cache_capacity
+ *  workspace : device, >= diffattn_fwd_kvcache_workspace_size(desc) bytes,
+ *              16-byte aligned, owned by the caller; its contents are scratch
+ *  out     : [batch][q_len][H][dv] bf16
+ * Two launches on `stream`: a key-split kernel writing partial (max, sum, O) of
+ * both components to the workspace, and a combine kernel (per-component
+ * log-sum-exp merge, O1/l1 - lambda O2/l2, RMSNorm, weight, (1 - lambda_init)).
+ * Supported: bf16, d = 64, dv = 128, q_len * (H / Hkv) in {1, 2, 4, 8, 16}.
+ * Errors: INVALID_ARG (null / misaligned pointers, bad sizes, workspace too
+ * small), UNSUPPORTED, CUDA; cache_seqlens out of range -> BAD_SEQLENS through
+ * diffattn_get_device_status (those sequences are not written).
+ */
+diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                     const void* v_cache, const int* cache_seqlens, const float* lambda,
+                                     int lambda_per_head, float lambda_init, const float* subln_w,
+                                     int causal, void* workspace, unsigned long long workspace_bytes,
+                                     void* out, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns OK, TIMEOUT, BAD_SEQLENS (first error recorded since the last read),
  * or CUDA if the synchronisation itself failed.

@@ -51,6 +51,42 @@ def oracle_out(inp, rows=None, lam_value=None, lambda_init=None):
                             inp.wl.causal, rows)
 
 
+def run_gpu_kv(inp, dev="cuda", num_splits=0, use_seqlens=True, out=None):
+    """The library's cache forward on `workloads.KvInputs`."""
+    wl = inp.wl
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(inp.lambda_q1.to(dev), inp.lambda_k1.to(dev), inp.lambda_q2.to(dev),
+                             inp.lambda_k2.to(dev), li)
+    y = da.diffattn_fwd_kvcache(inp.q.to(dev), inp.k_cache.to(dev), inp.v_cache.to(dev), lam, li,
+                                inp.subln_w.to(dev), cache_seqlens=inp.cache_seqlens.to(dev) if use_seqlens else None,
+                                causal=wl.causal, eps=wl.eps, num_splits=num_splits, out=out)
+    st = da.diffattn_get_device_status()
+    assert st == 0, da.diffattn_status_string(st)
+    return y
+
+
+def oracle_kv(inp, batches=None):
+    """Oracle for cache inputs: sequence b is its first L_b cache rows with the
+    new queries as its last q_len tokens; the oracle's causal rows at those
+    positions are the bottom-right-masked queries. Returns [len(batches), q_len, H, dv]."""
+    wl = inp.wl
+    li = orc.lambda_init(wl.depth)
+    lam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, li)
+    batches = range(wl.batch) if batches is None else batches
+    H, ql = wl.num_heads, wl.q_len
+    res = []
+    for b in batches:
+        L = int(inp.cache_seqlens[b])
+        q_full = np.zeros((L, H, 2 * wl.d))
+        q_full[L - ql:] = inp.q[b].double().numpy()
+        tt = np.repeat(np.arange(L - ql, L, dtype=np.int32), H)
+        hh = np.tile(np.arange(H, dtype=np.int32), ql)
+        y = orc.forward_rows([0, L], q_full, inp.k_cache[b, :L], inp.v_cache[b, :L], lam, li, inp.subln_w,
+                             wl.eps, wl.causal, rows=(tt, hh))
+        res.append(y.reshape(ql, H, wl.dv))
+    return np.stack(res)
+
+
 def sample_rows(inp, every=61, edge=128):
     """Every `every`-th query row of every head plus the first and last `edge`
     rows of every sequence (rows are independent, so sampling is exact)."""

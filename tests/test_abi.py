@@ -23,8 +23,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(diffattn_[a-z0-9_]+)\s*\(",
-                                 src, flags=re.M)))
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \t\*]*?\b(diffattn_[a-z0-9_]+)\s*\(", src, flags=re.M)))
 
 
 def test_header_declares_the_abi():

@@ -1,0 +1,82 @@
+"""GPU parity of the cache forward (decode / short query blocks) against the
+fp64 oracle, element by element, including the split-merge edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_diffattn_gb300 as da
+from differential_attention_diffattn_gb300 import workloads as W
+
+from gpu_util import compare, oracle_kv, run_gpu_kv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    da.build()
+    da.load_library()
+    torch.cuda.set_device(0)
+
+
+def kvw(**kw):
+    base = dict(num_heads=16, num_kv_heads=4, d=64, dv=128, depth=12, batch=3, q_len=1, capacity=1000)
+    base.update(kw)
+    return W.KvWorkload("t", **base)
+
+
+@pytest.mark.parametrize("H,Hkv,ql", [(16, 4, 1), (4, 4, 1), (8, 4, 1), (16, 16, 2), (16, 4, 2), (16, 4, 4),
+                                      (16, 1, 1), (8, 8, 2)])
+def test_rows_per_kv_head(H, Hkv, ql):
+    wl = kvw(num_heads=H, num_kv_heads=Hkv, q_len=ql)
+    inp = W.generate_kv(wl, seed=H + Hkv + ql, lengths=[1000, 517, ql])
+    compare(run_gpu_kv(inp), oracle_kv(inp), "bf16")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16])
+def test_forced_splits(splits):
+    inp = W.generate_kv(kvw(batch=2, capacity=2000), seed=40 + splits, lengths=[2000, 65])
+    compare(run_gpu_kv(inp, num_splits=splits), oracle_kv(inp), "bf16")
+
+
+def test_non_causal_and_per_head_lambda():
+    wl = kvw(q_len=4, causal=False, lambda_per_head=True, random_subln=True)
+    inp = W.generate_kv(wl, seed=50, lengths=[1000, 300, 4])
+    compare(run_gpu_kv(inp), oracle_kv(inp), "bf16")
+
+
+def test_full_caches_without_lengths():
+    inp = W.generate_kv(kvw(batch=2, capacity=777), seed=51)
+    compare(run_gpu_kv(inp, use_seqlens=False), oracle_kv(inp), "bf16")
+
+
+@pytest.mark.parametrize("name", ["decode_b8_c16384", "decode_b16_q4_ragged"])
+def test_cache_workloads(name):
+    inp = W.generate_kv(W.KV_WORKLOADS[name], seed=0)
+    got = run_gpu_kv(inp)
+    assert torch.isfinite(got.float()).all()
+    b_sel = [0, inp.wl.batch // 2, inp.wl.batch - 1]
+    compare(got[b_sel], oracle_kv(inp, b_sel), "bf16")
+
+
+def test_bad_cache_lengths_reported():
+    inp = W.generate_kv(kvw(batch=2, q_len=2), seed=52, lengths=[1000, 1])  # 1 < q_len
+    with pytest.raises(AssertionError):
+        run_gpu_kv(inp)
+    assert da.diffattn_get_device_status() == 0
+    good = W.generate_kv(kvw(batch=2, q_len=2), seed=52, lengths=[1000, 2])
+    compare(run_gpu_kv(good), oracle_kv(good), "bf16")
+
+
+def test_unsupported_rows():
+    inp = W.generate_kv(kvw(q_len=3), seed=53)  # 3 * 4 = 12 rows per kv head
+    with pytest.raises(da.DiffAttnError) as e:
+        run_gpu_kv(inp)
+    assert e.value.status == 2
+
+
+def test_deterministic_and_workspace_reuse():
+    inp = W.generate_kv(kvw(batch=2), seed=54, lengths=[999, 400])
+    a = run_gpu_kv(inp)
+    b = run_gpu_kv(inp)
+    assert torch.equal(a, b)

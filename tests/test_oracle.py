@@ -238,10 +238,40 @@ def pin_rows_subset(lib=None):
     np.testing.assert_array_equal(part, full[tok, hd])
 
 
+def pin_bottom_right_mask(lib=None):
+    """New queries at the end of a cached sequence: the oracle rows of the last
+    q_len positions equal the map form with the bottom-right mask
+    triu(-inf, 1 + src_len - tgt_len) of the FlashDiffAttention review snippet
+    (tgt_len = q_len queries against src_len = L keys), written out in NumPy."""
+    g = np.random.default_rng(7)
+    L, ql, H, Hkv, d = 11, 4, 4, 2, 8
+    q_new = g.normal(size=(ql, H, 2 * d))
+    k = g.normal(size=(L, Hkv, 2 * d))
+    v = g.normal(size=(L, Hkv, 2 * d))
+    w = g.uniform(0.5, 1.5, size=2 * d)
+    lam, li, eps = np.array([0.3, 0.9, -0.2, 1.4]), 0.55, 1e-5
+    q_full = np.zeros((L, H, 2 * d))
+    q_full[L - ql:] = q_new
+    tt = np.repeat(np.arange(L - ql, L, dtype=np.int32), H)
+    hh = np.tile(np.arange(H, dtype=np.int32), ql)
+    got = orc.forward_rows([0, L], q_full, k, v, lam, li, w, eps, True, rows=(tt, hh), lib=lib).reshape(ql, H, -1)
+    mask = np.triu(np.full((ql, L), -np.inf), 1 + L - ql)
+    for h in range(H):
+        kv = h // (H // Hkv)
+        maps = []
+        for c in range(2):
+            a = q_new[:, h, c * d:(c + 1) * d] @ k[:, kv, c * d:(c + 1) * d].T * d ** -0.5 + mask
+            a = np.exp(a - a.max(axis=1, keepdims=True))
+            maps.append(a / a.sum(axis=1, keepdims=True))
+        o = (maps[0] - lam[h] * maps[1]) @ v[:, kv, :]
+        want = o / np.sqrt(np.mean(o ** 2, axis=-1, keepdims=True) + eps) * w * (1 - li)
+        np.testing.assert_allclose(got[:, h], want, atol=TOL, rtol=0)
+
+
 PINS = [pin_lambda_init, pin_lambda_special, pin_hand_example, pin_lambda_zero_is_sdpa,
         pin_equal_components, pin_row0_closed_form, pin_uniform_scores, pin_map_form,
         pin_scale_invariance, pin_gqa_equals_replicated, pin_packed_equals_separate,
-        pin_head_permutation, pin_rows_subset]
+        pin_head_permutation, pin_rows_subset, pin_bottom_right_mask]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
