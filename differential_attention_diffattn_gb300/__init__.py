@@ -11,6 +11,7 @@ from ._lib import (  # noqa: F401
     DiffAttnKvDesc,
     diffattn_fwd,
     diffattn_fwd_kvcache,
+    diffattn_fwd_kvcache_noalloc,
     diffattn_fwd_kvcache_workspace_size,
     diffattn_get_device_status,
     diffattn_lambda,

@@ -19,7 +19,8 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 
 # Names the header declares with external linkage (checked by the ABI tests).
 EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_kvcache_workspace_size",
-            "diffattn_fwd_kvcache", "diffattn_get_device_status", "diffattn_status_string",
+            "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
+            "diffattn_status_string",
             "diffattn_set_wait_timeout_ns")
 
 
@@ -70,6 +71,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_fwd_kvcache.restype = ctypes.c_int
         lib.diffattn_fwd_kvcache.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, ctypes.c_int,
                                              ctypes.c_float, vp, ctypes.c_int, vp, ctypes.c_ulonglong, vp, vp]
+        lib.diffattn_fwd_kvcache_noalloc.restype = ctypes.c_int
+        lib.diffattn_fwd_kvcache_noalloc.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, ctypes.c_int,
+                                                     ctypes.c_float, vp, ctypes.c_int, vp, vp]
         lib.diffattn_get_device_status.restype = ctypes.c_int
         lib.diffattn_get_device_status.argtypes = [vp]
         lib.diffattn_status_string.restype = ctypes.c_char_p
@@ -249,6 +253,34 @@ def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, 
                                   _ptr(out), _stream_handle(stream))
     if st != OK:
         raise DiffAttnError(st, "diffattn_fwd_kvcache")
+    return out
+
+
+def diffattn_fwd_kvcache_noalloc(q, k_cache, v_cache, lam, lambda_init: float, subln_w, cache_seqlens=None,
+                                 causal: bool = True, eps: float = 1e-5, num_splits: int = 0, out=None,
+                                 stream=None):
+    """diffattn_fwd_kvcache whose key-split scratch is the library's static device
+    array instead of a workspace. The C entry point allocates nothing; only the
+    output tensor is created here when `out` is None."""
+    import torch
+    lib = load_library()
+    for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (lam, "lambda"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+    if cache_seqlens is not None:
+        _check_cuda(cache_seqlens, "cache_seqlens")
+        if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != q.shape[0]:
+            raise ValueError("cache_seqlens must be int32 [batch]")
+    desc = kv_desc(q, k_cache, v_cache, eps, num_splits)
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v_cache.shape[-1],), dtype=q.dtype, device=q.device)
+    _check_cuda(out, "out")
+    H = q.shape[2]
+    st = lib.diffattn_fwd_kvcache_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(cache_seqlens) if cache_seqlens is not None else None, _ptr(lam),
+                                          1 if (lam.numel() == H and H > 1) else 0, float(lambda_init),
+                                          _ptr(subln_w), 1 if causal else 0, _ptr(out), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_kvcache_noalloc")
     return out
 
 

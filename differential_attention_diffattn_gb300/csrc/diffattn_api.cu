@@ -262,6 +262,55 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
     return launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 
+}  // extern "C"
+
+// ---- allocation-free cache forward -------------------------------------------
+// The key-split partials of diffattn_fwd_kvcache_noalloc live in this array
+// (one per device, for the life of the process). Host code must not use the
+// array's name as an address: on the host it is only a stand-in, so the device
+// address is looked up once per device and cached.
+namespace diffattn {
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DIFFATTN_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call per device, with that device current).
+cudaError_t noalloc_scratch_ptr(void** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+}  // namespace diffattn
+
+extern "C" {
+
+diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                             const void* v_cache, const int* cache_seqlens, const float* lambda,
+                                             int lambda_per_head, float lambda_init, const float* subln_w,
+                                             int causal, void* out, void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const unsigned long long need = diffattn_fwd_kvcache_workspace_size(desc);
+    if (need > DIFFATTN_NOALLOC_SCRATCH_BYTES) return DIFFATTN_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (need > 0 && desc->batch > 0) {
+        if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    }
+    return diffattn_fwd_kvcache(desc, q, k_cache, v_cache, cache_seqlens, lambda, lambda_per_head, lambda_init,
+                                subln_w, causal, scratch, DIFFATTN_NOALLOC_SCRATCH_BYTES, out, stream);
+}
+
 diffattn_status diffattn_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     unsigned int word = 0;

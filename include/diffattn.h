@@ -193,6 +193,39 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
                                      void* out, void* stream);
 
 /*
+ * Size of the scratch array behind diffattn_fwd_kvcache_noalloc: 16 MiB of
+ * device memory per GPU that loads the library, held until the process exits.
+ */
+#define DIFFATTN_NOALLOC_SCRATCH_BYTES (16ull << 20)
+
+/*
+ * diffattn_fwd_kvcache without a workspace argument, for callers that cannot
+ * allocate device memory themselves: code embedded in a host program that owns
+ * every device allocation (a serving runtime with a fixed memory arena, a
+ * plugin interface that hands the library no allocator), or a caller on a
+ * latency-critical path where a device allocation, which may synchronise the
+ * device, is not acceptable. No counterpart on the pages: this is a calling
+ * convention of this library, not part of the method.
+ * The key-split partials go to one static device array of
+ * DIFFATTN_NOALLOC_SCRATCH_BYTES instead of a caller workspace; the function
+ * itself allocates nothing. Arguments and results are those of
+ * diffattn_fwd_kvcache. The first call on a device looks up the array's device
+ * address (once per device, with that device current); make that first call
+ * before any stream capture. Every call on a device shares the one array:
+ * calls that overlap on the GPU (different streams, or different host threads)
+ * race on it and must be serialised by the caller. Nothing in the array has to
+ * start at zero: each call writes every partial it later reads.
+ * Errors: as diffattn_fwd_kvcache, plus DIFFATTN_ERR_UNSUPPORTED when the shape
+ * needs more than DIFFATTN_NOALLOC_SCRATCH_BYTES of partials (see
+ * diffattn_fwd_kvcache_workspace_size; fewer key splits need less), and
+ * DIFFATTN_ERR_CUDA if the address lookup fails.
+ */
+diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                             const void* v_cache, const int* cache_seqlens, const float* lambda,
+                                             int lambda_per_head, float lambda_init, const float* subln_w,
+                                             int causal, void* out, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns OK, TIMEOUT, BAD_SEQLENS (first error recorded since the last read),
  * or CUDA if the synchronisation itself failed.
