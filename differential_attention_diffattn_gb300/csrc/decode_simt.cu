@@ -148,9 +148,12 @@ diffattn_decode_split_kernel(const KvParams p) {
         m_run[i] = -INFINITY;
         l_run[i] = 0.f;
     }
-    float acc[PAIRS];  // column tid of O for every pair
+    // P V: thread owns value columns 2*cp, 2*cp+1 for the keys of half kh of
+    // each tile; the two halves are added once, at the end of the split.
+    const int cp = tid & 63, kh = tid >> 6;
+    float acc[PAIRS][2];
 #pragma unroll
-    for (int i = 0; i < PAIRS; ++i) acc[i] = 0.f;
+    for (int i = 0; i < PAIRS; ++i) acc[i][0] = acc[i][1] = 0.f;
     const float sl2 = p.scale * LOG2E;
 
     load_tile(0, 0);
@@ -212,23 +215,49 @@ diffattn_decode_split_kernel(const KvParams p) {
             }
         }
         __syncthreads();
-        // ---- O += P V: thread owns value column tid for every pair
+        // ---- O += P V (probabilities as float4 broadcasts, values as bf16 pairs)
         {
-            const __nv_bfloat16* vcol = vs + (size_t)buf * TK * DVD + tid;
+            const uint32_t* vrow = reinterpret_cast<const uint32_t*>(vs + (size_t)buf * TK * DVD) + cp;
 #pragma unroll
-            for (int pr = 0; pr < PAIRS; ++pr) acc[pr] *= alpha_s[pr];
-#pragma unroll 4
-            for (int j = 0; j < TK; ++j) {
-                const float vv = __bfloat162float(vcol[j * DVD]);
+            for (int pr = 0; pr < PAIRS; ++pr) {
+                acc[pr][0] *= alpha_s[pr];
+                acc[pr][1] *= alpha_s[pr];
+            }
+#pragma unroll 2
+            for (int j = kh * (TK / 2); j < kh * (TK / 2) + TK / 2; j += 4) {
+                float vx[4], vy[4];
 #pragma unroll
-                for (int pr = 0; pr < PAIRS; ++pr) acc[pr] = fmaf(ps[pr * TK + j], vv, acc[pr]);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint32_t w2 = vrow[(j + jj) * (DVD / 2)];
+                    vx[jj] = __uint_as_float(w2 << 16);
+                    vy[jj] = __uint_as_float(w2 & 0xffff0000u);
+                }
+#pragma unroll
+                for (int pr = 0; pr < PAIRS; ++pr) {
+                    const float4 pp = *reinterpret_cast<const float4*>(ps + pr * TK + j);
+                    acc[pr][0] = fmaf(pp.x, vx[0], fmaf(pp.y, vx[1], fmaf(pp.z, vx[2], fmaf(pp.w, vx[3], acc[pr][0]))));
+                    acc[pr][1] = fmaf(pp.x, vy[0], fmaf(pp.y, vy[1], fmaf(pp.z, vy[2], fmaf(pp.w, vy[3], acc[pr][1]))));
+                }
             }
         }
         __syncthreads();  // the buffer is refilled by the next iteration's copy
     }
-    // ---- partials
+    // ---- partials: add the two key halves (through the K buffers, now idle), write O
+    float* red = reinterpret_cast<float*>(ks);  // [PAIRS][DVD] floats <= 2 K buffers
+    static_assert((size_t)PAIRS * DVD * 4 <= 2 * DecodeSmemLayout::k_tile, "reduction buffer");
+    if (kh == 1) {
 #pragma unroll
-    for (int pr = 0; pr < PAIRS; ++pr) p.ws_o[(slot(pr >> 1) * 2 + (pr & 1)) * DVD + tid] = acc[pr];
+        for (int pr = 0; pr < PAIRS; ++pr) *reinterpret_cast<float2*>(red + pr * DVD + 2 * cp) = make_float2(acc[pr][0], acc[pr][1]);
+    }
+    __syncthreads();
+    if (kh == 0) {
+#pragma unroll
+        for (int pr = 0; pr < PAIRS; ++pr) {
+            const float2 o = *reinterpret_cast<const float2*>(red + pr * DVD + 2 * cp);
+            *reinterpret_cast<float2*>(p.ws_o + (slot(pr >> 1) * 2 + (pr & 1)) * DVD + 2 * cp) =
+                make_float2(acc[pr][0] + o.x, acc[pr][1] + o.y);
+        }
+    }
 #pragma unroll
     for (int i = 0; i < PPW; ++i) {
         const int pr = warp + 4 * i;
@@ -277,10 +306,14 @@ diffattn_decode_combine_kernel(const KvParams p) {
     static_cast<__nv_bfloat16*>(p.out)[(size_t)row * DVD + tid] = __float2bfloat16_rn(y);
 }
 
+size_t split_smem_bytes(int R) {
+    return (size_t)R * 2 * DK * 4 + 2 * DecodeSmemLayout::k_tile + 2 * DecodeSmemLayout::v_tile +
+           (size_t)R * 2 * TK * 4 + (size_t)R * 2 * 4;
+}
+
 template <int R>
 cudaError_t launch_split(const KvParams& p, cudaStream_t stream) {
-    const size_t smem = (size_t)R * 2 * DK * 4 + 2 * DecodeSmemLayout::k_tile + 2 * DecodeSmemLayout::v_tile +
-                        (size_t)R * 2 * TK * 4 + (size_t)R * 2 * 4;
+    const size_t smem = split_smem_bytes(R);
     static bool attr_done[64] = {false};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -299,6 +332,13 @@ cudaError_t launch_split(const KvParams& p, cudaStream_t stream) {
 }  // namespace
 
 int decode_rows_supported(int rows) { return rows == 1 || rows == 2 || rows == 4 || rows == 8 || rows == 16; }
+
+int decode_ctas_per_sm(int rows) {
+    // 232448 bytes of shared memory per SM usable by blocks, 1 KB reserved per block
+    const size_t per = split_smem_bytes(rows) + 1024;
+    const int n = (int)(232448 / per);
+    return n < 1 ? 1 : (n > 8 ? 8 : n);
+}
 
 cudaError_t launch_decode(const KvParams& p, cudaStream_t stream) {
     const int R = p.q_len * (p.H / p.Hkv);

@@ -69,26 +69,45 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Key-split plan of a cache forward: (number of splits, keys per split).
-// Chooses enough (batch x kv head x split) CTAs to keep every SM streaming,
-// with splits of at least 256 keys; deterministic in the shape.
+// Key-split plan of a cache forward: (number of splits, keys per split), with
+// splits of at least 256 keys (64-key multiples). Without a requested count it
+// tries 1 to 4 full waves of resident split CTAs on the 152 SMs and keeps the
+// count that leaves the fewest idle CTA slots in the last wave (later waves
+// win ties: finer splits balance ragged caches). Deterministic in the shape.
 bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
     if (d.batch < 0 || d.q_len < 1 || d.cache_capacity < d.q_len || d.num_heads <= 0 || d.num_kv_heads <= 0 ||
         d.num_heads % d.num_kv_heads != 0 || d.num_splits < 0)
         return false;
     const long long cap = d.cache_capacity;
-    long long n = d.num_splits;
+    auto round_plan = [&](long long n, long long* c_out) {
+        long long c = (cap + n - 1) / n;
+        c = (c + 63) / 64 * 64;
+        *c_out = c;
+        return (cap + c - 1) / c;
+    };
+    long long n = d.num_splits, c = 0;
     if (n == 0) {
         const long long ctas = (long long)d.batch * d.num_kv_heads;
-        const long long target = 4LL * 152;
-        n = ctas > 0 ? (target + ctas - 1) / ctas : 1;
+        const int rows = d.q_len * (d.num_heads / d.num_kv_heads);
+        const long long slots = 152LL * (decode_rows_supported(rows) ? decode_ctas_per_sm(rows) : 1);
         const long long max_n = (cap + 255) / 256;
-        if (n > max_n) n = max_n;
-        if (n < 1) n = 1;
+        double best = -1.0;
+        n = 1;
+        for (long long waves = 1; waves <= 4 && ctas > 0; ++waves) {
+            long long cand = waves * slots / ctas;
+            if (cand < 1) cand = 1;
+            if (cand > max_n) cand = max_n;
+            long long cc;
+            cand = round_plan(cand, &cc);
+            const long long total = cand * ctas;
+            const double fill = (double)total / (double)(((total + slots - 1) / slots) * slots);
+            if (fill >= best - 1e-9) {
+                best = fill;
+                n = cand;
+            }
+        }
     }
-    long long c = (cap + n - 1) / n;
-    c = (c + 63) / 64 * 64;
-    n = (cap + c - 1) / c;
+    n = round_plan(n, &c);
     if (n > 65535) return false;
     *n_splits = (int)n;
     *chunk = (int)c;
