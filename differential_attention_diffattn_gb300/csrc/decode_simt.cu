@@ -269,7 +269,11 @@ diffattn_decode_split_kernel(const KvParams p) {
     }
 }
 
-// One CTA (128 threads = 128 value columns) per (batch, query, head).
+// One CTA (128 threads = 128 value columns) per (batch, query, head). The
+// (m, l) of every split are staged in shared memory by parallel loads, the
+// split weights 2^(m_s - M) computed once, then every thread sums its column.
+constexpr int MAX_COMBINE_SPLITS = 1024;
+
 __global__ void __launch_bounds__(DVD)
 diffattn_decode_combine_kernel(const KvParams p) {
     const int row = blockIdx.x;  // ((b * q_len) + t) * H + h
@@ -278,29 +282,51 @@ diffattn_decode_combine_kernel(const KvParams p) {
     const int tid = threadIdx.x;
     const int L = p.cache_seqlens ? p.cache_seqlens[b] : p.capacity;
     if (L < p.q_len || L > p.capacity) return;  // reported by the split kernel
-    __shared__ float red[DVD / 32];
+    __shared__ float wgt[2][MAX_COMBINE_SPLITS];  // m_s, then 2^(m_s - M)
+    __shared__ float lsm[2][MAX_COMBINE_SPLITS];
+    __shared__ float red[2][DVD / 32];
+    __shared__ float mmax[2];
+    const int n = p.num_splits;
+    const float* ml = p.ws_ml + (size_t)row * n * 4;  // [split][component][m, l]
+    for (int i = tid; i < 2 * n; i += DVD) {
+        const int s_ = i >> 1, c = i & 1;
+        wgt[c][s_] = ml[(s_ * 2 + c) * 2];
+        lsm[c][s_] = ml[(s_ * 2 + c) * 2 + 1];
+    }
+    __syncthreads();
+    if (tid < 64) {  // warp 0: max of component 0, warp 1: component 1
+        const int c = tid >> 5, ln = tid & 31;
+        float m = -INFINITY;
+        for (int s_ = ln; s_ < n; s_ += 32) m = fmaxf(m, wgt[c][s_]);
+        m = warp_max(m);
+        if (ln == 0) mmax[c] = m;
+    }
+    __syncthreads();
+    for (int i = tid; i < 2 * n; i += DVD) {
+        const int s_ = i >> 1, c = i & 1;
+        const float ms = wgt[c][s_];
+        wgt[c][s_] = ms == -INFINITY ? 0.f : exp2f(ms - mmax[c]);  // empty splits weigh nothing
+    }
+    __syncthreads();
     float o[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-        float M = -INFINITY;
-        for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.ws_ml[(((size_t)row * p.num_splits + s) * 2 + c) * 2]);
         float lsum = 0.f, acc = 0.f;
-        for (int s = 0; s < p.num_splits; ++s) {
-            const size_t sl = ((size_t)row * p.num_splits + s) * 2 + c;
-            const float ms = p.ws_ml[sl * 2];
-            if (ms == -INFINITY) continue;  // empty split
-            const float w = exp2f(ms - M);
-            lsum = fmaf(p.ws_ml[sl * 2 + 1], w, lsum);
-            acc = fmaf(p.ws_o[sl * DVD + tid], w, acc);
+        const float* op = p.ws_o + ((size_t)row * n * 2 + c) * DVD + tid;
+#pragma unroll 4
+        for (int s_ = 0; s_ < n; ++s_) {
+            const float wv = wgt[c][s_];
+            lsum = fmaf(lsm[c][s_], wv, lsum);
+            acc = fmaf(op[(size_t)s_ * 2 * DVD], wv, acc);
         }
         o[c] = acc / lsum;
     }
     const float lam = p.lambda[h * p.lambda_stride];
     const float dval = o[0] - lam * o[1];
     float ss = warp_sum(dval * dval);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    if ((tid & 31) == 0) red[0][tid >> 5] = ss;
     __syncthreads();
-    ss = red[0] + red[1] + red[2] + red[3];
+    ss = red[0][0] + red[0][1] + red[0][2] + red[0][3];
     const float rinv = 1.f / sqrtf(ss / (float)DVD + p.eps);
     const float y = dval * rinv * p.subln_w[tid] * (1.f - p.lambda_init);
     static_cast<__nv_bfloat16*>(p.out)[(size_t)row * DVD + tid] = __float2bfloat16_rn(y);
@@ -332,6 +358,8 @@ cudaError_t launch_split(const KvParams& p, cudaStream_t stream) {
 }  // namespace
 
 int decode_rows_supported(int rows) { return rows == 1 || rows == 2 || rows == 4 || rows == 8 || rows == 16; }
+
+int decode_max_splits() { return MAX_COMBINE_SPLITS; }
 
 int decode_ctas_per_sm(int rows) {
     // 232448 bytes of shared memory per SM usable by blocks, 1 KB reserved per block

@@ -108,7 +108,7 @@ bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
         }
     }
     n = round_plan(n, &c);
-    if (n > 65535) return false;
+    if (n > decode_max_splits()) return false;
     *n_splits = (int)n;
     *chunk = (int)c;
     return true;

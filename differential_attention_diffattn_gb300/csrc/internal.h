@@ -76,5 +76,6 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
 cudaError_t launch_decode(const KvParams& p, cudaStream_t stream);
 int decode_rows_supported(int rows);
 int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
+int decode_max_splits();           // most key splits the combine kernel merges
 
 }  // namespace diffattn

@@ -140,8 +140,8 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
  *  cache_capacity key/value rows, of which cache_seqlens[b] are valid (the new
  *  tokens included: they are the last q_len valid rows).
  *  num_heads, num_kv_heads, d, dv, dtype, eps as in diffattn_desc.
- *  num_splits: key splits per (sequence, kv head); 0 lets the library choose
- *  from the shape (the workspace size depends on it).
+ *  num_splits: key splits per (sequence, kv head), at most 1024; 0 lets the
+ *  library choose from the shape (the workspace size depends on it).
  */
 typedef struct {
     int batch;
