@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     diffattn_get_device_status,
     diffattn_lambda,
     diffattn_lambda_init,
+    diffattn_set_fault_injection,
     diffattn_set_wait_timeout_ns,
     diffattn_status_string,
     kv_desc,

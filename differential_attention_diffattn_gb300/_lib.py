@@ -20,8 +20,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 # Names the header declares with external linkage (checked by the ABI tests).
 EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
-            "diffattn_status_string",
-            "diffattn_set_wait_timeout_ns")
+            "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -80,6 +79,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_status_string.argtypes = [ctypes.c_int]
         lib.diffattn_set_wait_timeout_ns.restype = None
         lib.diffattn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.diffattn_set_fault_injection.restype = None
+        lib.diffattn_set_fault_injection.argtypes = [ctypes.c_int]
         del fp, ip
         if path is None:
             _lib = lib
@@ -295,3 +296,7 @@ def diffattn_status_string(status: int) -> str:
 
 def diffattn_set_wait_timeout_ns(ns: int) -> None:
     load_library().diffattn_set_wait_timeout_ns(int(ns))
+
+
+def diffattn_set_fault_injection(mode: int) -> None:
+    load_library().diffattn_set_fault_injection(int(mode))

@@ -18,6 +18,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_error_ptr[kMaxDevices] = {nullptr};
 unsigned long long g_timeout_ns = kDefaultWaitTimeoutNs;
+int g_inject = 0;
 
 cudaError_t error_word_ptr(unsigned int** out) {
     int dev = 0;
@@ -207,6 +208,7 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     p.scale = (float)(1.0 / std::sqrt((double)ds.d));
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
     p.timeout_ns = g_timeout_ns;
+    p.inject = g_inject;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
@@ -356,5 +358,7 @@ const char* diffattn_status_string(diffattn_status s) {
 }
 
 void diffattn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : kDefaultWaitTimeoutNs; }
+
+void diffattn_set_fault_injection(int mode) { g_inject = mode == 1 ? 1 : 0; }
 
 }  // extern "C"

@@ -169,7 +169,9 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 
     if (warp == PRODUCER_WARP) {
         // ================================================= TMA producer ===
-        if (lane == 0) {
+        // With the test hook set, no load is issued: the barriers the other roles
+        // wait on are never armed, so their bounded waits run out.
+        if (lane == 0 && p.inject != 1) {
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
             const int row_q = start + qt * BM;

@@ -37,6 +37,7 @@ struct FwdParams {
     float scale_log2;         // d^-0.5 * log2(e)
     float scale;              // d^-0.5
     unsigned long long timeout_ns;
+    int inject;               // test hook: 1 = the copy producer issues no loads
 };
 
 // TMA descriptors of the bf16 operands, built on the host per call.

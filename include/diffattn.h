@@ -242,6 +242,16 @@ const char* diffattn_status_string(diffattn_status status);
  */
 void diffattn_set_wait_timeout_ns(unsigned long long ns);
 
+/*
+ * Test hook (no paper counterpart) for failure detection. mode 1: the copy
+ * producer of the bf16 forward kernel issues no loads, so the barriers every
+ * other role waits on are never armed; each wait runs out after the wait limit,
+ * the kernel records DIFFATTN_ERR_TIMEOUT, frees its tensor memory and returns,
+ * and diffattn_get_device_status reports it. mode 0 (the default) turns it off.
+ * Affects launches made after the call; nothing faults, traps or hangs.
+ */
+void diffattn_set_fault_injection(int mode);
+
 #ifdef __cplusplus
 }
 #endif
