@@ -9,12 +9,15 @@ from ._lib import (  # noqa: F401
     DiffAttnDesc,
     DiffAttnError,
     DiffAttnKvDesc,
+    diffattn_bwd,
     diffattn_fwd,
+    diffattn_fwd_train,
     diffattn_fwd_kvcache,
     diffattn_fwd_kvcache_noalloc,
     diffattn_fwd_kvcache_workspace_size,
     diffattn_get_device_status,
     diffattn_lambda,
+    diffattn_lambda_bwd,
     diffattn_lambda_init,
     diffattn_set_fault_injection,
     diffattn_set_wait_timeout_ns,

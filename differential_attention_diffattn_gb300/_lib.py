@@ -18,7 +18,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = r
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 # Names the header declares with external linkage (checked by the ABI tests).
-EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_kvcache_workspace_size",
+EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_train",
+            "diffattn_bwd_workspace_size", "diffattn_bwd", "diffattn_lambda_bwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection")
 
@@ -65,6 +66,16 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                      vp, ctypes.c_int, vp, vp, vp]
+        lib.diffattn_fwd_train.restype = ctypes.c_int
+        lib.diffattn_fwd_train.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
+                                           vp, ctypes.c_int, vp, vp, vp, vp, vp, vp]
+        lib.diffattn_bwd_workspace_size.restype = ctypes.c_ulonglong
+        lib.diffattn_bwd_workspace_size.argtypes = [ctypes.POINTER(DiffAttnDesc)]
+        lib.diffattn_bwd.restype = ctypes.c_int
+        lib.diffattn_bwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float, vp,
+                                     ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_ulonglong, vp]
+        lib.diffattn_lambda_bwd.restype = ctypes.c_int
+        lib.diffattn_lambda_bwd.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp]
         lib.diffattn_fwd_kvcache_workspace_size.restype = ctypes.c_ulonglong
         lib.diffattn_fwd_kvcache_workspace_size.argtypes = [ctypes.POINTER(DiffAttnKvDesc)]
         lib.diffattn_fwd_kvcache.restype = ctypes.c_int
@@ -136,6 +147,115 @@ def diffattn_lambda(lq1, lk1, lq2, lk2, lambda_init: float, out=None, stream=Non
     if st != OK:
         raise DiffAttnError(st, "diffattn_lambda")
     return out
+
+
+def _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps):
+    """Checks shared by the forward entry points; returns (desc, H)."""
+    import torch
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (lam, "lambda"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+    if q.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    if lam.dtype != torch.float32 or subln_w.dtype != torch.float32:
+        raise ValueError("lambda and subln_w must be fp32")
+    desc = DiffAttnDesc()
+    if q.dim() == 4:
+        if cu_seqlens is not None:
+            raise ValueError("cu_seqlens goes with token-major [tokens, H, 2d] inputs")
+        B, T, H, two_d = q.shape
+        desc.batch, desc.seqlen = B, T
+    elif q.dim() == 3:
+        tokens, H, two_d = q.shape
+        if cu_seqlens is None:
+            desc.batch, desc.seqlen = 1, tokens
+        else:
+            _check_cuda(cu_seqlens, "cu_seqlens")
+            if cu_seqlens.dtype != torch.int32:
+                raise ValueError("cu_seqlens must be int32")
+            if max_seqlen is None:
+                raise ValueError("max_seqlen is required with cu_seqlens")
+            desc.num_seqs = cu_seqlens.numel() - 1
+            desc.max_seqlen = int(max_seqlen)
+            desc.total_tokens = tokens
+    else:
+        raise ValueError("q must be [B, T, H, 2d] or [tokens, H, 2d]")
+    Hkv, dv = k.shape[-2], v.shape[-1]
+    desc.num_heads, desc.num_kv_heads = H, Hkv
+    desc.d, desc.dv = two_d // 2, dv
+    desc.dtype = dt
+    desc.eps = float(eps)
+    if k.shape[:-2] != q.shape[:-2] or v.shape[:-2] != q.shape[:-2] or v.shape[-2] != Hkv:
+        raise ValueError("q, k, v token dimensions or kv heads disagree")
+    if lam.numel() not in (1, H):
+        raise ValueError("lambda must hold 1 or H values")
+    return desc, H
+
+
+def diffattn_fwd_train(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,
+                       max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, stream=None):
+    """Forward that also returns what diffattn_bwd needs: (out, lse, o1, o2) with
+    lse fp32 [..., H, 2] and o1, o2 fp32 [..., H, dv]."""
+    import torch
+    lib = load_library()
+    desc, H = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
+    shp = q.shape[:-1]
+    if out is None:
+        out = torch.empty(shp + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    lse = torch.empty(shp + (2,), dtype=torch.float32, device=q.device)
+    o1 = torch.empty(shp + (v.shape[-1],), dtype=torch.float32, device=q.device)
+    o2 = torch.empty_like(o1)
+    st = lib.diffattn_fwd_train(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
+                                1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
+                                1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(out),
+                                _ptr(lse), _ptr(o1), _ptr(o2), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_train")
+    return out, lse, o1, o2
+
+
+def diffattn_bwd(q, k, v, lam, lambda_init: float, subln_w, dout, lse, o1, o2, causal: bool = True,
+                 cu_seqlens=None, max_seqlen: Optional[int] = None, eps: float = 1e-5, workspace=None,
+                 stream=None):
+    """Gradients (dq, dk, dv, dlambda, dsubln_w) of diffattn_fwd_train's output."""
+    import torch
+    lib = load_library()
+    desc, H = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
+    for t, name in ((dout, "dout"), (lse, "lse"), (o1, "o1"), (o2, "o2")):
+        _check_cuda(t, name)
+    need = int(lib.diffattn_bwd_workspace_size(ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dlam = torch.empty(lam.numel() if (lam.numel() == H and H > 1) else 1, dtype=torch.float32, device=q.device)
+    dw = torch.empty_like(subln_w)
+    st = lib.diffattn_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
+                          1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
+                          1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(dout),
+                          _ptr(lse), _ptr(o1), _ptr(o2), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlam), _ptr(dw),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_bwd")
+    return dq, dk, dv, dlam, dw
+
+
+def diffattn_lambda_bwd(lq1, lk1, lq2, lk2, dlambda, stream=None):
+    """Gradients of the four lambda vectors from the gradient of lambda."""
+    import torch
+    lib = load_library()
+    d = lq1.shape[-1]
+    n = 1 if lq1.dim() == 1 else lq1.shape[0]
+    outs = [torch.empty_like(lq1) for _ in range(4)]
+    st = lib.diffattn_lambda_bwd(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), _ptr(dlambda), n, d,
+                                 *[_ptr(o) for o in outs], _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_lambda_bwd")
+    return tuple(outs)
 
 
 def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,

@@ -1,0 +1,145 @@
+// CUDA-core parts of the backward pass: the per-row preprocessing (gradient of
+// the per-head RMSNorm and the output scale, the row deltas of the two
+// softmaxes, and the lambda / norm-weight gradients) and the gradient of the
+// lambda reparameterisation.
+//
+// Per (token, head) row, with D = O1 - lambda O2, r = sqrt(mean(D^2) + eps),
+// y = D / r * w * (1 - lambda_init) ("DiffTransformer.py",
+// MultiHeadDifferentialAttention.forward, "Normalize each head independently
+// using RMSNorm", "Scale the normalized output") and u = dy * w * (1 - lambda_init):
+//   dD      = u / r - D * <u, D> / (dv r^3)
+//   delta_c = <dD, O_c>               (O_c the normalised attention output)
+//   dlambda -= <dD, O2>               (D depends on lambda through -lambda O2)
+//   dw     += dy * D / r * (1 - lambda_init)
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace diffattn {
+namespace {
+
+constexpr int DVD = 128;
+constexpr int ROWS_PER_WARP = 16;
+constexpr int WARPS = 4;
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ void load4(const void* base, size_t idx, float (&f)[4]) {
+    const uint2 u = reinterpret_cast<const uint2*>(base)[idx];
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
+// Warp w of block (x, h) handles rows t = (x * WARPS + w) * ROWS_PER_WARP .. +15 of head h;
+// lane l owns value columns 4l .. 4l+3.
+__global__ void __launch_bounds__(32 * WARPS)
+diffattn_bwd_pre_kernel(const BwdPreParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int t0 = (blockIdx.x * WARPS + warp) * ROWS_PER_WARP;
+    const float lam = p.lambda[h * p.lambda_stride];
+    const float post = 1.f - p.lambda_init;
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = p.subln_w[4 * lane + i];
+    float dw[4] = {0.f, 0.f, 0.f, 0.f};
+    float dlam = 0.f;
+    for (int t = t0; t < min(t0 + ROWS_PER_WARP, p.tokens); ++t) {
+        const size_t row = (size_t)t * p.H + h;
+        float dy[4], o1[4], o2[4], D[4], u[4];
+        load4(p.dout, row * (DVD / 4) + lane, dy);
+        const float4 a1 = reinterpret_cast<const float4*>(p.o1)[row * (DVD / 4) + lane];
+        const float4 a2 = reinterpret_cast<const float4*>(p.o2)[row * (DVD / 4) + lane];
+        o1[0] = a1.x; o1[1] = a1.y; o1[2] = a1.z; o1[3] = a1.w;
+        o2[0] = a2.x; o2[1] = a2.y; o2[2] = a2.z; o2[3] = a2.w;
+        float ss = 0.f, ud = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            D[i] = o1[i] - lam * o2[i];
+            u[i] = dy[i] * w[i] * post;
+            ss = fmaf(D[i], D[i], ss);
+            ud = fmaf(u[i], D[i], ud);
+        }
+        ss = warp_sum(ss);
+        ud = warp_sum(ud);
+        const float rinv = 1.f / sqrtf(ss / (float)DVD + p.eps);
+        const float corr = ud * rinv * rinv * rinv / (float)DVD;
+        float dd[4], d1 = 0.f, d2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            dd[i] = u[i] * rinv - D[i] * corr;
+            d1 = fmaf(dd[i], o1[i], d1);
+            d2 = fmaf(dd[i], o2[i], d2);
+            dw[i] = fmaf(dy[i], D[i] * rinv * post, dw[i]);
+        }
+        d1 = warp_sum(d1);
+        d2 = warp_sum(d2);
+        dlam -= d2;
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(dd[0], dd[1]);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(dd[2], dd[3]);
+        uint2 st;
+        st.x = *reinterpret_cast<uint32_t*>(&lo2);
+        st.y = *reinterpret_cast<uint32_t*>(&hi2);
+        reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
+        if (lane == 0) {
+            const float2 l2 = reinterpret_cast<const float2*>(p.lse)[row];
+            reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(l2.x, l2.y, d1, d2);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) atomicAdd(p.dsubln_w + 4 * lane + i, dw[i]);
+    if (lane == 0) atomicAdd(p.dlambda + h * p.lambda_stride, dlam);
+}
+
+// One warp per lambda parameter set:
+//   dlq1 = dl e^a lk1, dlk1 = dl e^a lq1, dlq2 = -dl e^b lk2, dlk2 = -dl e^b lq2,
+//   a = lq1 . lk1, b = lq2 . lk2   (derivative of "Compute lambda using reparameterization").
+__global__ void diffattn_lambda_bwd_kernel(const float* __restrict__ lq1, const float* __restrict__ lk1,
+                                           const float* __restrict__ lq2, const float* __restrict__ lk2,
+                                           const float* __restrict__ dl, int n_sets, int d, float* dlq1,
+                                           float* dlk1, float* dlq2, float* dlk2) {
+    const int set = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (set >= n_sets) return;
+    const size_t base = (size_t)set * d;
+    float a = 0.f, b = 0.f;
+    for (int e = lane; e < d; e += 32) {
+        a = fmaf(lq1[base + e], lk1[base + e], a);
+        b = fmaf(lq2[base + e], lk2[base + e], b);
+    }
+    a = warp_sum(a);
+    b = warp_sum(b);
+    const float ga = dl[set] * expf(a), gb = -dl[set] * expf(b);
+    for (int e = lane; e < d; e += 32) {
+        dlq1[base + e] = ga * lk1[base + e];
+        dlk1[base + e] = ga * lq1[base + e];
+        dlq2[base + e] = gb * lk2[base + e];
+        dlk2[base + e] = gb * lq2[base + e];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
+    const int rows_per_block = WARPS * ROWS_PER_WARP;
+    dim3 grid((unsigned)((p.tokens + rows_per_block - 1) / rows_per_block), (unsigned)p.H);
+    diffattn_bwd_pre_kernel<<<grid, 32 * WARPS, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                              const float* dlambda, int n_sets, int d, float* dlq1, float* dlk1, float* dlq2,
+                              float* dlk2, cudaStream_t stream) {
+    const int warps = 4;
+    diffattn_lambda_bwd_kernel<<<(n_sets + warps - 1) / warps, 32 * warps, 0, stream>>>(
+        lq1, lk1, lq2, lk2, dlambda, n_sets, d, dlq1, dlk1, dlq2, dlk2);
+    return cudaGetLastError();
+}
+
+}  // namespace diffattn

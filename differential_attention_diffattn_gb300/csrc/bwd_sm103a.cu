@@ -1,0 +1,540 @@
+// Backward pass of the differential-attention forward on sm_103a (bf16
+// operands, fp32 accumulation in tensor memory), d = 64, dv = 128.
+//
+// With D = O1 - lambda O2 (O_c = softmax(s Q_c K_c^T) V) and dD the gradient of
+// the pre-norm output (from the per-row preprocessing kernel), the two
+// components see dO_1 = dD and dO_2 = -lambda dD, so one product dP = dD V^T
+// serves both, and per (query row i, key j):
+//   P_c  = 2^(s log2(e) <Q_c[i], K_c[j]> - lse_c[i])                (saved by the forward)
+//   dS_1 = P_1 (dP - delta_1[i]),  dS_2 = -lambda P_2 (dP - delta_2[i])
+//   delta_c[i] = <dD[i], O_c[i] / l_c[i]>                        (preprocessing)
+//   dQ_c += s dS_c K_c,  dK_c += s dS_c^T Q_c,  dV += (P_1 - lambda P_2)^T dD
+// (the derivative of softmax(...) V through "DiffTransformer.py",
+// MultiHeadDifferentialAttention.forward, in the output-difference form of
+// "LlamaDiffSdpaAttention.py", forward).
+//
+// Two kernels, each a TMA producer warp, an MMA warp (elected lane issues) and
+// one warpgroup of 128 threads that owns one TMEM lane each:
+//   dQ kernel : CTA = 128 query rows of one head; walks the visible 128-key
+//               tiles. TMEM: S1 [0,128), S2 [128,256), dP [256,384),
+//               dQ1 [384,448), dQ2 [448,512); dS_c (bf16) over S_c.
+//   dKV kernel: CTA = 128 keys of one kv head; walks the heads of its group and
+//               the 64-row query blocks that see its keys. With keys as the MMA
+//               rows: S_c^T [0,64) [64,128), dP^T [128,192), dV [192,320),
+//               dK1 [320,384), dK2 [384,448); the bf16 operands P_1 - lambda P_2,
+//               dS_1^T, dS_2^T go over S1^T, S2^T, dP^T.
+// Every wait is bounded; on a timeout a CTA records the error, lets its copies
+// and MMAs land, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace diffattn {
+namespace {
+
+constexpr int HD = 64;
+constexpr int DV = 128;
+constexpr uint32_t ROW = 128;                      // bytes of one swizzled row (64 bf16)
+constexpr int NT = 192;                            // 4 compute warps + producer + MMA
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t a) { return smem_desc_sw128(a, 16, 1024); }
+// MN-major operand whose N extent is split in 64-wide boxes `box` bytes apart.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t a, uint32_t box) { return smem_desc_sw128(a, box, 1024); }
+__device__ __forceinline__ bool warp_all(bool p) { return __all_sync(0xffffffffu, p); }
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// ---- sequence bounds (uniform over the CTA); false: nothing to do / bad lengths
+__device__ __forceinline__ bool seq_bounds(const BwdParams& p, int seq, int* start, int* len) {
+    if (p.cu_seqlens != nullptr) {
+        const int s0 = p.cu_seqlens[seq], s1 = p.cu_seqlens[seq + 1];
+        const bool bad = s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen ||
+                         (seq == 0 && s0 != 0) || (seq == p.num_seqs - 1 && s1 != p.total_tokens);
+        if (bad) {
+            if (threadIdx.x == 0) atomicOr(p.error_word, kErrBadSeqlens);
+            return false;
+        }
+        *start = s0;
+        *len = s1 - s0;
+    } else {
+        *start = seq * p.seqlen;
+        *len = p.seqlen;
+    }
+    return true;
+}
+
+// =============================================================== dQ ===
+namespace dq {
+constexpr int BM = 128, BN = 128, STAGES = 2;
+constexpr uint32_t BOX = 128 * ROW;                // [128 x 64] bf16 box: 16 KB
+constexpr uint32_t OFF_Q = 0;                      // Q1 | Q2
+constexpr uint32_t OFF_DD = 2 * BOX;               // dD (two 64-column halves)
+constexpr uint32_t OFF_ST = 4 * BOX;               // stages: K1 | K2 | V lo | V hi
+constexpr uint32_t STAGE = 4 * BOX;
+constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
+constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
+static_assert(SMEM <= 232448, "smem");
+struct Misc {
+    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready, ds_ready, dq_done;
+    uint32_t tmem;
+    int abort_flag;
+};
+}  // namespace dq
+
+__global__ void __launch_bounds__(NT, 1)
+diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dd,
+                       const BwdParams p) {
+    using namespace dq;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x, seq = blockIdx.z;
+    const int qt = gridDim.y - 1 - blockIdx.y;
+    int start = 0, len = 0;
+    if (!seq_bounds(p, seq, &start, &len)) return;
+    if (qt * BM >= len) return;
+    const int n_kv = p.causal ? qt + 1 : (len + BN - 1) / BN;
+    const int g = h / (p.H / p.Hkv);
+
+    const uint32_t b_q = smem_u32(&ms.q_full), b_s = smem_u32(&ms.s_ready), b_ds = smem_u32(&ms.ds_ready),
+                   b_dq = smem_u32(&ms.dq_done);
+    auto b_kf = [&](int s) { return smem_u32(&ms.kv_full[s]); };
+    auto b_ke = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    if (warp == PRODUCER_WARP && lane == 0) {
+        mbar_init(b_q, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_kf(s), 1);
+            mbar_init(b_ke(s), 1);
+        }
+        mbar_init(b_s, 1);
+        mbar_init(b_ds, 128);
+        mbar_init(b_dq, 1);
+        ms.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem;
+    const AbortState ab{&ms.abort_flag, p.error_word, p.timeout_ns};
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            const int row_q = start + qt * BM;
+            mbar_arrive_expect_tx(b_q, 4 * BOX);
+            tma_load_2d(sb + OFF_Q, &tm_q, b_q, h * 2 * HD, row_q, pol);
+            tma_load_2d(sb + OFF_Q + BOX, &tm_q, b_q, h * 2 * HD + HD, row_q, pol);
+            tma_load_2d(sb + OFF_DD, &tm_dd, b_q, h * DV, row_q, pol);
+            tma_load_2d(sb + OFF_DD + BOX, &tm_dd, b_q, h * DV + 64, row_q, pol);
+            int issued = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % STAGES;
+                if (!mbar_wait(b_ke(s), ((uint32_t)(j / STAGES) & 1u) ^ 1u, ab)) break;
+                const uint32_t st = sb + OFF_ST + (uint32_t)s * STAGE;
+                const int row = start + j * BN;
+                mbar_arrive_expect_tx(b_kf(s), STAGE);
+                tma_load_2d(st, &tm_k, b_kf(s), g * 2 * HD, row, pol);
+                tma_load_2d(st + BOX, &tm_k, b_kf(s), g * 2 * HD + HD, row, pol);
+                tma_load_2d(st + 2 * BOX, &tm_v, b_kf(s), g * DV, row, pol);
+                tma_load_2d(st + 3 * BOX, &tm_v, b_kf(s), g * DV + 64, row, pol);
+                issued = j + 1;
+            }
+            mbar_wait_drain(b_q, 0, p.timeout_ns);
+            for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+                mbar_wait_drain(b_kf(j % STAGES), (uint32_t)(j / STAGES) & 1u, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false);   // S_c, dP: both operands K-major
+        constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true);    // dQ_c: B = K_c is MN-major (d contiguous)
+        const uint64_t dq_q = desc_k(sb + OFF_Q), dq_dd = desc_k(sb + OFF_DD);
+        const uint64_t dk0 = desc_k(sb + OFF_ST), dkm = desc_mn(sb + OFF_ST, BOX);
+        constexpr uint64_t KS = 32 >> 4, BX = BOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
+        bool ok = warp_all(mbar_wait(b_q, 0, ab));
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int s = j % STAGES;
+            if (!(ok = warp_all(mbar_wait(b_kf(s), (uint32_t)(j / STAGES) & 1u, ab)))) break;
+            tc_fence_after();
+            const uint64_t st_k = dk0 + (uint64_t)s * SG;
+            for (int c = 0; c < 2; ++c) {  // S_c = Q_c K_c^T, K = d = 64
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_elect(tmem + c * 128, dq_q + c * BX + kk * KS, st_k + c * BX + kk * KS, id_s, kk > 0);
+            }
+            // dP = dD V^T, K = dv = 128: the two 64-column halves of dD and of V
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ss_elect(tmem + 256, dq_dd + (kk >> 2) * BX + (kk & 3) * KS,
+                             st_k + 2 * BX + (kk >> 2) * BX + (kk & 3) * KS, id_s, kk > 0);
+            mma_commit_elect(b_s);
+            if (!(ok = warp_all(mbar_wait(b_ds, (uint32_t)j & 1u, ab)))) break;
+            tc_fence_after();
+            // dQ_c += dS_c K_c: A = dS_c (bf16 in TMEM, K = keys), B = K_c rows (MN-major)
+            const uint64_t st_km = dkm + (uint64_t)s * SG;
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts_elect(tmem + 384 + c * 64, tmem + c * 128 + kk * 8, st_km + c * BX + kk * KR, id_dq,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_elect(b_ke(s));
+        }
+        mma_commit_elect(b_dq);
+        mbar_wait_drain(b_dq, 0, p.timeout_ns);
+        __syncwarp();
+    } else {
+        // ================================================ compute warpgroup ===
+        const int r = warp * 32 + lane;  // query row in the tile = TMEM lane
+        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        const int qi = qt * BM + r;
+        const bool row_ok = qi < len;
+        const size_t grow = (size_t)(start + (row_ok ? qi : 0));
+        float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);  // lse1, lse2, delta1, delta2
+        if (row_ok) rs = reinterpret_cast<const float4*>(p.rowstat)[(size_t)h * p.total_tokens + grow];
+        const float lam = p.lambda[h * p.lambda_stride];
+        const float sl2 = p.scale_log2, sc = p.scale;
+        const int lim = row_ok ? (p.causal ? min(qi + 1, len) : len) : 0;  // keys < lim are visible
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)j & 1u, ab)))) break;
+            tc_fence_after();
+            const int kb = j * BN;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t s1[32], s2[32], dp[32];
+                tmem_ld32(tmem + lo + ch * 32, s1);
+                tmem_ld32(tmem + lo + 128 + ch * 32, s2);
+                tmem_ld32(tmem + lo + 256 + ch * 32, dp);
+                tmem_wait_ld();
+                uint32_t d1[16], d2[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float a[2], b2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int e = ch * 32 + i + u;
+                        const bool vis = kb + e < lim;
+                        const float pp = __uint_as_float(dp[i + u]);
+                        const float p1 = vis ? ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -rs.x)) : 0.f;
+                        const float p2 = vis ? ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -rs.y)) : 0.f;
+                        a[u] = p1 * (pp - rs.z) * sc;
+                        b2[u] = -lam * p2 * (pp - rs.w) * sc;
+                    }
+                    d1[i / 2] = pack_bf16x2(a[0], a[1]);
+                    d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
+                }
+                // dS_c of keys [32 ch, 32 ch + 32) -> columns [16 ch, 16 ch + 16) of S_c (already read)
+                tmem_st16(tmem + lo + ch * 16, d1);
+                tmem_st16(tmem + lo + 128 + ch * 16, d2);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_ds);
+        }
+        ok = ok && warp_all(mbar_wait(b_dq, 0, ab));
+        // ok is warp-uniform; row_ok is not: every lane takes part in the (warp-wide)
+        // TMEM loads and only the global stores depend on the row.
+        if (ok) {
+            tc_fence_after();
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (grow * p.H + h) * (2 * HD));
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {  // dQ1 = columns 0..63, dQ2 = 64..127 of the output row
+                uint32_t o[32];
+                tmem_ld32(tmem + lo + 384 + ch * 32, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================== dKV ===
+namespace dkv {
+constexpr int BK = 128, BQ = 64, STAGES = 3;
+constexpr uint32_t KBOX = 128 * ROW;               // [128 keys x 64] 16 KB
+constexpr uint32_t QBOX = 64 * ROW;                // [64 rows x 64] 8 KB
+constexpr uint32_t OFF_K = 0;                      // K1 | K2
+constexpr uint32_t OFF_V = 2 * KBOX;               // V lo | V hi
+constexpr uint32_t OFF_ST = 4 * KBOX;              // stages: Q1 | Q2 | dD lo | dD hi | row stats
+constexpr uint32_t ST_STAT = 4 * QBOX;
+constexpr uint32_t STAGE = 4 * QBOX + 1024;
+constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
+constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
+static_assert(SMEM <= 232448, "smem");
+struct Misc {
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready, ds_ready, acc_done;
+    uint32_t tmem;
+    int abort_flag;
+};
+}  // namespace dkv
+
+__global__ void __launch_bounds__(NT, 1)
+diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dd,
+                        const BwdParams p) {
+    using namespace dkv;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.x, seq = blockIdx.z;
+    const int kt = gridDim.y - 1 - blockIdx.y;
+    int start = 0, len = 0;
+    if (!seq_bounds(p, seq, &start, &len)) return;
+    if (kt * BK >= len) return;
+    const int G = p.H / p.Hkv;
+    const int qb0 = p.causal ? (kt * BK) / BQ : 0;          // first query block that sees these keys
+    const int nqb = (len + BQ - 1) / BQ - qb0;             // query blocks per head
+    const int n_items = G * nqb;                            // (head, query block) items
+
+    const uint32_t b_kv = smem_u32(&ms.kv_full), b_s = smem_u32(&ms.s_ready), b_ds = smem_u32(&ms.ds_ready),
+                   b_acc = smem_u32(&ms.acc_done);
+    auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
+    auto b_se = [&](int s) { return smem_u32(&ms.st_empty[s]); };
+    auto item_head = [&](int it) { return g * G + it / nqb; };
+    auto item_row0 = [&](int it) { return (qb0 + it % nqb) * BQ; };  // first query position of the block
+    if (warp == PRODUCER_WARP && lane == 0) {
+        mbar_init(b_kv, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(b_sf(s), 1);
+            mbar_init(b_se(s), 1);
+        }
+        mbar_init(b_s, 1);
+        mbar_init(b_ds, 128);
+        mbar_init(b_acc, 1);
+        ms.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem;
+    const AbortState ab{&ms.abort_flag, p.error_word, p.timeout_ns};
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            const int row_k = start + kt * BK;
+            mbar_arrive_expect_tx(b_kv, 4 * KBOX);
+            tma_load_2d(sb + OFF_K, &tm_k, b_kv, g * 2 * HD, row_k, pol);
+            tma_load_2d(sb + OFF_K + KBOX, &tm_k, b_kv, g * 2 * HD + HD, row_k, pol);
+            tma_load_2d(sb + OFF_V, &tm_v, b_kv, g * DV, row_k, pol);
+            tma_load_2d(sb + OFF_V + KBOX, &tm_v, b_kv, g * DV + 64, row_k, pol);
+            int issued = 0;
+            for (int it = 0; it < n_items; ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(b_se(s), ((uint32_t)(it / STAGES) & 1u) ^ 1u, ab)) break;
+                const uint32_t st = sb + OFF_ST + (uint32_t)s * STAGE;
+                const int hh = item_head(it);
+                const int t0 = start + item_row0(it);
+                const int nrow = min(BQ, p.total_tokens - t0);  // row stats past the last token are not read
+                const uint32_t stat_bytes = (uint32_t)nrow * 16u;
+                mbar_arrive_expect_tx(b_sf(s), 4 * QBOX + stat_bytes);
+                tma_load_2d(st, &tm_q, b_sf(s), hh * 2 * HD, t0, pol);
+                tma_load_2d(st + QBOX, &tm_q, b_sf(s), hh * 2 * HD + HD, t0, pol);
+                tma_load_2d(st + 2 * QBOX, &tm_dd, b_sf(s), hh * DV, t0, pol);
+                tma_load_2d(st + 3 * QBOX, &tm_dd, b_sf(s), hh * DV + 64, t0, pol);
+                bulk_load(st + ST_STAT, p.rowstat + ((size_t)hh * p.total_tokens + t0) * 4, stat_bytes, b_sf(s));
+                issued = it + 1;
+            }
+            mbar_wait_drain(b_kv, 0, p.timeout_ns);
+            for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
+                mbar_wait_drain(b_sf(it % STAGES), (uint32_t)(it / STAGES) & 1u, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false);    // S_c^T, dP^T: N = 64 query rows
+        constexpr uint32_t id_v = idesc_bf16_f32(128, 128, true);    // dV: B = dD rows, MN-major (dv)
+        constexpr uint32_t id_k = idesc_bf16_f32(128, 64, true);     // dK_c: B = Q_c rows, MN-major (d)
+        constexpr uint64_t KS = 32 >> 4, KB = KBOX >> 4, QB = QBOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
+        const uint64_t d_k = desc_k(sb + OFF_K), d_v = desc_k(sb + OFF_V);
+        const uint64_t d_q = desc_k(sb + OFF_ST), d_qm = desc_mn(sb + OFF_ST, QBOX);
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab));
+        for (int it = 0; ok && it < n_items; ++it) {
+            const int s = it % STAGES;
+            if (!(ok = warp_all(mbar_wait(b_sf(s), (uint32_t)(it / STAGES) & 1u, ab)))) break;
+            tc_fence_after();
+            const uint64_t sq = d_q + (uint64_t)s * SG;
+            for (int c = 0; c < 2; ++c) {  // S_c^T = K_c Q_c^T, K = d
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss_elect(tmem + c * 64, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
+            }
+            // dP^T = V dD^T, K = dv = 128 over the two 64-column halves
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ss_elect(tmem + 128, d_v + (kk >> 2) * KB + (kk & 3) * KS, sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS,
+                             id_s, kk > 0);
+            mma_commit_elect(b_s);
+            if (!(ok = warp_all(mbar_wait(b_ds, (uint32_t)it & 1u, ab)))) break;
+            tc_fence_after();
+            const uint64_t sqm = d_qm + (uint64_t)s * SG;
+            // dV += (P1 - lambda P2)^T-rows dD: A = TMEM [0,32), K = 64 query rows
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts_elect(tmem + 192, tmem + kk * 8, sqm + 2 * QB + kk * KR, id_v, (it > 0 || kk > 0) ? 1u : 0u);
+            // dK_c += dS_c^T-rows Q_c: A = TMEM [64,96) / [128,160)
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts_elect(tmem + 320 + c * 64, tmem + 64 + c * 64 + kk * 8, sqm + c * QB + kk * KR, id_k,
+                                 (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_elect(b_se(s));
+        }
+        mma_commit_elect(b_acc);
+        mbar_wait_drain(b_acc, 0, p.timeout_ns);
+        __syncwarp();
+    } else {
+        // ================================================ compute warpgroup ===
+        const int k = warp * 32 + lane;  // key in the tile = TMEM lane
+        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        const int kj = kt * BK + k;      // key position in the sequence
+        const bool key_ok = kj < len;
+        const float sl2 = p.scale_log2, sc = p.scale;
+        bool ok = true;
+        for (int it = 0; it < n_items; ++it) {
+            if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)it & 1u, ab)))) break;
+            tc_fence_after();
+            const int s = it % STAGES;
+            const float4* stat = reinterpret_cast<const float4*>(smem + OFF_ST + (uint32_t)s * STAGE + ST_STAT);
+            const int hh = item_head(it);
+            const float lam = p.lambda[hh * p.lambda_stride];
+            const int row0 = item_row0(it);
+#pragma unroll 1
+            for (int ch = 0; ch < 2; ++ch) {  // query rows [32 ch, 32 ch + 32) of the block
+                uint32_t s1[32], s2[32], dp[32];
+                tmem_ld32(tmem + lo + ch * 32, s1);
+                tmem_ld32(tmem + lo + 64 + ch * 32, s2);
+                tmem_ld32(tmem + lo + 128 + ch * 32, dp);
+                tmem_wait_ld();
+                uint32_t pc[16], d1[16], d2[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float a[2], b1[2], b2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int rr = ch * 32 + i + u;
+                        const int qi = row0 + rr;
+                        const bool vis = key_ok && qi < len && (!p.causal || kj <= qi);
+                        const float4 st = stat[rr];  // lse1, lse2, delta1, delta2 of query row rr
+                        const float pp = __uint_as_float(dp[i + u]);
+                        const float p1 = vis ? ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x)) : 0.f;
+                        const float p2 = vis ? ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y)) : 0.f;
+                        a[u] = p1 - lam * p2;
+                        b1[u] = vis ? p1 * (pp - st.z) * sc : 0.f;
+                        b2[u] = vis ? -lam * p2 * (pp - st.w) * sc : 0.f;
+                    }
+                    pc[i / 2] = pack_bf16x2(a[0], a[1]);
+                    d1[i / 2] = pack_bf16x2(b1[0], b1[1]);
+                    d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
+                }
+                // rows [32 ch, +32) -> columns [16 ch, +16) of the S1^T / S2^T / dP^T regions (already read)
+                tmem_st16(tmem + lo + ch * 16, pc);
+                tmem_st16(tmem + lo + 64 + ch * 16, d1);
+                tmem_st16(tmem + lo + 128 + ch * 16, d2);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(b_ds);
+        }
+        ok = ok && warp_all(mbar_wait(b_acc, 0, ab));
+        // ok is warp-uniform; key_ok is not: every lane takes part in the (warp-wide)
+        // TMEM loads and only the global stores depend on the key.
+        if (ok) {
+            tc_fence_after();
+            const size_t grow = (size_t)(start + (key_ok ? kj : 0));
+            uint4* dvp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + (grow * p.Hkv + g) * DV);
+            uint4* dkp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + (grow * p.Hkv + g) * (2 * HD));
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lo + 192 + ch * 32, o);   // dV columns [32 ch, +32)
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+                if (key_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dvp[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+                tmem_ld32(tmem + lo + 320 + ch * 32, o);   // dK1 | dK2 columns [32 ch, +32)
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+                if (key_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dkp[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, uint32_t bytes, bool* done) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !done[dev]) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (err != cudaSuccess) return err;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& m, cudaStream_t stream) {
+    static bool dq_done[64] = {false}, dkv_done[64] = {false};
+    cudaError_t err = set_smem(diffattn_bwd_dq_kernel, dq::SMEM, dq_done);
+    if (err != cudaSuccess) return err;
+    err = set_smem(diffattn_bwd_dkv_kernel, dkv::SMEM, dkv_done);
+    if (err != cudaSuccess) return err;
+    const int n_qt = (p.max_seqlen + dq::BM - 1) / dq::BM;
+    diffattn_bwd_dq_kernel<<<dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs), NT, dq::SMEM, stream>>>(
+        m.q128, m.k128, m.v128, m.dd128, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int n_kt = (p.max_seqlen + dkv::BK - 1) / dkv::BK;
+    diffattn_bwd_dkv_kernel<<<dim3((unsigned)p.Hkv, (unsigned)n_kt, (unsigned)p.num_seqs), NT, dkv::SMEM, stream>>>(
+        m.q64, m.k128, m.v128, m.dd64, p);
+    return cudaGetLastError();
+}
+
+}  // namespace diffattn

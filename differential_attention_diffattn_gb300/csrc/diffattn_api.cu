@@ -56,12 +56,13 @@ EncodeTiledFn encode_tiled_fn() {
 
 // 2-D bf16 map over a [rows][row_elems] row-major tensor; box = 64 elements
 // (128 bytes, 128-byte swizzle) x 128 rows. Rows past the end read as zero.
-bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, uint64_t rows) {
+bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, uint64_t rows,
+                      uint32_t box_rows = 128) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {row_elems, rows};
     const cuuint64_t strides[1] = {row_elems * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -143,10 +144,20 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
     return DIFFATTN_OK;
 }
 
-diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
-                             const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
-                             int causal, const int* cu_seqlens, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+// Shared body of diffattn_fwd and diffattn_fwd_train; lse, o1, o2 are all null
+// (inference) or all set (training outputs, bf16 tcgen05 kernel only).
+diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                           const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
+                           int causal, const int* cu_seqlens, void* out, float* lse, void* o1, void* o2,
+                           void* stream) {
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const bool train = lse != nullptr || o1 != nullptr || o2 != nullptr;
+    if (train && (!lse || !o1 || !o2 || !aligned16(o1) || !aligned16(o2) ||
+                  (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_desc& ds = *desc;
     if (ds.num_heads <= 0 || ds.num_kv_heads <= 0 || ds.num_heads % ds.num_kv_heads != 0 || ds.num_heads > 65535)
         return DIFFATTN_ERR_INVALID_ARG;
@@ -181,6 +192,7 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     const bool bf16_tc = ds.dtype == DIFFATTN_DTYPE_BF16 && ds.d == 64;
     const bool f32_simt = ds.dtype == DIFFATTN_DTYPE_F32 && (ds.d == 16 || ds.d == 32 || ds.d == 64);
     if (!bf16_tc && !f32_simt) return DIFFATTN_ERR_UNSUPPORTED;
+    if (train && !bf16_tc) return DIFFATTN_ERR_UNSUPPORTED;
 
     // An empty problem launches nothing; its tensor pointers may be NULL.
     if (p.total_tokens == 0 || p.num_seqs == 0 || p.max_seqlen == 0) return DIFFATTN_OK;
@@ -209,6 +221,9 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
     p.timeout_ns = g_timeout_ns;
     p.inject = g_inject;
+    p.lse = lse;
+    p.o1 = o1;
+    p.o2 = o2;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
@@ -219,6 +234,25 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
     return launch_fwd_bf16_sm103a(p, maps, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                             const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
+                             int causal, const int* cu_seqlens, void* out, void* stream) {
+    return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
+                      nullptr, nullptr, nullptr, stream);
+}
+
+diffattn_status diffattn_fwd_train(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                                   const float* lambda, int lambda_per_head, float lambda_init,
+                                   const float* subln_w, int causal, const int* cu_seqlens, void* out, float* lse,
+                                   void* o1, void* o2, void* stream) {
+    if (!lse || !o1 || !o2) return DIFFATTN_ERR_INVALID_ARG;
+    return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out, lse,
+                      o1, o2, stream);
 }
 
 unsigned long long diffattn_fwd_kvcache_workspace_size(const diffattn_kv_desc* desc) {
@@ -330,6 +364,119 @@ diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const
     }
     return diffattn_fwd_kvcache(desc, q, k_cache, v_cache, cache_seqlens, lambda, lambda_per_head, lambda_init,
                                 subln_w, causal, scratch, DIFFATTN_NOALLOC_SCRATCH_BYTES, out, stream);
+}
+
+unsigned long long diffattn_bwd_workspace_size(const diffattn_desc* desc) {
+    if (!desc || desc->num_heads <= 0 || desc->dv <= 0) return 0;
+    long long tokens = desc->batch > 0 && desc->seqlen > 0 ? (long long)desc->batch * desc->seqlen : 0;
+    if (desc->total_tokens > 0) tokens = desc->total_tokens > tokens ? desc->total_tokens : tokens;
+    return (unsigned long long)tokens * desc->num_heads * ((unsigned long long)desc->dv * 2 + 16);
+}
+
+diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                             const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
+                             int causal, const int* cu_seqlens, const void* dout, const float* lse, const void* o1,
+                             const void* o2, void* dq, void* dk, void* dv, float* dlambda, float* dsubln_w,
+                             void* workspace, unsigned long long workspace_bytes, void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_desc& ds = *desc;
+    if (ds.num_heads <= 0 || ds.num_kv_heads <= 0 || ds.num_heads % ds.num_kv_heads != 0 || ds.num_heads > 65535)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.d <= 0 || ds.dv != 2 * ds.d) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.dtype != DIFFATTN_DTYPE_BF16 || ds.d != 64) return DIFFATTN_ERR_UNSUPPORTED;
+    int num_seqs, seqlen, max_seqlen, tokens;
+    if (cu_seqlens == nullptr) {
+        if (ds.batch < 0 || ds.seqlen < 0 || (long long)ds.batch * ds.seqlen > INT32_MAX) return DIFFATTN_ERR_INVALID_ARG;
+        num_seqs = ds.batch;
+        seqlen = ds.seqlen;
+        max_seqlen = ds.seqlen;
+        tokens = ds.batch * ds.seqlen;
+    } else {
+        if (ds.num_seqs < 0 || ds.max_seqlen < 0 || ds.total_tokens < 0) return DIFFATTN_ERR_INVALID_ARG;
+        num_seqs = ds.num_seqs;
+        seqlen = 0;
+        max_seqlen = ds.max_seqlen;
+        tokens = ds.total_tokens;
+    }
+    if (num_seqs > 65535 || (long long)tokens * ds.num_heads * ds.dv >= (1LL << 40)) return DIFFATTN_ERR_INVALID_ARG;
+    if (tokens == 0 || num_seqs == 0 || max_seqlen == 0) return DIFFATTN_OK;
+    const void* b16[] = {q, k, v, dout, o1, o2, dq, dk, dv, workspace};
+    for (const void* ptr : b16)
+        if (!ptr || !aligned16(ptr)) return DIFFATTN_ERR_INVALID_ARG;
+    const void* f32[] = {lambda, subln_w, lse, dlambda, dsubln_w};
+    for (const void* ptr : f32)
+        if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
+    const unsigned long long dd_bytes = (unsigned long long)tokens * ds.num_heads * ds.dv * 2;
+    if (workspace_bytes < dd_bytes + (unsigned long long)tokens * ds.num_heads * 16) return DIFFATTN_ERR_INVALID_ARG;
+
+    unsigned int* err_word = nullptr;
+    if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int n_lambda = lambda_per_head ? ds.num_heads : 1;
+    if (cudaMemsetAsync(dlambda, 0, sizeof(float) * n_lambda, st) != cudaSuccess ||
+        cudaMemsetAsync(dsubln_w, 0, sizeof(float) * ds.dv, st) != cudaSuccess)
+        return DIFFATTN_ERR_CUDA;
+
+    void* dd = workspace;
+    float* rowstat = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dd_bytes);
+    BwdPreParams pre{};
+    pre.dout = dout;
+    pre.o1 = o1;
+    pre.o2 = o2;
+    pre.lse = lse;
+    pre.lambda = lambda;
+    pre.lambda_stride = lambda_per_head ? 1 : 0;
+    pre.lambda_init = lambda_init;
+    pre.subln_w = subln_w;
+    pre.eps = ds.eps;
+    pre.tokens = tokens;
+    pre.H = ds.num_heads;
+    pre.dd = dd;
+    pre.rowstat = rowstat;
+    pre.dlambda = dlambda;
+    pre.dsubln_w = dsubln_w;
+    if (launch_bwd_pre(pre, st) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+
+    BwdParams p{};
+    p.lambda = lambda;
+    p.lambda_stride = pre.lambda_stride;
+    p.causal = causal ? 1 : 0;
+    p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs;
+    p.seqlen = seqlen;
+    p.max_seqlen = max_seqlen;
+    p.total_tokens = tokens;
+    p.H = ds.num_heads;
+    p.Hkv = ds.num_kv_heads;
+    p.scale = (float)(1.0 / std::sqrt((double)ds.d));
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
+    p.rowstat = rowstat;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.error_word = err_word;
+    p.timeout_ns = g_timeout_ns;
+    BwdTensorMaps m;
+    const uint64_t qw = (uint64_t)ds.num_heads * 2 * ds.d, kw = (uint64_t)ds.num_kv_heads * 2 * ds.d;
+    const uint64_t vw = (uint64_t)ds.num_kv_heads * ds.dv, dw = (uint64_t)ds.num_heads * ds.dv;
+    if (!encode_bf16_rows(&m.q128, q, qw, tokens, 128) || !encode_bf16_rows(&m.q64, q, qw, tokens, 64) ||
+        !encode_bf16_rows(&m.k128, k, kw, tokens, 128) || !encode_bf16_rows(&m.v128, v, vw, tokens, 128) ||
+        !encode_bf16_rows(&m.dd128, dd, dw, tokens, 128) || !encode_bf16_rows(&m.dd64, dd, dw, tokens, 64))
+        return DIFFATTN_ERR_CUDA;
+    return launch_bwd_sm103a(p, m, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
+diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                    const float* dlambda, int n_sets, int d, float* dlq1, float* dlk1,
+                                    float* dlq2, float* dlk2, void* stream) {
+    if (!lq1 || !lk1 || !lq2 || !lk2 || !dlambda || !dlq1 || !dlk1 || !dlq2 || !dlk2) return DIFFATTN_ERR_INVALID_ARG;
+    if (n_sets < 1 || d < 1 || d > 1024) return DIFFATTN_ERR_INVALID_ARG;
+    return launch_lambda_bwd(lq1, lk1, lq2, lk2, dlambda, n_sets, d, dlq1, dlk1, dlq2, dlk2,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
 }
 
 diffattn_status diffattn_get_device_status(void* stream) {

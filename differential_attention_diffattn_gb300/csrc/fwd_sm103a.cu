@@ -284,9 +284,10 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 for (int e = 0; e < BN; ++e)
                     if (e >= lim) x[e] = -INFINITY;
             }
-            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+            float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]),
+                  mx3 = fmaxf(x[6], x[7]);
 #pragma unroll
-            for (int e = 4; e < BN; e += 8) {
+            for (int e = 8; e < BN; e += 8) {
                 mx0 = fmax3(mx0, x[e], x[e + 1]);
                 mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
                 mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
@@ -338,6 +339,9 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             mbar_arrive(bar_p_ready(c));
         }
 
+        // Training outputs: log2-sum-exp of the scaled scores per component,
+        // lse_c = m_c + log2(l_c), so that P_c = 2^(S_c * scale * log2(e) - lse_c).
+        if (ok && p.lse != nullptr && qi < len) p.lse[((size_t)(start + qi) * p.H + h) * 2 + c] = m + __log2f(l);
         if (c == 1) {
             ms.inv_l2[r] = 1.f / l;
             mbar_arrive(bar_l2_ready);
@@ -390,6 +394,20 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
                             dst[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    }
+                    // Training outputs: the normalised attention output of each component,
+                    // kept in fp32 (the lambda gradient sums many cancelling terms of them).
+                    if (store && p.o1 != nullptr) {
+                        const size_t base = ((size_t)(start + qi) * p.H + h) * DV / 4 + ch * 8;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            reinterpret_cast<float4*>(p.o1)[base + i] =
+                                make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
+                                            __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
+                            reinterpret_cast<float4*>(p.o2)[base + i] =
+                                make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
+                                            __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
+                        }
                     }
                 }
             }

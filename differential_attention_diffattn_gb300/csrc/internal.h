@@ -38,6 +38,9 @@ struct FwdParams {
     float scale;              // d^-0.5
     unsigned long long timeout_ns;
     int inject;               // test hook: 1 = the copy producer issues no loads
+    float* lse;               // training outputs (all null, or all set; bf16 kernel only):
+    void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
+    void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c
 };
 
 // TMA descriptors of the bf16 operands, built on the host per call.
@@ -68,6 +71,47 @@ struct KvParams {
     float scale;               // d^-0.5
 };
 
+// Backward pass (bf16, d = 64, dv = 128).
+struct BwdParams {
+    const float* lambda;       // [H] or [1]
+    int lambda_stride;
+    int causal;
+    const int* cu_seqlens;     // nullptr (dense) or [num_seqs + 1]
+    int num_seqs, seqlen, max_seqlen, total_tokens;
+    int H, Hkv;
+    float scale, scale_log2;
+    const float* rowstat;      // [H][tokens][4]: lse1, lse2, delta1, delta2 (workspace)
+    void* dq;                  // [tokens][H][2d]
+    void* dk;                  // [tokens][Hkv][2d]
+    void* dv;                  // [tokens][Hkv][dv]
+    unsigned int* error_word;
+    unsigned long long timeout_ns;
+};
+
+// TMA descriptors of the backward kernels: q and dD with 128- and 64-row boxes,
+// k and v with 128-row boxes.
+struct BwdTensorMaps {
+    CUtensorMap q128, q64, k128, v128, dd128, dd64;
+};
+
+// Per-row preprocessing of the backward (CUDA cores).
+struct BwdPreParams {
+    const void* dout;          // [tokens][H][dv] bf16
+    const void* o1;            // [tokens][H][dv] fp32, normalised O1 (forward)
+    const void* o2;
+    const float* lse;          // [tokens][H][2]
+    const float* lambda;
+    int lambda_stride;
+    float lambda_init;
+    const float* subln_w;      // [dv]
+    float eps;
+    int tokens, H;
+    void* dd;                  // out: [tokens][H][dv] bf16, gradient of the pre-norm output
+    float* rowstat;            // out: [H][tokens][4]
+    float* dlambda;            // out (accumulated): [H] or [1]
+    float* dsubln_w;           // out (accumulated): [dv]
+};
+
 // Kernel launchers (each defined in its own translation unit). They return the
 // cudaError_t of the launch.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
@@ -75,6 +119,11 @@ cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, 
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_decode(const KvParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& maps, cudaStream_t stream);
+cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                              const float* dlambda, int n_sets, int d, float* dlq1, float* dlk1, float* dlq2,
+                              float* dlk2, cudaStream_t stream);
 int decode_rows_supported(int rows);
 int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
 int decode_max_splits();           // most key splits the combine kernel merges

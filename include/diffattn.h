@@ -134,6 +134,66 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
                              const int* cu_seqlens, void* out, void* stream);
 
 /*
+ * Forward for training: diffattn_fwd (bf16 tcgen05 kernel only) that also
+ * saves what the backward pass needs, per (token, head):
+ *  lse : device fp32 [tokens][H][2]: for component c, log2 of the softmax
+ *        denominator in the log2 domain of the scaled scores, so that the
+ *        probabilities are 2^(s * log2(e) * <Q_c, K_c[j]> - lse[..][c]);
+ *  o1, o2 : device fp32 [tokens][H][dv]: the normalised attention outputs
+ *        softmax(s Q1 K1^T) V and softmax(s Q2 K2^T) V, 16-byte aligned (fp32:
+ *        the lambda gradient is a sum of many cancelling terms of these).
+ * Errors: as diffattn_fwd; INVALID_ARG if any of lse, o1, o2 is NULL or
+ * misaligned; UNSUPPORTED for fp32.
+ */
+diffattn_status diffattn_fwd_train(const diffattn_desc* desc, const void* q, const void* k,
+                                   const void* v, const float* lambda, int lambda_per_head,
+                                   float lambda_init, const float* subln_w, int causal,
+                                   const int* cu_seqlens, void* out, float* lse, void* o1, void* o2,
+                                   void* stream);
+
+/*
+ * Bytes of device workspace diffattn_bwd needs for `desc`: tokens x H x
+ * (2 dv + 16) (the gradient of the pre-norm output in bf16 and four fp32 row
+ * statistics per (token, head)).
+ */
+unsigned long long diffattn_bwd_workspace_size(const diffattn_desc* desc);
+
+/*
+ * Backward pass of diffattn_fwd_train (bf16, d = 64, dv = 128): given dout, the
+ * gradient of the loss with respect to out, and the forward's saved lse, o1,
+ * o2, writes the gradients with respect to q, k, v (bf16, layouts of q, k, v),
+ * lambda (fp32, [H] or [1] like `lambda`; for shared lambda the heads' sum) and
+ * subln_w (fp32 [dv]). The pages define the forward only; these are its plain
+ * derivatives (the modules on "DiffTransformer.py" and "LlamaDiffSdpaAttention.py"
+ * train lambda_q1 ... lambda_k2 and the norm weight). Launches, on `stream`:
+ * two memsets, a per-row kernel (the RMSNorm and output-scale gradient, the row
+ * statistics of both softmaxes, the lambda and weight gradients), a dQ kernel
+ * and a dK/dV kernel (tcgen05; grouped kv heads summed inside the CTA).
+ * workspace: device, 16-byte aligned, >= diffattn_bwd_workspace_size(desc).
+ * Errors: as diffattn_fwd; UNSUPPORTED for anything but bf16 with d = 64.
+ * Use diffattn_lambda_bwd to turn the lambda gradient into the gradients of the
+ * four lambda vectors.
+ */
+diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                             const float* lambda, int lambda_per_head, float lambda_init,
+                             const float* subln_w, int causal, const int* cu_seqlens, const void* dout,
+                             const float* lse, const void* o1, const void* o2, void* dq, void* dk,
+                             void* dv, float* dlambda, float* dsubln_w, void* workspace,
+                             unsigned long long workspace_bytes, void* stream);
+
+/*
+ * Gradient of the lambda reparameterisation ("DiffTransformer.py",
+ * MultiHeadDifferentialAttention.forward, "Compute lambda using
+ * reparameterization"): with a = lq1 . lk1, b = lq2 . lk2 per set,
+ *   dlq1 = dlambda e^a lk1, dlk1 = dlambda e^a lq1,
+ *   dlq2 = -dlambda e^b lk2, dlk2 = -dlambda e^b lq2.
+ * All device fp32; vectors [n_sets][d], dlambda [n_sets]. Outputs overwritten.
+ */
+diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2,
+                                    const float* lk2, const float* dlambda, int n_sets, int d,
+                                    float* dlq1, float* dlk1, float* dlq2, float* dlk2, void* stream);
+
+/*
  * Shape of a forward against a key/value cache (decode, or a short block of new
  * queries appended to a cached sequence).
  *  batch sequences; each has q_len new query tokens and a cache of

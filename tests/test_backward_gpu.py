@@ -1,0 +1,118 @@
+"""GPU parity of the training forward outputs and the backward pass against
+the fp64 gradient oracle (autograd of the plain forward, itself pinned by
+finite differences of the C oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import differential_attention_diffattn_gb300 as da
+from differential_attention_diffattn_gb300 import workloads as W
+from oracle import backward as ob
+from oracle import oracle as orc
+
+from gpu_util import compare, oracle_out
+
+pytestmark = pytest.mark.gpu
+
+# bf16 operands (P, dS, dD and the inputs) bound the gradient accuracy: each
+# gradient tensor must match the fp64 oracle to a normalised L1 of 2e-2 and a
+# max-abs error of 5e-2 of its largest magnitude.
+TOL_REL_L1 = 2e-2
+TOL_MAX_REL = 5e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    da.build()
+    da.load_library()
+    torch.cuda.set_device(0)
+
+
+def grad_close(got, want, name):
+    g = got.detach().double().cpu().numpy()
+    w = want.detach().double().cpu().numpy()
+    assert np.isfinite(g).all(), name
+    err = np.abs(g - w)
+    rel = err.sum() / max(np.abs(w).sum(), 1e-30)
+    mx = err.max() / max(np.abs(w).max(), 1e-30)
+    assert rel <= TOL_REL_L1 and mx <= TOL_MAX_REL, (name, rel, mx)
+
+
+def run_case(wl, lens, seed):
+    inp = W.generate(wl, seed=seed, seq_lens=lens)
+    dev = "cuda"
+    li = da.diffattn_lambda_init(wl.depth)
+    lv = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    lam = da.diffattn_lambda(*lv, li)
+    q, k, v, w = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.subln_w.to(dev)
+    cu = inp.cu_seqlens.to(dev)
+    out, lse, o1, o2 = da.diffattn_fwd_train(q, k, v, lam, li, w, causal=wl.causal, cu_seqlens=cu,
+                                             max_seqlen=inp.max_seqlen, eps=wl.eps)
+    g = torch.Generator().manual_seed(seed + 1)
+    dy = torch.randn(out.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv, dlam, dw = da.diffattn_bwd(q, k, v, lam, li, w, dy.to(dev), lse, o1, o2, causal=wl.causal,
+                                           cu_seqlens=cu, max_seqlen=inp.max_seqlen, eps=wl.eps)
+    dl = da.diffattn_lambda_bwd(*lv, dlam)
+    assert da.diffattn_get_device_status() == 0
+    return inp, dy, out, lse, o1, o2, dq, dk, dv, dlam, dw, dl
+
+
+BF = W.WORKLOADS["b2_t512_gqa"]
+
+
+def test_training_outputs_match_oracle():
+    inp, dy, out, lse, o1, o2, *_ = run_case(BF, [300, 129], 81)
+    compare(out, oracle_out(inp), "bf16")
+    # normalised attention outputs: the oracle with lambda = 0, lambda_init = 0,
+    # w = 1 and a huge eps returns O1 / sqrt(eps); swapping components gives O2
+    E = 1e12
+    G = inp.wl.num_heads // inp.wl.num_kv_heads
+    ones = np.ones(inp.wl.dv)
+    want1 = orc.forward_rows(inp.cu_seqlens, inp.q, inp.k, inp.v, 0.0, 0.0, ones, E, True) * np.sqrt(E)
+    d = inp.wl.d
+    q_sw = torch.cat([inp.q[..., d:], inp.q[..., :d]], -1)
+    k_sw = torch.cat([inp.k[..., d:], inp.k[..., :d]], -1)
+    want2 = orc.forward_rows(inp.cu_seqlens, q_sw, k_sw, inp.v, 0.0, 0.0, ones, E, True) * np.sqrt(E)
+    for got, want in ((o1, want1), (o2, want2)):
+        err = np.abs(got.float().cpu().numpy() - want)
+        assert err.max() <= 2e-2 and err.sum() / np.abs(want).sum() <= 5e-3
+        # the first query of a causal sequence sees one key: its probability is
+        # exactly 1, so the normalised output is that key's value (to fp32 rounding
+        # of the exponential of a zero argument)
+        for t in inp.cu_seqlens[:-1].tolist():
+            row = got[t].double().cpu()
+            v0 = inp.v[t].double().repeat_interleave(G, dim=0)
+            assert (row - v0).abs().max() <= 1e-6 * v0.abs().max(), t
+    # lse: log2 sum over visible keys of 2^(s log2(e) <q_c, k_c>), per component
+    qf, kf = inp.q.double(), inp.k.double()
+    cu = inp.cu_seqlens.tolist()
+    for t in (0, 1, 150, 299, 300, 428):
+        sq = max(i for i in range(len(cu) - 1) if cu[i] <= t)
+        a = cu[sq]
+        for h in (0, 5, 15):
+            for c in range(2):
+                sc = (kf[a:t + 1, h // G, c * d:(c + 1) * d] @ qf[t, h, c * d:(c + 1) * d]) * d ** -0.5 / np.log(2)
+                want = float(torch.logsumexp(sc * np.log(2), 0) / np.log(2))
+                assert abs(float(lse[t, h, c]) - want) < 1e-3
+
+
+@pytest.mark.parametrize("lens,H,Hkv,causal,per_head", [
+    ([256], 16, 4, True, False),
+    ([300, 129, 1], 8, 2, True, True),
+    ([200], 4, 4, False, False),
+    ([513], 16, 16, True, False),
+])
+def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
+    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, lambda_per_head=per_head,
+                          random_subln=True)
+    inp, dy, out, lse, o1, o2, dq, dk, dv, dlam, dw, dl = run_case(wl, lens, 90 + H + len(lens))
+    li = orc.lambda_init(wl.depth)
+    want = ob.gradients(inp.cu_seqlens.tolist(), inp.q.double(), inp.k.double(), inp.v.double(),
+                        inp.lambda_q1.double(), inp.lambda_k1.double(), inp.lambda_q2.double(),
+                        inp.lambda_k2.double(), inp.subln_w.double(), li, wl.eps, causal, dy.double())
+    grad_close(dq, want["q"], "dq")
+    grad_close(dk, want["k"], "dk")
+    grad_close(dv, want["v"], "dv")
+    grad_close(dw, want["w"], "dw")
+    for got, name in zip(dl, ("lq1", "lk1", "lq2", "lk2")):
+        grad_close(got, want[name], name)
