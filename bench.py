@@ -49,6 +49,14 @@ def peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
+def dense_view(t, inp):
+    """Token-major [tokens, ...] as [B, T, ...] for a dense batch of equal
+    sequences (several sequences, no cu_seqlens); unchanged otherwise."""
+    if inp.wl.varlen or len(inp.seq_lens) <= 1:
+        return t
+    return t.view(len(inp.seq_lens), inp.seq_lens[0], *t.shape[1:])
+
+
 def causal_pairs(seq_lens, heads):
     return sum(n * (n + 1) // 2 for n in seq_lens) * heads
 
@@ -147,8 +155,8 @@ def run_ours(args, rank, world, local_rank):
     # L2, so a step never starts on tensors the previous step left in L2.
     sets = []
     for _ in range(2):
-        s = dict(q=inp.q.to(dev), k=inp.k.to(dev), v=inp.v.to(dev))
-        s["out"] = torch.empty(tokens, wl.num_heads, wl.dv, dtype=s["q"].dtype, device=dev)
+        s = dict(q=dense_view(inp.q.to(dev), inp), k=dense_view(inp.k.to(dev), inp), v=dense_view(inp.v.to(dev), inp))
+        s["out"] = dense_view(torch.empty(tokens, wl.num_heads, wl.dv, dtype=s["q"].dtype, device=dev), inp)
         sets.append(s)
     lvec = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
     w = inp.subln_w.to(dev)
@@ -212,14 +220,14 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         s = sets[0]
         for n in ("q", "k", "v"):
-            s[n].copy_(host[n], non_blocking=True)
+            s[n].copy_(dense_view(host[n], inp), non_blocking=True)
         for dst, src in zip(lvec, host_l):
             dst.copy_(src, non_blocking=True)
         w.copy_(host["subln_w"], non_blocking=True)
         cu.copy_(host["cu_seqlens"], non_blocking=True)
         da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
         fwd(s)
-        out_h.copy_(s["out"], non_blocking=True)
+        out_h.copy_(s["out"].view(out_h.shape), non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -273,6 +281,164 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_stride)
     return line
+
+
+# ------------------------------------------------ training step (GPU) ---
+
+BWD_FLOP_PER_PAIR = 1280  # S_1, S_2 recomputed once, dP, dV, dQ_1, dQ_2, dK_1, dK_2
+
+
+def run_ours_bwd(args, rank, world, local_rank):
+    """Forward with saved statistics + backward (all gradients, including the
+    lambda vectors and the norm weight). Algorithmic flop per visible pair and
+    diff head: 768 forward + 1280 backward."""
+    import torch
+
+    import differential_attention_diffattn_gb300 as da
+    from differential_attention_diffattn_gb300 import shard
+    from differential_attention_diffattn_gb300 import workloads as W
+
+    da.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    inp = W.generate(wl, seed=args.seed)
+    tokens, H, dvv = inp.tokens, wl.num_heads, wl.dv
+    pairs = causal_pairs(inp.seq_lens, H)
+    fwd_flop, bwd_flop = FLOP_PER_PAIR * pairs, BWD_FLOP_PER_PAIR * pairs
+    li = da.diffattn_lambda_init(wl.depth)
+    stream = torch.cuda.current_stream()
+    g = torch.Generator().manual_seed(args.seed + 1)
+    dout_h = torch.randn(tokens, H, dvv, generator=g).to(torch.bfloat16)
+    cu = inp.cu_seqlens.to(dev) if wl.varlen else None
+    kw = dict(causal=wl.causal, cu_seqlens=cu, max_seqlen=inp.max_seqlen if wl.varlen else None, eps=wl.eps)
+    sets = []
+    for _ in range(2):  # two rotating sets, each far larger than L2
+        s = {n: dense_view(t.to(dev), inp) for n, t in (("q", inp.q), ("k", inp.k), ("v", inp.v), ("dout", dout_h))}
+        s["out"] = dense_view(torch.empty(tokens, H, dvv, dtype=torch.bfloat16, device=dev), inp)
+        s["lse"] = dense_view(torch.empty(tokens, H, 2, dtype=torch.float32, device=dev), inp)
+        s["o1"] = dense_view(torch.empty(tokens, H, dvv, dtype=torch.float32, device=dev), inp)
+        s["o2"] = torch.empty_like(s["o1"])
+        s["grads"] = (torch.empty_like(s["q"]), torch.empty_like(s["k"]), torch.empty_like(s["v"]),
+                      torch.empty(H if wl.lambda_per_head else 1, dtype=torch.float32, device=dev),
+                      torch.empty(dvv, dtype=torch.float32, device=dev))
+        sets.append(s)
+    lvec = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    w = inp.subln_w.to(dev)
+    lam = torch.empty(H if wl.lambda_per_head else 1, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, da.diffattn_bwd_workspace_size(sets[0]["q"], sets[0]["k"], sets[0]["v"], lam, w, cu,
+                                                          kw["max_seqlen"], wl.eps)), dtype=torch.uint8, device=dev)
+
+    def fwd(s):
+        da.diffattn_fwd_train(s["q"], s["k"], s["v"], lam, li, w, out=s["out"], lse=s["lse"], o1=s["o1"],
+                              o2=s["o2"], stream=stream, **kw)
+
+    def bwd(s):
+        da.diffattn_bwd(s["q"], s["k"], s["v"], lam, li, w, s["dout"], s["lse"], s["o1"], s["o2"], workspace=ws,
+                        grads=s["grads"], stream=stream, **kw)
+
+    def lam_bwd(s):
+        return da.diffattn_lambda_bwd(*lvec, s["grads"][3], stream=stream)
+
+    for i in range(args.warmup):
+        s = sets[i % 2]
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        fwd(s)
+        bwd(s)
+        lam_bwd(s)
+    torch.cuda.synchronize()
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error during warm-up")
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk(), mk()) for _ in range(args.steps)]
+    t0, t1 = mk(), mk()
+    sampler = None
+    if rank == 0:
+        visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        sampler = ClockSampler(visible[local_rank].strip() if local_rank < len(visible) else str(local_rank))
+        sampler.start()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        s = sets[i % 2]
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        ev[i][0].record(stream)
+        fwd(s)
+        ev[i][1].record(stream)
+        bwd(s)
+        ev[i][2].record(stream)
+        lam_bwd(s)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the timed region")
+    elapsed_ms = shard.max_over_ranks(t0.elapsed_time(t1))
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    value = (fwd_flop + bwd_flop) * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end: q, k, v, dout and the parameters from pinned host memory, all
+    # gradients back to pinned host memory
+    hq = {n: getattr(inp, n).pin_memory() for n in ("q", "k", "v", "subln_w")}
+    hq["dout"] = dout_h.pin_memory()
+    hl = [x.pin_memory() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    hg = [t.cpu().pin_memory() for t in sets[0]["grads"][:3]] + [x.cpu().pin_memory() for x in lvec] + \
+        [sets[0]["grads"][4].cpu().pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in list(hq.values()) + hl)
+    d2h = sum(t.numel() * t.element_size() for t in hg)
+
+    def e2e_step():
+        s = sets[0]
+        for n in ("q", "k", "v", "dout"):
+            s[n].copy_(dense_view(hq[n], inp), non_blocking=True)
+        for dst, src in zip(lvec, hl):
+            dst.copy_(src, non_blocking=True)
+        w.copy_(hq["subln_w"], non_blocking=True)
+        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+        fwd(s)
+        bwd(s)
+        lg = lam_bwd(s)
+        for dst, src in zip(hg, list(s["grads"][:3]) + list(lg) + [s["grads"][4]]):
+            dst.copy_(src.view(dst.shape), non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = mk(), mk()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = shard.max_over_ranks(e0.elapsed_time(e1))
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the end-to-end region")
+    if not all(torch.isfinite(t.float()).all() for t in hg):
+        raise RuntimeError("non-finite gradient")
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    peak = float(pk["bf16_tflops"])
+    bwd_achieved = bwd_flop / (bwd_ms * 1e-3) / 1e12
+    return {
+        "metric": "diff-attn fwd+bwd TFLOP/s (causal)", "value": round(value, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": tokens, "seq_len": inp.max_seqlen, "diff_heads": H,
+                   "kv_heads": wl.num_kv_heads, "d": wl.d, "dv": dvv, "causal": wl.causal,
+                   "flop_per_pair": FLOP_PER_PAIR + BWD_FLOP_PER_PAIR, "flop_per_step": fwd_flop + bwd_flop,
+                   "l2": "two rotating input/output sets, each larger than L2"},
+        "fwd_train": {"ms": round(fwd_ms, 4), "tflops": round(fwd_flop / (fwd_ms * 1e-3) / 1e12, 2)},
+        "e2e": {"value": round((fwd_flop + bwd_flop) * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps, "ms_per_step": round(e2e_ms / args.e2e_steps, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(bwd_achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"{pk_kind} bf16 dense burst",
+                     "kernel": "diffattn_bwd (preprocessing + dQ + dK/dV kernels)", "launch_ms": round(bwd_ms, 4),
+                     "algorithmic_flop_per_launch": bwd_flop},
+        "clocks": clocks, "gpu_launches": 6 * args.steps, "impl": "ours",
+    }
 
 
 # ------------------------------------------------- cache forward (GPU) ---
@@ -457,6 +623,7 @@ def main():
     ap.add_argument("--cpu-stride", type=int, default=2, help="CPU baseline: every n-th query row")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
+    ap.add_argument("--backward", action="store_true", help="time forward + backward (training step)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -479,7 +646,10 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
         from differential_attention_diffattn_gb300 import workloads as W
-        runner = run_ours_kv if args.workload in W.KV_WORKLOADS else run_ours
+        if args.workload in W.KV_WORKLOADS:
+            runner = run_ours_kv
+        else:
+            runner = run_ours_bwd if args.backward else run_ours
         line = runner(args, rank, world, local_rank)
     finally:
         if world > 1:

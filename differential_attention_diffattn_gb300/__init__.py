@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) differential-attention forward behind a C ABI.
+"""GB300 (sm_103a) differential attention (forward, backward, cache forward) behind a C ABI.
 
 The public functions carry the names of the C entry points in
 include/diffattn.h and take torch tensors for device memory and streams.
@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     DiffAttnError,
     DiffAttnKvDesc,
     diffattn_bwd,
+    diffattn_bwd_workspace_size,
     diffattn_fwd,
     diffattn_fwd_train,
     diffattn_fwd_kvcache,

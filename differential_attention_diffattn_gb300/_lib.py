@@ -198,18 +198,24 @@ def _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps):
 
 
 def diffattn_fwd_train(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,
-                       max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, stream=None):
+                       max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, lse=None, o1=None, o2=None,
+                       stream=None):
     """Forward that also returns what diffattn_bwd needs: (out, lse, o1, o2) with
-    lse fp32 [..., H, 2] and o1, o2 fp32 [..., H, dv]."""
+    lse fp32 [..., H, 2] and o1, o2 fp32 [..., H, dv] (allocated when not given)."""
     import torch
     lib = load_library()
     desc, H = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
     shp = q.shape[:-1]
     if out is None:
         out = torch.empty(shp + (v.shape[-1],), dtype=q.dtype, device=q.device)
-    lse = torch.empty(shp + (2,), dtype=torch.float32, device=q.device)
-    o1 = torch.empty(shp + (v.shape[-1],), dtype=torch.float32, device=q.device)
-    o2 = torch.empty_like(o1)
+    if lse is None:
+        lse = torch.empty(shp + (2,), dtype=torch.float32, device=q.device)
+    if o1 is None:
+        o1 = torch.empty(shp + (v.shape[-1],), dtype=torch.float32, device=q.device)
+    if o2 is None:
+        o2 = torch.empty_like(o1)
+    for t, name in ((out, "out"), (lse, "lse"), (o1, "o1"), (o2, "o2")):
+        _check_cuda(t, name)
     st = lib.diffattn_fwd_train(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
                                 1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
                                 1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(out),
@@ -219,10 +225,18 @@ def diffattn_fwd_train(q, k, v, lam, lambda_init: float, subln_w, causal: bool =
     return out, lse, o1, o2
 
 
+def diffattn_bwd_workspace_size(q, k, v, lam, subln_w, cu_seqlens=None, max_seqlen: Optional[int] = None,
+                                eps: float = 1e-5) -> int:
+    """Bytes of device scratch diffattn_bwd needs for these shapes."""
+    desc, _ = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
+    return int(load_library().diffattn_bwd_workspace_size(ctypes.byref(desc)))
+
+
 def diffattn_bwd(q, k, v, lam, lambda_init: float, subln_w, dout, lse, o1, o2, causal: bool = True,
                  cu_seqlens=None, max_seqlen: Optional[int] = None, eps: float = 1e-5, workspace=None,
-                 stream=None):
-    """Gradients (dq, dk, dv, dlambda, dsubln_w) of diffattn_fwd_train's output."""
+                 grads=None, stream=None):
+    """Gradients (dq, dk, dv, dlambda, dsubln_w) of diffattn_fwd_train's output;
+    `grads` optionally gives those five tensors to write into."""
     import torch
     lib = load_library()
     desc, H = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
@@ -231,9 +245,15 @@ def diffattn_bwd(q, k, v, lam, lambda_init: float, subln_w, dout, lse, o1, o2, c
     need = int(lib.diffattn_bwd_workspace_size(ctypes.byref(desc)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dlam = torch.empty(lam.numel() if (lam.numel() == H and H > 1) else 1, dtype=torch.float32, device=q.device)
-    dw = torch.empty_like(subln_w)
+    if grads is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dlam = torch.empty(lam.numel() if (lam.numel() == H and H > 1) else 1, dtype=torch.float32,
+                           device=q.device)
+        dw = torch.empty_like(subln_w)
+    else:
+        dq, dk, dv, dlam, dw = grads
+        for t, name in ((dq, "dq"), (dk, "dk"), (dv, "dv"), (dlam, "dlambda"), (dw, "dsubln_w")):
+            _check_cuda(t, name)
     st = lib.diffattn_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
                           1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
                           1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(dout),

@@ -19,8 +19,8 @@ namespace diffattn {
 namespace {
 
 constexpr int DVD = 128;
-constexpr int ROWS_PER_WARP = 16;
-constexpr int WARPS = 4;
+constexpr int ROWS_PER_WARP = 8;  // loaded together, so their memory latencies overlap
+constexpr int WARPS = 8;
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -28,18 +28,13 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-__device__ __forceinline__ void load4(const void* base, size_t idx, float (&f)[4]) {
-    const uint2 u = reinterpret_cast<const uint2*>(base)[idx];
-    f[0] = __uint_as_float(u.x << 16);
-    f[1] = __uint_as_float(u.x & 0xffff0000u);
-    f[2] = __uint_as_float(u.y << 16);
-    f[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-
-// Warp w of block (x, h) handles rows t = (x * WARPS + w) * ROWS_PER_WARP .. +15 of head h;
-// lane l owns value columns 4l .. 4l+3.
+// Block (x, h): rows t = x * 64 .. x * 64 + 63 of head h; warp w takes 8 of them,
+// lane l owns value columns 4l .. 4l+3. The norm-weight and lambda gradients are
+// summed over the block before one set of atomics.
 __global__ void __launch_bounds__(32 * WARPS)
 diffattn_bwd_pre_kernel(const BwdPreParams p) {
+    __shared__ float s_dw[WARPS][DVD];
+    __shared__ float s_dl[WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y;
     const int t0 = (blockIdx.x * WARPS + warp) * ROWS_PER_WARP;
@@ -48,21 +43,36 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
     float w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = p.subln_w[4 * lane + i];
+    float dy[ROWS_PER_WARP][4], o1[ROWS_PER_WARP][4], o2[ROWS_PER_WARP][4];
+#pragma unroll
+    for (int r = 0; r < ROWS_PER_WARP; ++r) {
+        const int t = t0 + r;
+        if (t < p.tokens) {
+            const size_t idx = ((size_t)t * p.H + h) * (DVD / 4) + lane;
+            const uint2 u = reinterpret_cast<const uint2*>(p.dout)[idx];
+            dy[r][0] = __uint_as_float(u.x << 16);
+            dy[r][1] = __uint_as_float(u.x & 0xffff0000u);
+            dy[r][2] = __uint_as_float(u.y << 16);
+            dy[r][3] = __uint_as_float(u.y & 0xffff0000u);
+            const float4 a1 = reinterpret_cast<const float4*>(p.o1)[idx];
+            const float4 a2 = reinterpret_cast<const float4*>(p.o2)[idx];
+            o1[r][0] = a1.x; o1[r][1] = a1.y; o1[r][2] = a1.z; o1[r][3] = a1.w;
+            o2[r][0] = a2.x; o2[r][1] = a2.y; o2[r][2] = a2.z; o2[r][3] = a2.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dy[r][i] = o1[r][i] = o2[r][i] = 0.f;
+        }
+    }
     float dw[4] = {0.f, 0.f, 0.f, 0.f};
     float dlam = 0.f;
-    for (int t = t0; t < min(t0 + ROWS_PER_WARP, p.tokens); ++t) {
-        const size_t row = (size_t)t * p.H + h;
-        float dy[4], o1[4], o2[4], D[4], u[4];
-        load4(p.dout, row * (DVD / 4) + lane, dy);
-        const float4 a1 = reinterpret_cast<const float4*>(p.o1)[row * (DVD / 4) + lane];
-        const float4 a2 = reinterpret_cast<const float4*>(p.o2)[row * (DVD / 4) + lane];
-        o1[0] = a1.x; o1[1] = a1.y; o1[2] = a1.z; o1[3] = a1.w;
-        o2[0] = a2.x; o2[1] = a2.y; o2[2] = a2.z; o2[3] = a2.w;
-        float ss = 0.f, ud = 0.f;
+#pragma unroll
+    for (int r = 0; r < ROWS_PER_WARP; ++r) {
+        const int t = t0 + r;
+        float D[4], u[4], ss = 0.f, ud = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            D[i] = o1[i] - lam * o2[i];
-            u[i] = dy[i] * w[i] * post;
+            D[i] = o1[r][i] - lam * o2[r][i];
+            u[i] = dy[r][i] * w[i] * post;
             ss = fmaf(D[i], D[i], ss);
             ud = fmaf(u[i], D[i], ud);
         }
@@ -74,27 +84,43 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             dd[i] = u[i] * rinv - D[i] * corr;
-            d1 = fmaf(dd[i], o1[i], d1);
-            d2 = fmaf(dd[i], o2[i], d2);
-            dw[i] = fmaf(dy[i], D[i] * rinv * post, dw[i]);
+            d1 = fmaf(dd[i], o1[r][i], d1);
+            d2 = fmaf(dd[i], o2[r][i], d2);
+            dw[i] = fmaf(dy[r][i], D[i] * rinv * post, dw[i]);  // zero for rows past the end (dy = 0)
         }
         d1 = warp_sum(d1);
         d2 = warp_sum(d2);
-        dlam -= d2;
-        __nv_bfloat162 lo2 = __floats2bfloat162_rn(dd[0], dd[1]);
-        __nv_bfloat162 hi2 = __floats2bfloat162_rn(dd[2], dd[3]);
-        uint2 st;
-        st.x = *reinterpret_cast<uint32_t*>(&lo2);
-        st.y = *reinterpret_cast<uint32_t*>(&hi2);
-        reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
-        if (lane == 0) {
-            const float2 l2 = reinterpret_cast<const float2*>(p.lse)[row];
-            reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(l2.x, l2.y, d1, d2);
+        if (t < p.tokens) {
+            dlam -= d2;
+            const size_t row = (size_t)t * p.H + h;
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(dd[0], dd[1]);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(dd[2], dd[3]);
+            uint2 st;
+            st.x = *reinterpret_cast<uint32_t*>(&lo2);
+            st.y = *reinterpret_cast<uint32_t*>(&hi2);
+            reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
+            if (lane == 0) {
+                const float2 l2 = reinterpret_cast<const float2*>(p.lse)[row];
+                reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(l2.x, l2.y, d1, d2);
+            }
         }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) atomicAdd(p.dsubln_w + 4 * lane + i, dw[i]);
-    if (lane == 0) atomicAdd(p.dlambda + h * p.lambda_stride, dlam);
+    for (int i = 0; i < 4; ++i) s_dw[warp][4 * lane + i] = dw[i];
+    if (lane == 0) s_dl[warp] = dlam;
+    __syncthreads();
+    if (threadIdx.x < DVD) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < WARPS; ++k) acc += s_dw[k][threadIdx.x];
+        atomicAdd(p.dsubln_w + threadIdx.x, acc);
+    }
+    if (threadIdx.x == 0) {
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < WARPS; ++k) acc += s_dl[k];
+        atomicAdd(p.dlambda + h * p.lambda_stride, acc);
+    }
 }
 
 // One warp per lambda parameter set:

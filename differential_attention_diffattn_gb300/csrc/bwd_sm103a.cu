@@ -71,6 +71,34 @@ __device__ __forceinline__ bool seq_bounds(const BwdParams& p, int seq, int* sta
 }
 
 // =============================================================== dQ ===
+// One thread (= one query row) and 32 keys: dS_1, dS_2 as bf16 pairs from S_1,
+// S_2, dP and the row's (lse_1, lse_2, delta_1, delta_2). MASK zeroes keys at or
+// past `nvis` (the number of visible keys in this group of 32, any value).
+template <bool MASK>
+__device__ __forceinline__ void dq_keys32(const uint32_t (&s1)[32], const uint32_t (&s2)[32],
+                                          const uint32_t (&dp)[32], const float4 rs, float lam, float sl2, float sc,
+                                          int nvis, uint32_t (&d1)[16], uint32_t (&d2)[16]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float a[2], b[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float pp = __uint_as_float(dp[i + u]);
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -rs.x));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -rs.y));
+            a[u] = p1 * (pp - rs.z) * sc;
+            b[u] = -lam * p2 * (pp - rs.w) * sc;
+            if (MASK) {
+                const bool vis = i + u < nvis;
+                a[u] = vis ? a[u] : 0.f;
+                b[u] = vis ? b[u] : 0.f;
+            }
+        }
+        d1[i / 2] = pack_bf16x2(a[0], a[1]);
+        d2[i / 2] = pack_bf16x2(b[0], b[1]);
+    }
+}
+
 namespace dq {
 constexpr int BM = 128, BN = 128, STAGES = 2;
 constexpr uint32_t BOX = 128 * ROW;                // [128 x 64] bf16 box: 16 KB
@@ -211,6 +239,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)j & 1u, ab)))) break;
             tc_fence_after();
             const int kb = j * BN;
+            // masking only on tiles where some row of the warp has keys past its limit
+            const bool need_mask = __any_sync(0xffffffffu, kb + BN > lim);
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t s1[32], s2[32], dp[32];
@@ -219,22 +249,10 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 tmem_ld32(tmem + lo + 256 + ch * 32, dp);
                 tmem_wait_ld();
                 uint32_t d1[16], d2[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float a[2], b2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int e = ch * 32 + i + u;
-                        const bool vis = kb + e < lim;
-                        const float pp = __uint_as_float(dp[i + u]);
-                        const float p1 = vis ? ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -rs.x)) : 0.f;
-                        const float p2 = vis ? ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -rs.y)) : 0.f;
-                        a[u] = p1 * (pp - rs.z) * sc;
-                        b2[u] = -lam * p2 * (pp - rs.w) * sc;
-                    }
-                    d1[i / 2] = pack_bf16x2(a[0], a[1]);
-                    d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
-                }
+                if (need_mask)
+                    dq_keys32<true>(s1, s2, dp, rs, lam, sl2, sc, lim - (kb + ch * 32), d1, d2);
+                else
+                    dq_keys32<false>(s1, s2, dp, rs, lam, sl2, sc, 0, d1, d2);
                 // dS_c of keys [32 ch, 32 ch + 32) -> columns [16 ch, 16 ch + 16) of S_c (already read)
                 tmem_st16(tmem + lo + ch * 16, d1);
                 tmem_st16(tmem + lo + 128 + ch * 16, d2);
@@ -292,6 +310,42 @@ struct Misc {
     int abort_flag;
 };
 }  // namespace dkv
+
+// One thread (= one key) and 32 query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
+// pairs from S_1^T, S_2^T, dP^T and the rows' (lse_1, lse_2, delta_1, delta_2).
+// MASK zeroes rows outside [q_min, q_end); without it every row is visible.
+// The exponentials run on every element and masking is a select after the
+// products, so stale statistics of rows past the end never reach the results.
+template <bool MASK>
+__device__ __forceinline__ void dkv_rows32(const uint32_t (&s1)[32], const uint32_t (&s2)[32],
+                                           const uint32_t (&dp)[32], const float4* stat, float lam, float sl2,
+                                           float sc, int q0, int q_end, int q_min, uint32_t (&pc)[16],
+                                           uint32_t (&d1)[16], uint32_t (&d2)[16]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float a[2], b1[2], b2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float4 st = stat[i + u];
+            const float pp = __uint_as_float(dp[i + u]);
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y));
+            a[u] = p1 - lam * p2;
+            b1[u] = p1 * (pp - st.z) * sc;
+            b2[u] = -lam * p2 * (pp - st.w) * sc;
+            if (MASK) {
+                const int qi = q0 + i + u;
+                const bool vis = (qi < q_end) & (qi >= q_min);
+                a[u] = vis ? a[u] : 0.f;
+                b1[u] = vis ? b1[u] : 0.f;
+                b2[u] = vis ? b2[u] : 0.f;
+            }
+        }
+        pc[i / 2] = pack_bf16x2(a[0], a[1]);
+        d1[i / 2] = pack_bf16x2(b1[0], b1[1]);
+        d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
+    }
+}
 
 __global__ void __launch_bounds__(NT, 1)
 diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -418,6 +472,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const uint32_t lo = (uint32_t)(warp * 32) << 16;
         const int kj = kt * BK + k;      // key position in the sequence
         const bool key_ok = kj < len;
+        const int q_end = key_ok ? len : 0;       // visible query rows of this key: [q_min, q_end)
+        const int q_min = p.causal ? kj : 0;
         const float sl2 = p.scale_log2, sc = p.scale;
         bool ok = true;
         for (int it = 0; it < n_items; ++it) {
@@ -428,6 +484,9 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             const int hh = item_head(it);
             const float lam = p.lambda[hh * p.lambda_stride];
             const int row0 = item_row0(it);
+            // masking only where a row or key passes the sequence end or (causal) a row
+            // precedes a key of the tile: the first two blocks and the last one
+            const bool need_mask = row0 + BQ > len || kt * BK + BK > len || (p.causal && row0 < kt * BK + BK - 1);
 #pragma unroll 1
             for (int ch = 0; ch < 2; ++ch) {  // query rows [32 ch, 32 ch + 32) of the block
                 uint32_t s1[32], s2[32], dp[32];
@@ -436,26 +495,10 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 tmem_ld32(tmem + lo + 128 + ch * 32, dp);
                 tmem_wait_ld();
                 uint32_t pc[16], d1[16], d2[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float a[2], b1[2], b2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int rr = ch * 32 + i + u;
-                        const int qi = row0 + rr;
-                        const bool vis = key_ok && qi < len && (!p.causal || kj <= qi);
-                        const float4 st = stat[rr];  // lse1, lse2, delta1, delta2 of query row rr
-                        const float pp = __uint_as_float(dp[i + u]);
-                        const float p1 = vis ? ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x)) : 0.f;
-                        const float p2 = vis ? ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y)) : 0.f;
-                        a[u] = p1 - lam * p2;
-                        b1[u] = vis ? p1 * (pp - st.z) * sc : 0.f;
-                        b2[u] = vis ? -lam * p2 * (pp - st.w) * sc : 0.f;
-                    }
-                    pc[i / 2] = pack_bf16x2(a[0], a[1]);
-                    d1[i / 2] = pack_bf16x2(b1[0], b1[1]);
-                    d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
-                }
+                if (need_mask)
+                    dkv_rows32<true>(s1, s2, dp, stat + ch * 32, lam, sl2, sc, row0 + ch * 32, q_end, q_min, pc, d1, d2);
+                else
+                    dkv_rows32<false>(s1, s2, dp, stat + ch * 32, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
                 // rows [32 ch, +32) -> columns [16 ch, +16) of the S1^T / S2^T / dP^T regions (already read)
                 tmem_st16(tmem + lo + ch * 16, pc);
                 tmem_st16(tmem + lo + 64 + ch * 16, d1);
