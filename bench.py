@@ -34,6 +34,9 @@ FLOP_PER_PAIR = 768
 WORKLOAD = "long_t16384"
 KERNEL_SRC = os.path.join(ROOT, "differential_attention_diffattn_gb300", "csrc", "fwd_sm103a.cu")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fwd_bf16_sm103a_long_t16384.md")
+# rotary placements: (rot_dim in units of d, interleaved)
+ROPE_PLACEMENTS = {"row2d_half": (2, False), "comp_interleaved": (1, True)}
+ROPE_THETA = 10000.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -163,12 +166,33 @@ def run_ours(args, rank, world, local_rank):
     cu = inp.cu_seqlens.to(dev)
     lam = torch.empty(1 if not wl.lambda_per_head else wl.num_heads, dtype=torch.float32, device=dev)
 
-    def fwd(s):
+    rope = ROPE_PLACEMENTS.get(args.rope)
+    if rope is not None:
+        # q, k arrive before the rotary embedding: each step rotates them into
+        # scratch tensors that the attention then reads
+        rot_dim = rope[0] * wl.d
+        cos, sin = da.diffattn_rope_tables(ROPE_THETA, inp.max_seqlen, rot_dim)
+        for s in sets:
+            s["qr"], s["kr"] = torch.empty_like(s["q"]), torch.empty_like(s["k"])
+    rope_bytes = 2 * (inp.q.numel() + inp.k.numel()) * inp.q.element_size()
+    rope_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if rope is not None else None
+
+    def fwd(s, i=None):
+        q, k = s["q"], s["k"]
+        if rope is not None:
+            if i is not None:
+                rope_ev[i][0].record(stream)
+            da.diffattn_rope_qk(q, k, cos, sin, rot_dim, rope[1], cu_seqlens=cu if packed else None,
+                                q_out=s["qr"], k_out=s["kr"], stream=stream)
+            if i is not None:
+                rope_ev[i][1].record(stream)
+            q, k = s["qr"], s["kr"]
         if packed:
-            da.diffattn_fwd(s["q"], s["k"], s["v"], lam, li, w, causal=wl.causal, cu_seqlens=cu,
+            da.diffattn_fwd(q, k, s["v"], lam, li, w, causal=wl.causal, cu_seqlens=cu,
                             max_seqlen=inp.max_seqlen, eps=wl.eps, out=s["out"], stream=stream)
         else:
-            da.diffattn_fwd(s["q"], s["k"], s["v"], lam, li, w, causal=wl.causal, eps=wl.eps, out=s["out"],
+            da.diffattn_fwd(q, k, s["v"], lam, li, w, causal=wl.causal, eps=wl.eps, out=s["out"],
                             stream=stream)
 
     def step(i):
@@ -195,7 +219,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.steps):
         da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
         ev[i][0].record(stream)
-        fwd(sets[i % 2])
+        fwd(sets[i % 2], i)
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -204,6 +228,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
     elapsed_ms = t0.elapsed_time(t1)
     fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    rope_ms = sum(a.elapsed_time(b) for a, b in rope_ev) / args.steps if rope is not None else 0.0
+    fwd_ms -= rope_ms  # the attention kernel alone
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the timed region")
     elapsed_ms = shard.max_over_ranks(elapsed_ms)
@@ -275,9 +301,16 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "diffattn_fwd_bf16_sm103a_kernel", "launch_ms": round(fwd_ms, 4),
                      "algorithmic_flop_per_launch": flops_step},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if rope is not None else 2) * args.steps,
         "impl": "ours",
     }
+    if rope is not None:
+        line["metric"] = METRIC + " (with rotary embedding of q, k)"
+        line["config"]["rope"] = {"placement": args.rope, "rot_dim": rot_dim, "interleaved": rope[1],
+                                  "theta": ROPE_THETA}
+        line["rope"] = {"kernel": "diffattn_rope_qk_kernel", "ms": round(rope_ms, 5), "bytes": rope_bytes,
+                        "gbs": round(rope_bytes / (rope_ms * 1e-3) / 1e9, 1),
+                        "frac_of_hbm": round(rope_bytes / (rope_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4)}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.cpu_stride)
     return line
@@ -624,6 +657,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
     ap.add_argument("--backward", action="store_true", help="time forward + backward (training step)")
+    ap.add_argument("--rope", choices=sorted(ROPE_PLACEMENTS), default=None,
+                    help="rotate q, k (pre-rotary inputs) inside each step before the attention")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     DiffAttnDesc,
     DiffAttnError,
     DiffAttnKvDesc,
+    DiffAttnRopeDesc,
     diffattn_bwd,
     diffattn_bwd_workspace_size,
     diffattn_fwd,
@@ -20,6 +21,8 @@ from ._lib import (  # noqa: F401
     diffattn_lambda,
     diffattn_lambda_bwd,
     diffattn_lambda_init,
+    diffattn_rope_qk,
+    diffattn_rope_tables,
     diffattn_set_fault_injection,
     diffattn_set_wait_timeout_ns,
     diffattn_status_string,

@@ -1,7 +1,7 @@
 """Builds libdiffattn.so in-tree with nvcc for sm_103a.
 
-Three translation units compile in parallel (host ABI, CUDA-core kernels, the
-tcgen05 kernel) and link into one shared library with the CUDA runtime linked
+The translation units (host ABI, CUDA-core kernels, tcgen05 kernels) compile
+in parallel and link into one shared library with the CUDA runtime linked
 statically. No cmake, no torch extension machinery.
 """
 from __future__ import annotations
@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdiffattn.so")
 INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
-SOURCES = ["diffattn_api.cu", "fwd_simt.cu", "fwd_sm103a.cu", "decode_simt.cu", "bwd_simt.cu", "bwd_sm103a.cu"]
+SOURCES = ["diffattn_api.cu", "fwd_simt.cu", "fwd_sm103a.cu", "decode_simt.cu", "bwd_simt.cu", "bwd_sm103a.cu",
+           "rope_simt.cu"]
 HEADERS = ["internal.h", "sm103a_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

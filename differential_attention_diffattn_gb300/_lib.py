@@ -14,14 +14,15 @@ from typing import Optional
 
 from . import _build
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS, ERR_BAD_POSITIONS = range(7)
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 # Names the header declares with external linkage (checked by the ABI tests).
 EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn_fwd_train",
             "diffattn_bwd_workspace_size", "diffattn_bwd", "diffattn_lambda_bwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
-            "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection")
+            "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
+            "diffattn_rope_tables", "diffattn_rope_qk")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -35,6 +36,13 @@ class DiffAttnKvDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("cache_capacity", ctypes.c_int),
                 ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("d", ctypes.c_int),
                 ("dv", ctypes.c_int), ("dtype", ctypes.c_int), ("eps", ctypes.c_float), ("num_splits", ctypes.c_int)]
+
+
+class DiffAttnRopeDesc(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_longlong), ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("d", ctypes.c_int), ("dtype", ctypes.c_int), ("rot_dim", ctypes.c_int),
+                ("interleaved", ctypes.c_int), ("n_pos", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("seqlen", ctypes.c_int)]
 
 
 class DiffAttnError(RuntimeError):
@@ -92,6 +100,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
         lib.diffattn_set_fault_injection.restype = None
         lib.diffattn_set_fault_injection.argtypes = [ctypes.c_int]
+        lib.diffattn_rope_tables.restype = ctypes.c_int
+        lib.diffattn_rope_tables.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        lib.diffattn_rope_qk.restype = ctypes.c_int
+        lib.diffattn_rope_qk.argtypes = [ctypes.POINTER(DiffAttnRopeDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
         del fp, ip
         if path is None:
             _lib = lib
@@ -440,3 +452,72 @@ def diffattn_set_wait_timeout_ns(ns: int) -> None:
 
 def diffattn_set_fault_injection(mode: int) -> None:
     load_library().diffattn_set_fault_injection(int(mode))
+
+
+# ------------------------------------------------------------- rotary ---
+
+def diffattn_rope_tables(theta: float, n_pos: int, rot_dim: int, device=None, stream=None):
+    """(cos, sin) fp32 [n_pos, rot_dim/2] on the device: p * theta^(-2i/rot_dim),
+    computed in fp64 by the kernel."""
+    import torch
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    cos = torch.empty(n_pos, rot_dim // 2, dtype=torch.float32, device=dev)
+    sin = torch.empty_like(cos)
+    st = load_library().diffattn_rope_tables(float(theta), int(n_pos), int(rot_dim), _ptr(cos), _ptr(sin),
+                                             _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_rope_tables")
+    return cos, sin
+
+
+def diffattn_rope_qk(q, k, cos, sin, rot_dim: int, interleaved: bool, positions=None, cu_seqlens=None,
+                     q_out=None, k_out=None, stream=None):
+    """Rotate q [tokens, H, 2d] (or [B, T, H, 2d]) and k (same layout with Hkv
+    heads, or None). Positions: `positions` int32 [tokens] if given, else
+    `cu_seqlens` (packed sequences), else the dense layout. Pass q_out=q /
+    k_out=k to rotate in place. Returns (q_out, k_out)."""
+    import torch
+    _check_cuda(q, "q")
+    if q.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    desc = DiffAttnRopeDesc()
+    H, two_d = q.shape[-2], q.shape[-1]
+    desc.tokens = q.numel() // (H * two_d)
+    desc.num_heads, desc.d, desc.dtype = H, two_d // 2, dt
+    desc.rot_dim, desc.interleaved = int(rot_dim), 1 if interleaved else 0
+    desc.n_pos = cos.shape[0]
+    if k is not None:
+        _check_cuda(k, "k")
+        if k.dtype != q.dtype or k.shape[:-2] != q.shape[:-2] or k.shape[-1] != two_d:
+            raise ValueError("k must match q's dtype, token dims and head width")
+        desc.num_kv_heads = k.shape[-2]
+    for t, name in ((cos, "cos"), (sin, "sin")):
+        _check_cuda(t, name)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be fp32")
+    if positions is not None:
+        _check_cuda(positions, "positions")
+        if positions.dtype != torch.int32 or positions.numel() != desc.tokens:
+            raise ValueError("positions must be int32 [tokens]")
+    elif cu_seqlens is not None:
+        _check_cuda(cu_seqlens, "cu_seqlens")
+        if cu_seqlens.dtype != torch.int32:
+            raise ValueError("cu_seqlens must be int32")
+        desc.num_seqs = cu_seqlens.numel() - 1
+    else:
+        desc.seqlen = q.shape[1] if q.dim() == 4 else q.shape[0]
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    st = load_library().diffattn_rope_qk(ctypes.byref(desc), _ptr(positions) if positions is not None else None,
+                                         _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(cos),
+                                         _ptr(sin), _ptr(q), _ptr(q_out), _ptr(k) if k is not None else None,
+                                         _ptr(k_out) if k is not None else None, _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_rope_qk")
+    return q_out, k_out

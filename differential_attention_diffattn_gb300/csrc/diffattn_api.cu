@@ -479,6 +479,70 @@ diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const fl
                : DIFFATTN_ERR_CUDA;
 }
 
+// --------------------------------------------------------------- rotary ---
+
+diffattn_status diffattn_rope_tables(double theta, int n_pos, int rot_dim, float* cos_out, float* sin_out,
+                                     void* stream) {
+    if (!cos_out || !sin_out || n_pos < 1 || rot_dim < 2 || (rot_dim & 1) || !(theta > 0.0) || !std::isfinite(theta))
+        return DIFFATTN_ERR_INVALID_ARG;
+    return launch_rope_tables(theta, n_pos, rot_dim, cos_out, sin_out, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
+diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* positions, const int* cu_seqlens,
+                                 const float* cos_table, const float* sin_table, const void* q_in, void* q_out,
+                                 const void* k_in, void* k_out, void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_rope_desc& ds = *desc;
+    if (ds.tokens < 0 || ds.num_heads < 1 || ds.num_kv_heads < 0 || ds.d < 4 || (ds.d % 4) != 0 || ds.n_pos < 1)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if ((ds.rot_dim != ds.d && ds.rot_dim != 2 * ds.d) || (ds.rot_dim % 8) != 0) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.tokens == 0) return DIFFATTN_OK;
+    if (!cos_table || !sin_table || !q_in || !q_out) return DIFFATTN_ERR_INVALID_ARG;
+    if (!aligned16(cos_table) || !aligned16(sin_table) || !aligned16(q_in) || !aligned16(q_out))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.num_kv_heads > 0 && (!k_in || !k_out || !aligned16(k_in) || !aligned16(k_out)))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (!positions) {
+        if (cu_seqlens) {
+            if (ds.num_seqs < 1 || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return DIFFATTN_ERR_INVALID_ARG;
+        } else if (ds.seqlen < 1) {
+            return DIFFATTN_ERR_INVALID_ARG;
+        }
+    } else if ((reinterpret_cast<uintptr_t>(positions) & 3u) != 0) {
+        return DIFFATTN_ERR_INVALID_ARG;
+    }
+    if (ds.tokens * (long long)(ds.num_heads + ds.num_kv_heads) * (2 * ds.d) >= (1LL << 40))
+        return DIFFATTN_ERR_INVALID_ARG;
+    unsigned int* err_word = nullptr;
+    if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    RopeParams p{};
+    p.q_in = q_in;
+    p.q_out = q_out;
+    p.k_in = ds.num_kv_heads > 0 ? k_in : nullptr;
+    p.k_out = ds.num_kv_heads > 0 ? k_out : nullptr;
+    p.positions = positions;
+    p.cu_seqlens = positions ? nullptr : cu_seqlens;
+    p.cos = cos_table;
+    p.sin = sin_table;
+    p.error_word = err_word;
+    p.tokens = ds.tokens;
+    p.H = ds.num_heads;
+    p.Hkv = ds.num_kv_heads;
+    p.width = 2 * ds.d;
+    p.rot_dim = ds.rot_dim;
+    p.n_pos = ds.n_pos;
+    p.num_seqs = ds.num_seqs;
+    p.seqlen = ds.seqlen;
+    return launch_rope_qk(p, ds.dtype == DIFFATTN_DTYPE_BF16, ds.interleaved != 0, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
 diffattn_status diffattn_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     unsigned int word = 0;
@@ -488,6 +552,7 @@ diffattn_status diffattn_get_device_status(void* stream) {
         if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     }
     if (word & kErrBadSeqlens) return DIFFATTN_ERR_BAD_SEQLENS;
+    if (word & kErrBadPositions) return DIFFATTN_ERR_BAD_POSITIONS;
     if (word & kErrTimeout) return DIFFATTN_ERR_TIMEOUT;
     return DIFFATTN_OK;
 }
@@ -500,6 +565,7 @@ const char* diffattn_status_string(diffattn_status s) {
         case DIFFATTN_ERR_CUDA: return "CUDA error";
         case DIFFATTN_ERR_TIMEOUT: return "kernel pipeline wait timed out";
         case DIFFATTN_ERR_BAD_SEQLENS: return "invalid cu_seqlens";
+        case DIFFATTN_ERR_BAD_POSITIONS: return "rotary position outside the tables";
     }
     return "unknown status";
 }

@@ -8,7 +8,7 @@
 namespace diffattn {
 
 // Bits of the per-device error word written by kernels.
-enum : uint32_t { kErrTimeout = 1u, kErrBadSeqlens = 2u };
+enum : uint32_t { kErrTimeout = 1u, kErrBadSeqlens = 2u, kErrBadPositions = 4u };
 
 // Default limit of every bounded pipeline wait inside a kernel.
 constexpr unsigned long long kDefaultWaitTimeoutNs = 2000000000ull;
@@ -112,6 +112,21 @@ struct BwdPreParams {
     float* dsubln_w;           // out (accumulated): [dv]
 };
 
+// Rotary embedding of q [tokens][H][width] and k [tokens][Hkv][width] (width = 2d).
+struct RopeParams {
+    const void* q_in;
+    void* q_out;
+    const void* k_in;          // may be null with Hkv = 0
+    void* k_out;
+    const int* positions;      // [tokens] or null
+    const int* cu_seqlens;     // [num_seqs + 1] or null
+    const float* cos;          // [n_pos][rot_dim / 2]
+    const float* sin;
+    unsigned int* error_word;
+    long long tokens;
+    int H, Hkv, width, rot_dim, n_pos, num_seqs, seqlen;
+};
+
 // Kernel launchers (each defined in its own translation unit). They return the
 // cudaError_t of the launch.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
@@ -124,6 +139,9 @@ cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& maps, cud
 cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                               const float* dlambda, int n_sets, int d, float* dlq1, float* dlk1, float* dlq2,
                               float* dlk2, cudaStream_t stream);
+cudaError_t launch_rope_tables(double theta, int n_pos, int rot_dim, float* cos_out, float* sin_out,
+                               cudaStream_t stream);
+cudaError_t launch_rope_qk(const RopeParams& p, bool bf16, bool interleaved, cudaStream_t stream);
 int decode_rows_supported(int rows);
 int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
 int decode_max_splits();           // most key splits the combine kernel merges

@@ -46,7 +46,8 @@ typedef enum {
     DIFFATTN_ERR_UNSUPPORTED = 2,   /* valid request outside the built kernels' shapes */
     DIFFATTN_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed             */
     DIFFATTN_ERR_TIMEOUT = 4,       /* a kernel pipeline wait gave up (device status)  */
-    DIFFATTN_ERR_BAD_SEQLENS = 5    /* cu_seqlens not monotone / out of range (device) */
+    DIFFATTN_ERR_BAD_SEQLENS = 5,   /* cu_seqlens not monotone / out of range (device) */
+    DIFFATTN_ERR_BAD_POSITIONS = 6  /* a rotary position outside the tables (device)  */
 } diffattn_status;
 
 typedef enum {
@@ -286,9 +287,61 @@ diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const
                                              int causal, void* out, void* stream);
 
 /*
+ * Rotary position embedding ahead of the attention.
+ *
+ * Passages: "LlamaDiffSdpaAttention.py", forward ("Apply RoPE before splitting":
+ * apply_rotary_pos_emb on the whole 2d-wide head row, half-split pairs, then the
+ * q1 | q2 chunk) and "Add an isolated implementation of FlashDiffAttention"
+ * (test script: apply_rotary_emb(..., interleaved=True) on the doubled d-wide
+ * heads). Both are this rule: each head row of width 2d is split into segments
+ * of rot_dim coordinates; in a segment, pair i < rot_dim/2 is (i, i + rot_dim/2)
+ * (interleaved = 0) or (2i, 2i+1) (interleaved = 1), rotated by the angle
+ * pos * theta^(-2i/rot_dim):  a' = a cos - b sin,  b' = b cos + a sin.
+ * rot_dim = 2d gives the Llama placement, rot_dim = d the doubled-head one.
+ */
+typedef struct diffattn_rope_desc {
+    long long tokens;   /* rows of q (and of k)                                         */
+    int num_heads;      /* H: q is [tokens][H][2d]                                      */
+    int num_kv_heads;   /* Hkv: k is [tokens][Hkv][2d]; 0 rotates q only                */
+    int d;              /* component dim; head rows are 2d wide; d % 4 == 0             */
+    int dtype;          /* diffattn_dtype of q and k                                     */
+    int rot_dim;        /* d or 2d                                                       */
+    int interleaved;    /* 0: pairs (i, i + rot_dim/2); 1: pairs (2i, 2i+1)              */
+    int n_pos;          /* rows of the cos / sin tables                                  */
+    int num_seqs;       /* > 0 with cu_seqlens: positions restart at every sequence      */
+    int seqlen;         /* dense batches (no positions, no cu_seqlens): pos = t % seqlen */
+} diffattn_rope_desc;
+
+/*
+ * Fills cos_out, sin_out (device fp32 [n_pos][rot_dim/2], caller-owned) with
+ * cos / sin of p * theta^(-2i/rot_dim), computed in fp64 on the device and
+ * rounded once (the pages' modules cache these tables and cast them to bf16).
+ * Errors: INVALID_ARG for null pointers, n_pos < 1, odd or non-positive rot_dim,
+ * theta <= 0; CUDA if the launch fails. Asynchronous on `stream`.
+ */
+diffattn_status diffattn_rope_tables(double theta, int n_pos, int rot_dim, float* cos_out, float* sin_out,
+                                     void* stream);
+
+/*
+ * Rotates q (and k) with the tables of diffattn_rope_tables. Positions come
+ * from `positions` (device int32 [tokens], e.g. a decode step's cache offsets)
+ * if given, else from `cu_seqlens` (device int32 [num_seqs + 1]: position = token
+ * index inside its sequence), else from the dense layout (t % seqlen).
+ * q_out may equal q_in and k_out k_in (in place); all device pointers are
+ * caller-owned and 16-byte aligned; k_in / k_out are ignored when num_kv_heads
+ * is 0. A position outside [0, n_pos) leaves that row unrotated (copied through)
+ * and makes diffattn_get_device_status return DIFFATTN_ERR_BAD_POSITIONS.
+ * Errors: INVALID_ARG for null or misaligned pointers, rot_dim not d or 2d,
+ * rot_dim % 8 != 0, a missing position source; CUDA if the launch fails.
+ */
+diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* positions, const int* cu_seqlens,
+                                 const float* cos_table, const float* sin_table, const void* q_in, void* q_out,
+                                 const void* k_in, void* k_out, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
- * Returns OK, TIMEOUT, BAD_SEQLENS (first error recorded since the last read),
- * or CUDA if the synchronisation itself failed.
+ * Returns OK, TIMEOUT, BAD_SEQLENS, BAD_POSITIONS (the first error recorded since
+ * the last read), or CUDA if the synchronisation itself failed.
  */
 diffattn_status diffattn_get_device_status(void* stream);
 

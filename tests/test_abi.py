@@ -43,8 +43,8 @@ def test_lambda_init_host(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
-        assert da.diffattn_status_string(s)
+    for s in range(7):
+        assert da.diffattn_status_string(s) != "unknown status"
     assert da.diffattn_status_string(99) == "unknown status"
 
 
@@ -103,3 +103,44 @@ def test_lambda_rejects_on_host(lib):
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(RuntimeError):
         _lib.load_library(str(tmp_path / "missing.so"))
+
+
+def _rope_desc(**kw):
+    d = _lib.DiffAttnRopeDesc()
+    base = dict(tokens=16, num_heads=4, num_kv_heads=2, d=64, dtype=_lib.DTYPE_BF16, rot_dim=64, interleaved=1,
+                n_pos=16, num_seqs=0, seqlen=16)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+def _rope(lib, desc, pos=None, cu=None, cos=FAKE, sin=FAKE, q=FAKE, qo=FAKE, k=FAKE, ko=FAKE):
+    vp = ctypes.c_void_p
+    w = lambda x: vp(x) if x else None  # noqa: E731
+    return lib.diffattn_rope_qk(ctypes.byref(desc), w(pos), w(cu), w(cos), w(sin), w(q), w(qo), w(k), w(ko), None)
+
+
+@pytest.mark.parametrize("kw,ptrs,want", [
+    (dict(rot_dim=32), {}, 1),                  # neither d nor 2d
+    (dict(d=12, rot_dim=12), {}, 1),            # rot_dim % 8 != 0
+    (dict(n_pos=0), {}, 1),
+    (dict(dtype=5), {}, 1),
+    (dict(seqlen=0), {}, 1),                    # no position source
+    (dict(num_seqs=0), dict(cu=FAKE), 1),       # cu_seqlens without sequences
+    ({}, dict(q=0), 1),
+    ({}, dict(k=0), 1),                         # k missing while num_kv_heads > 0
+    ({}, dict(cos=FAKE + 4), 1),                # misaligned table
+    ({}, dict(pos=FAKE + 2), 1),                # misaligned positions
+    (dict(tokens=0), {}, 0),                    # empty: nothing to launch
+])
+def test_rope_rejects_on_host(lib, kw, ptrs, want):
+    assert _rope(lib, _rope_desc(**kw), **ptrs) == want
+
+
+def test_rope_tables_reject_on_host(lib):
+    vp = ctypes.c_void_p
+    assert lib.diffattn_rope_tables(10000.0, 0, 64, vp(FAKE), vp(FAKE), None) == 1
+    assert lib.diffattn_rope_tables(10000.0, 8, 63, vp(FAKE), vp(FAKE), None) == 1
+    assert lib.diffattn_rope_tables(-1.0, 8, 64, vp(FAKE), vp(FAKE), None) == 1
+    assert lib.diffattn_rope_tables(10000.0, 8, 64, None, vp(FAKE), None) == 1
