@@ -474,6 +474,104 @@ def run_ours_bwd(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------------- context-parallel split (GPU) ---
+
+def run_ours_cp(args, rank, world, local_rank):
+    """One long sequence split into 2N zigzag chunks. With one process the N
+    ranks' blocks (training-forward partials + merges) run one rank after
+    another on this GPU; under torchrun each rank runs its own chunks and the
+    K/V chunks go around an NCCL ring."""
+    import torch
+
+    import differential_attention_diffattn_gb300 as da
+    from differential_attention_diffattn_gb300 import context_parallel as cp
+    from differential_attention_diffattn_gb300 import shard
+    from differential_attention_diffattn_gb300 import workloads as W
+
+    da.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    inp = W.generate(wl, seed=args.seed)
+    if len(inp.seq_lens) != 1:
+        raise SystemExit("--cp splits one sequence: pick a single-sequence workload")
+    n_ranks = world if world > 1 else args.cp
+    T = inp.tokens
+    chunk = T // (2 * n_ranks)
+    if chunk * 2 * n_ranks != T or chunk % 128 != 0:
+        raise SystemExit(f"{T} tokens do not split into {2 * n_ranks} chunks of a multiple of 128")
+    flops = FLOP_PER_PAIR * causal_pairs(inp.seq_lens, wl.num_heads)
+    li = da.diffattn_lambda_init(wl.depth)
+    lvec = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    lam = da.diffattn_lambda(*lvec, li)
+    w = inp.subln_w.to(dev)
+    stream = torch.cuda.current_stream()
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    kern = cp.GpuKernels(lam, li, w, wl.eps, stream=stream)
+    merge_ev = []
+
+    class Timed(cp.GpuKernels):
+        def merge(self, parts, n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            y = super().merge(parts, n)
+            b.record(stream)
+            merge_ev.append((a, b, n))
+            return y
+    kern = Timed(lam, li, w, wl.eps, stream=stream)
+    kv = {b: (k[b * chunk:(b + 1) * chunk], v[b * chunk:(b + 1) * chunk]) for b in range(2 * n_ranks)}
+
+    def step():
+        if world > 1:
+            return cp.ring_forward(cp.split_zigzag(q, world, rank), cp.split_zigzag(k, world, rank),
+                                   cp.split_zigzag(v, world, rank), kern)
+        outs = {}
+        for r in range(n_ranks):
+            outs.update(cp.local_forward(cp.split_zigzag(q, n_ranks, r), kv, kern))
+        return outs
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    merge_ev.clear()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        outs = step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if da.diffattn_get_device_status() != 0:
+        raise RuntimeError("device reported an error in the timed region")
+    elapsed = shard.max_over_ranks(t0.elapsed_time(t1))
+    merge_ms = sum(a.elapsed_time(b) for a, b, _ in merge_ev) / args.steps
+    merge_bytes = sum(n * chunk * wl.num_heads * (2 * wl.dv * 4 + 8) + chunk * wl.num_heads * wl.dv * 2
+                      for _, _, n in merge_ev) // args.steps
+    if rank != 0:
+        return None
+    if not all(torch.isfinite(y.float()).all() for y in outs.values()):
+        raise RuntimeError("non-finite output")
+    pk, pk_kind = peaks()
+    return {
+        "metric": "diff-attn fwd TFLOP/s (causal), context-parallel split", "value":
+            round(flops * args.steps / (elapsed * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps, 4),
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": T, "diff_heads": wl.num_heads, "kv_heads": wl.num_kv_heads,
+                   "cp_ranks": n_ranks, "chunk": chunk,
+                   "emulated_on_one_gpu": world == 1, "flop_per_step": flops},
+        "merge": {"kernel": "diffattn_merge_kernel", "ms": round(merge_ms, 5), "bytes": merge_bytes,
+                  "gbs": round(merge_bytes / (merge_ms * 1e-3) / 1e9, 1) if merge_ms > 0 else None,
+                  "frac_of_hbm": round(merge_bytes / (merge_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4)
+                  if merge_ms > 0 else None},
+        # per rank: 2N + 1 training-forward partials and 2 merges
+        "gpu_launches": (n_ranks if world == 1 else 1) * (2 * n_ranks + 3) * args.steps, "impl": "ours",
+    }
+
+
 # ------------------------------------------------- cache forward (GPU) ---
 
 def run_ours_kv(args, rank, world, local_rank):
@@ -657,6 +755,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
     ap.add_argument("--backward", action="store_true", help="time forward + backward (training step)")
+    ap.add_argument("--cp", type=int, default=0,
+                    help="context-parallel split of one sequence over N ranks (emulated on one GPU when run alone)")
     ap.add_argument("--rope", choices=sorted(ROPE_PLACEMENTS), default=None,
                     help="rotate q, k (pre-rotary inputs) inside each step before the attention")
     args = ap.parse_args()
@@ -683,6 +783,8 @@ def main():
         from differential_attention_diffattn_gb300 import workloads as W
         if args.workload in W.KV_WORKLOADS:
             runner = run_ours_kv
+        elif args.cp:
+            runner = run_ours_cp
         else:
             runner = run_ours_bwd if args.backward else run_ours
         line = runner(args, rank, world, local_rank)

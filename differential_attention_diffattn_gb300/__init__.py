@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     DiffAttnDesc,
     DiffAttnError,
     DiffAttnKvDesc,
+    DiffAttnMergeDesc,
     DiffAttnRopeDesc,
     diffattn_bwd,
     diffattn_bwd_workspace_size,
@@ -21,6 +22,7 @@ from ._lib import (  # noqa: F401
     diffattn_lambda,
     diffattn_lambda_bwd,
     diffattn_lambda_init,
+    diffattn_merge_partials,
     diffattn_rope_qk,
     diffattn_rope_tables,
     diffattn_set_fault_injection,

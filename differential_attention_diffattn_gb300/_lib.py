@@ -22,7 +22,7 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_bwd_workspace_size", "diffattn_bwd", "diffattn_lambda_bwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
-            "diffattn_rope_tables", "diffattn_rope_qk")
+            "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -43,6 +43,11 @@ class DiffAttnRopeDesc(ctypes.Structure):
                 ("d", ctypes.c_int), ("dtype", ctypes.c_int), ("rot_dim", ctypes.c_int),
                 ("interleaved", ctypes.c_int), ("n_pos", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("seqlen", ctypes.c_int)]
+
+
+class DiffAttnMergeDesc(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_longlong), ("num_heads", ctypes.c_int), ("dv", ctypes.c_int),
+                ("n_parts", ctypes.c_int), ("out_dtype", ctypes.c_int), ("eps", ctypes.c_float)]
 
 
 class DiffAttnError(RuntimeError):
@@ -104,6 +109,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_rope_tables.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         lib.diffattn_rope_qk.restype = ctypes.c_int
         lib.diffattn_rope_qk.argtypes = [ctypes.POINTER(DiffAttnRopeDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.diffattn_merge_partials.restype = ctypes.c_int
+        lib.diffattn_merge_partials.argtypes = [ctypes.POINTER(DiffAttnMergeDesc), vp, vp, vp, vp, ctypes.c_int,
+                                                ctypes.c_float, vp, vp, vp]
         del fp, ip
         if path is None:
             _lib = lib
@@ -521,3 +529,34 @@ def diffattn_rope_qk(q, k, cos, sin, rot_dim: int, interleaved: bool, positions=
     if st != OK:
         raise DiffAttnError(st, "diffattn_rope_qk")
     return q_out, k_out
+
+
+# -------------------------------------------------------------- merge ---
+
+def diffattn_merge_partials(lse, o1, o2, lam, lambda_init: float, subln_w, eps: float = 1e-5, out=None,
+                            out_dtype=None, stream=None):
+    """Merge stacked partials lse [n, ..., H, 2], o1 / o2 [n, ..., H, dv] (fp32,
+    as diffattn_fwd_train saves them per key block) into the forward output
+    [..., H, dv] (bf16 unless `out_dtype` or `out` says otherwise)."""
+    import torch
+    for t, name in ((lse, "lse"), (o1, "o1"), (o2, "o2"), (lam, "lambda"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be fp32")
+    n, H, dv = o1.shape[0], o1.shape[-2], o1.shape[-1]
+    if o2.shape != o1.shape or lse.shape[:-1] != o1.shape[:-1] or lse.shape[-1] != 2:
+        raise ValueError("partials disagree in shape")
+    if out is None:
+        out = torch.empty(o1.shape[1:], dtype=out_dtype or torch.bfloat16, device=o1.device)
+    _check_cuda(out, "out")
+    desc = DiffAttnMergeDesc()
+    desc.tokens = o1[0].numel() // (H * dv)
+    desc.num_heads, desc.dv, desc.n_parts = H, dv, n
+    desc.out_dtype = DTYPE_BF16 if out.dtype == torch.bfloat16 else DTYPE_F32
+    desc.eps = float(eps)
+    st = load_library().diffattn_merge_partials(ctypes.byref(desc), _ptr(lse), _ptr(o1), _ptr(o2), _ptr(lam),
+                                                1 if (lam.numel() == H and H > 1) else 0, float(lambda_init),
+                                                _ptr(subln_w), _ptr(out), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_merge_partials")
+    return out

@@ -543,6 +543,40 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
                : DIFFATTN_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- merge ---
+
+diffattn_status diffattn_merge_partials(const diffattn_merge_desc* desc, const float* lse, const float* o1,
+                                        const float* o2, const float* lambda, int lambda_per_head,
+                                        float lambda_init, const float* subln_w, void* out, void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_merge_desc& ds = *desc;
+    if (ds.tokens < 0 || ds.num_heads < 1 || ds.dv < 4 || ds.dv > 512 || (ds.dv % 4) != 0 || ds.n_parts < 1)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.out_dtype != DIFFATTN_DTYPE_F32 && ds.out_dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.tokens == 0) return DIFFATTN_OK;
+    if (!lse || !o1 || !o2 || !lambda || !subln_w || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (!aligned16(lse) || !aligned16(o1) || !aligned16(o2) || !aligned16(subln_w) || !aligned16(out))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if ((long long)ds.n_parts * ds.tokens * ds.num_heads * ds.dv >= (1LL << 40)) return DIFFATTN_ERR_INVALID_ARG;
+    MergeParams p{};
+    p.lse = lse;
+    p.o1 = o1;
+    p.o2 = o2;
+    p.lambda = lambda;
+    p.lambda_stride = lambda_per_head ? 1 : 0;
+    p.lambda_init = lambda_init;
+    p.subln_w = subln_w;
+    p.eps = ds.eps;
+    p.out = out;
+    p.out_bf16 = ds.out_dtype == DIFFATTN_DTYPE_BF16;
+    p.tokens = ds.tokens;
+    p.H = ds.num_heads;
+    p.dv = ds.dv;
+    p.n_parts = ds.n_parts;
+    return launch_merge(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+
 diffattn_status diffattn_get_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     unsigned int word = 0;

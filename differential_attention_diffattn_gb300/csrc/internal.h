@@ -127,6 +127,22 @@ struct RopeParams {
     int H, Hkv, width, rot_dim, n_pos, num_seqs, seqlen;
 };
 
+// Merge of partials over key blocks (context-parallel split).
+struct MergeParams {
+    const float* lse;          // [n_parts][tokens][H][2]
+    const float* o1;           // [n_parts][tokens][H][dv]
+    const float* o2;
+    const float* lambda;       // [H] or [1]
+    int lambda_stride;
+    float lambda_init;
+    const float* subln_w;      // [dv]
+    float eps;
+    void* out;                 // [tokens][H][dv], bf16 or fp32
+    int out_bf16;
+    long long tokens;
+    int H, dv, n_parts;
+};
+
 // Kernel launchers (each defined in its own translation unit). They return the
 // cudaError_t of the launch.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
@@ -142,6 +158,7 @@ cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* l
 cudaError_t launch_rope_tables(double theta, int n_pos, int rot_dim, float* cos_out, float* sin_out,
                                cudaStream_t stream);
 cudaError_t launch_rope_qk(const RopeParams& p, bool bf16, bool interleaved, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 int decode_rows_supported(int rows);
 int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
 int decode_max_splits();           // most key splits the combine kernel merges

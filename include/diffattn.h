@@ -339,6 +339,41 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
                                  const void* k_in, void* k_out, void* stream);
 
 /*
+ * Context-parallel merge. The pages give no context-parallel scheme; it
+ * follows from the forward ("DiffTransformer.py",
+ * MultiHeadDifferentialAttention.forward): each component's softmax over all
+ * visible keys combines its softmaxes over disjoint key blocks, weighted by
+ * their sums of exponentials, and the combine with lambda and the RMSNorm (not
+ * linear) run after both merges. A part is what diffattn_fwd_train saves for
+ * one block of keys: lse_c (log2 of the sum of 2^(scaled score)) and O_c
+ * normalised over that block. Per (token, head) row and component, with
+ * L = max_j lse_c^j:  O_c = sum_j 2^(lse_c^j - L) O_c^j / sum_j 2^(lse_c^j - L);
+ * then out = RMSNorm(O_1 - lambda O_2) * w * (1 - lambda_init).
+ */
+typedef struct diffattn_merge_desc {
+    long long tokens;   /* query rows                                           */
+    int num_heads;      /* H                                                    */
+    int dv;             /* value width, a multiple of 4, at most 512            */
+    int n_parts;        /* key blocks, >= 1                                     */
+    int out_dtype;      /* diffattn_dtype of out                                */
+    float eps;          /* RMSNorm epsilon                                      */
+} diffattn_merge_desc;
+
+/*
+ * lse: device fp32 [n_parts][tokens][H][2]; o1, o2: device fp32
+ * [n_parts][tokens][H][dv] (parts stacked; a part in which a row sees no key
+ * has lse = -inf there and its O is not read); lambda fp32 [1] or [H]
+ * (lambda_per_head); subln_w fp32 [dv]; out [tokens][H][dv] in out_dtype. All
+ * device pointers caller-owned and 16-byte aligned. A row with no visible key
+ * in any part gets 0 for that component. Errors: INVALID_ARG for null or
+ * misaligned pointers and sizes outside the above; CUDA if the launch fails.
+ * Asynchronous on `stream`.
+ */
+diffattn_status diffattn_merge_partials(const diffattn_merge_desc* desc, const float* lse, const float* o1,
+                                        const float* o2, const float* lambda, int lambda_per_head,
+                                        float lambda_init, const float* subln_w, void* out, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns OK, TIMEOUT, BAD_SEQLENS, BAD_POSITIONS (the first error recorded since
  * the last read), or CUDA if the synchronisation itself failed.
