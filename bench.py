@@ -175,6 +175,15 @@ def run_ours(args, rank, world, local_rank):
         for s in sets:
             s["qr"], s["kr"] = torch.empty_like(s["q"]), torch.empty_like(s["k"])
     rope_bytes = 2 * (inp.q.numel() + inp.k.numel()) * inp.q.element_size()
+    hidden = wl.num_heads * wl.dv
+    if args.out_proj:
+        # o_proj = Linear(H * dv, hidden, bias=False) after the attention, hidden = H * dv
+        w_o = (torch.randn(hidden, hidden, generator=torch.Generator().manual_seed(args.seed + 7)) *
+               hidden ** -0.5).to(torch.bfloat16).to(dev)
+        for s in sets:
+            s["y"] = torch.empty(tokens, hidden, dtype=torch.bfloat16, device=dev)
+    proj_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] if args.out_proj else None
     rope_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] if rope is not None else None
 
@@ -194,6 +203,12 @@ def run_ours(args, rank, world, local_rank):
         else:
             da.diffattn_fwd(q, k, s["v"], lam, li, w, causal=wl.causal, eps=wl.eps, out=s["out"],
                             stream=stream)
+        if args.out_proj:
+            if i is not None:
+                proj_ev[i][0].record(stream)
+            da.diffattn_out_proj(s["out"], w_o, out=s["y"], stream=stream)
+            if i is not None:
+                proj_ev[i][1].record(stream)
 
     def step(i):
         da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
@@ -229,12 +244,14 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = t0.elapsed_time(t1)
     fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     rope_ms = sum(a.elapsed_time(b) for a, b in rope_ev) / args.steps if rope is not None else 0.0
-    fwd_ms -= rope_ms  # the attention kernel alone
+    proj_ms = sum(a.elapsed_time(b) for a, b in proj_ev) / args.steps if args.out_proj else 0.0
+    fwd_ms -= rope_ms + proj_ms  # the attention kernel alone
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the timed region")
     elapsed_ms = shard.max_over_ranks(elapsed_ms)
     ms_step = elapsed_ms / args.steps
-    value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+    step_flops = flops_step + (2 * tokens * hidden * hidden if args.out_proj else 0)
+    value = step_flops * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----------------
     host = {n: getattr(inp, n).pin_memory() for n in ("q", "k", "v", "subln_w", "cu_seqlens")}
@@ -268,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = shard.max_over_ranks(e2e_ms)
-    e2e_value = flops_step * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_value = step_flops * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the end-to-end region")
     if not torch.isfinite(out_h[:: max(1, tokens // 64)].float()).all():
@@ -287,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "batch": len(inp.seq_lens) if not packed else None,
                    "seq_len": inp.max_seqlen, "tokens": tokens, "diff_heads": wl.num_heads,
                    "kv_heads": wl.num_kv_heads, "d": wl.d, "dv": wl.dv, "depth": wl.depth,
-                   "causal": wl.causal, "flop_per_pair": FLOP_PER_PAIR, "flop_per_step": flops_step,
+                   "causal": wl.causal, "flop_per_pair": FLOP_PER_PAIR, "flop_per_step": step_flops,
                    "l2": "inputs larger than L2: two rotating ~256 MB input/output sets",
                    "inputs": "seeded N(0,1) q/k/v rounded to bf16, lambda vectors N(0,0.1^2) fp32, subln w = 1"},
         "tokens_per_s": round(tokens * world * args.steps / (elapsed_ms * 1e-3), 1),
@@ -301,9 +318,16 @@ def run_ours(args, rank, world, local_rank):
                      "kernel": "diffattn_fwd_bf16_sm103a_kernel", "launch_ms": round(fwd_ms, 4),
                      "algorithmic_flop_per_launch": flops_step},
         "clocks": clocks,
-        "gpu_launches": (3 if rope is not None else 2) * args.steps,
+        "gpu_launches": (2 + (rope is not None) + bool(args.out_proj)) * args.steps,
         "impl": "ours",
     }
+    if args.out_proj:
+        proj_flop = 2 * tokens * hidden * hidden
+        line["metric"] = METRIC + " (with o_proj)"
+        line["config"]["o_proj"] = {"in_features": hidden, "out_features": hidden}
+        line["out_proj"] = {"kernel": "diffattn_out_proj_kernel", "ms": round(proj_ms, 5), "flop": proj_flop,
+                            "tflops": round(proj_flop / (proj_ms * 1e-3) / 1e12, 1),
+                            "frac_of_bf16_peak": round(proj_flop / (proj_ms * 1e-3) / 1e12 / peak, 4)}
     if rope is not None:
         line["metric"] = METRIC + " (with rotary embedding of q, k)"
         line["config"]["rope"] = {"placement": args.rope, "rot_dim": rot_dim, "interleaved": rope[1],
@@ -755,6 +779,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
     ap.add_argument("--backward", action="store_true", help="time forward + backward (training step)")
+    ap.add_argument("--out-proj", action="store_true", help="run o_proj (H*dv -> H*dv) after the attention")
     ap.add_argument("--cp", type=int, default=0,
                     help="context-parallel split of one sequence over N ranks (emulated on one GPU when run alone)")
     ap.add_argument("--rope", choices=sorted(ROPE_PLACEMENTS), default=None,

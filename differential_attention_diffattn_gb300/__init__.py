@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     DiffAttnError,
     DiffAttnKvDesc,
     DiffAttnMergeDesc,
+    DiffAttnOutProjDesc,
     DiffAttnRopeDesc,
     diffattn_bwd,
     diffattn_bwd_workspace_size,
@@ -23,6 +24,7 @@ from ._lib import (  # noqa: F401
     diffattn_lambda_bwd,
     diffattn_lambda_init,
     diffattn_merge_partials,
+    diffattn_out_proj,
     diffattn_rope_qk,
     diffattn_rope_tables,
     diffattn_set_fault_injection,

@@ -22,7 +22,7 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_bwd_workspace_size", "diffattn_bwd", "diffattn_lambda_bwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
-            "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials")
+            "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -48,6 +48,10 @@ class DiffAttnRopeDesc(ctypes.Structure):
 class DiffAttnMergeDesc(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_longlong), ("num_heads", ctypes.c_int), ("dv", ctypes.c_int),
                 ("n_parts", ctypes.c_int), ("out_dtype", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+class DiffAttnOutProjDesc(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int), ("in_features", ctypes.c_int), ("out_features", ctypes.c_int)]
 
 
 class DiffAttnError(RuntimeError):
@@ -109,6 +113,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_rope_tables.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         lib.diffattn_rope_qk.restype = ctypes.c_int
         lib.diffattn_rope_qk.argtypes = [ctypes.POINTER(DiffAttnRopeDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.diffattn_out_proj.restype = ctypes.c_int
+        lib.diffattn_out_proj.argtypes = [ctypes.POINTER(DiffAttnOutProjDesc), vp, vp, vp, vp]
         lib.diffattn_merge_partials.restype = ctypes.c_int
         lib.diffattn_merge_partials.argtypes = [ctypes.POINTER(DiffAttnMergeDesc), vp, vp, vp, vp, ctypes.c_int,
                                                 ctypes.c_float, vp, vp, vp]
@@ -559,4 +565,32 @@ def diffattn_merge_partials(lse, o1, o2, lam, lambda_init: float, subln_w, eps: 
                                                 _ptr(subln_w), _ptr(out), _stream_handle(stream))
     if st != OK:
         raise DiffAttnError(st, "diffattn_merge_partials")
+    return out
+
+
+# ----------------------------------------------------------- out_proj ---
+
+def diffattn_out_proj(x, w, out=None, stream=None):
+    """y = x W^T: w bf16 [N, K]; x bf16 contiguous with K values per row (e.g.
+    the attention output [tokens, H, dv] or [B, T, H, dv] with K = H * dv).
+    Returns y bf16 [rows, N], rows = x.numel() / K."""
+    import torch
+    for t, name in ((x, "x"), (w, "w")):
+        _check_cuda(t, name)
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bf16")
+    if w.dim() != 2:
+        raise ValueError("w must be [N, K]")
+    N, K = w.shape
+    if x.numel() % K != 0:
+        raise ValueError(f"x does not hold rows of {K} values")
+    M = x.numel() // K
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check_cuda(out, "out")
+    desc = DiffAttnOutProjDesc()
+    desc.tokens, desc.in_features, desc.out_features = M, K, N
+    st = load_library().diffattn_out_proj(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(out), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_out_proj")
     return out

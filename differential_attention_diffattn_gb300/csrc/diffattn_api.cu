@@ -543,6 +543,34 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
                : DIFFATTN_ERR_CUDA;
 }
 
+// ------------------------------------------------------------- out_proj ---
+
+diffattn_status diffattn_out_proj(const diffattn_out_proj_desc* desc, const void* x, const void* w, void* y,
+                                  void* stream) {
+    if (!desc) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn_out_proj_desc& ds = *desc;
+    if (ds.tokens < 0 || ds.in_features < 8 || ds.out_features < 8 || (ds.in_features % 8) != 0 ||
+        (ds.out_features % 8) != 0)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.tokens == 0) return DIFFATTN_OK;
+    if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return DIFFATTN_ERR_INVALID_ARG;
+    unsigned int* err_word = nullptr;
+    if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
+    CUtensorMap tm_x, tm_w;
+    if (!encode_bf16_rows(&tm_x, x, (uint64_t)ds.in_features, (uint64_t)ds.tokens, 128) ||
+        !encode_bf16_rows(&tm_w, w, (uint64_t)ds.in_features, (uint64_t)ds.out_features, 256))
+        return DIFFATTN_ERR_CUDA;
+    GemmParams p{};
+    p.M = ds.tokens;
+    p.N = ds.out_features;
+    p.K = ds.in_features;
+    p.y = y;
+    p.error_word = err_word;
+    p.timeout_ns = g_timeout_ns;
+    return launch_out_proj(p, tm_x, tm_w, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK
+                                                                                             : DIFFATTN_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- merge ---
 
 diffattn_status diffattn_merge_partials(const diffattn_merge_desc* desc, const float* lse, const float* o1,

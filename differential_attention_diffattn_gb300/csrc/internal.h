@@ -143,6 +143,14 @@ struct MergeParams {
     int H, dv, n_parts;
 };
 
+// Output projection y[M][N] = x[M][K] W[N][K]^T (bf16).
+struct GemmParams {
+    int M, N, K;
+    void* y;
+    unsigned int* error_word;
+    unsigned long long timeout_ns;
+};
+
 // Kernel launchers (each defined in its own translation unit). They return the
 // cudaError_t of the launch.
 cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
@@ -159,6 +167,8 @@ cudaError_t launch_rope_tables(double theta, int n_pos, int rot_dim, float* cos_
                                cudaStream_t stream);
 cudaError_t launch_rope_qk(const RopeParams& p, bool bf16, bool interleaved, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_out_proj(const GemmParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                            cudaStream_t stream);
 int decode_rows_supported(int rows);
 int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
 int decode_max_splits();           // most key splits the combine kernel merges

@@ -374,6 +374,30 @@ diffattn_status diffattn_merge_partials(const diffattn_merge_desc* desc, const f
                                         float lambda_init, const float* subln_w, void* out, void* stream);
 
 /*
+ * Output projection after the attention. Passages: "LlamaDiffSdpaAttention.py",
+ * forward (the attention output reshaped to [tokens, H * dv] and passed through
+ * o_proj = nn.Linear(H * dv, hidden, bias=False)); "DiffTransformer.py" (W_o,
+ * no bias). nn.Linear stores W as [out_features][in_features]:
+ *   y[t][n] = sum_k x[t][k] W[n][k]        (bf16 in, fp32 accumulate, bf16 out)
+ */
+typedef struct diffattn_out_proj_desc {
+    int tokens;         /* M: rows of x and y                                   */
+    int in_features;    /* K = H * dv; a multiple of 8                          */
+    int out_features;   /* N; a multiple of 8                                   */
+} diffattn_out_proj_desc;
+
+/*
+ * x: device bf16 [tokens][in_features] (e.g. diffattn_fwd's output viewed as
+ * [tokens][H * dv]); w: device bf16 [out_features][in_features]; y: device bf16
+ * [tokens][out_features]. All caller-owned, 16-byte aligned. Errors:
+ * INVALID_ARG for null or misaligned pointers and sizes outside the above; CUDA
+ * if a tensor map or the launch fails. Asynchronous on `stream`; a pipeline wait
+ * that gives up is reported by diffattn_get_device_status as TIMEOUT.
+ */
+diffattn_status diffattn_out_proj(const diffattn_out_proj_desc* desc, const void* x, const void* w, void* y,
+                                  void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns OK, TIMEOUT, BAD_SEQLENS, BAD_POSITIONS (the first error recorded since
  * the last read), or CUDA if the synchronisation itself failed.
