@@ -17,8 +17,8 @@
 //
 // Roles (320 threads):
 //   warps 0-3  softmax of component 1 (TMEM lanes 0-127 = query rows), then
-//              the epilogue;
-//   warps 4-7  softmax of component 2;
+//              the epilogue for values 0-63 of every row;
+//   warps 4-7  softmax of component 2, then the epilogue for values 64-127;
 //   warp  8    TMA producer (Q once, K1|K2 and V per tile into a STAGES ring);
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer.
 // Tensor memory (512 columns of 128 lanes x 32 bit):
@@ -79,10 +79,8 @@ struct Misc {  // lives at OFF_MISC
     uint64_t s_full[2];
     uint64_t p_ready[2];
     uint64_t o_full;
-    uint64_t l2_ready;
     uint32_t tmem_base;
     int abort_flag;
-    float inv_l2[BM];
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
 
@@ -135,7 +133,6 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full);
-    const uint32_t bar_l2_ready = smem_u32(&ms.l2_ready);
     const uint32_t sq = sbase + OFF_Q;
     auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
     auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
@@ -156,7 +153,6 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             mbar_init(bar_p_ready(c), 128);
         }
         mbar_init(bar_o_full, 1);
-        mbar_init(bar_l2_ready, 128);
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -342,74 +338,69 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         // Training outputs: log2-sum-exp of the scaled scores per component,
         // lse_c = m_c + log2(l_c), so that P_c = 2^(S_c * scale * log2(e) - lse_c).
         if (ok && p.lse != nullptr && qi < len) p.lse[((size_t)(start + qi) * p.H + h) * 2 + c] = m + __log2f(l);
-        if (c == 1) {
-            ms.inv_l2[r] = 1.f / l;
-            mbar_arrive(bar_l2_ready);
-        } else {
-            ok = ok && warp_all(mbar_wait(bar_o_full, 0, ab)) && warp_all(mbar_wait(bar_l2_ready, 0, ab));
-            if (ok) {
-                tc_fence_after();
-                const float lam = p.lambda[h * p.lambda_stride];
-                const float il1 = 1.f / l;
-                const float il2 = ms.inv_l2[r];
-                const uint32_t t_o1 = tmem + lane_off + col_o(0);
-                const uint32_t t_o2 = tmem + lane_off + col_o(1);
-                // pass 1: mean square of D = O1/l1 - lambda O2/l2 over the dv values of the row
-                float ss0 = 0.f, ss1 = 0.f;
+        // ---- epilogue, split by columns: warpgroup c handles values [64c, 64c + 64)
+        // of every row. 1/l_c and the partial sums of squares cross between the two
+        // warpgroups through the Q1 box (2 KB of it): every MMA reading Q1 has
+        // retired once either warpgroup has left its loop (the tensor pipe
+        // completes in issue order and S_2 of the last tile follows S_1).
+        float* xch = reinterpret_cast<float*>(smem + OFF_Q);  // [0,256): 1/l_c, [256,512): sum D^2
+        xch[c * BM + r] = 1.f / l;
+        named_barrier_sync(1, 256);
+        ok = warp_all(ok && mbar_wait(bar_o_full, 0, ab));
+        const bool store = qi < len;
+        float D[64];
+        float ssp = 0.f;
+        if (ok) {
+            tc_fence_after();
+            const float lam = p.lambda[h * p.lambda_stride];
+            const float il1 = xch[r], il2 = xch[BM + r];
+            const uint32_t t_o1 = tmem + lane_off + col_o(0) + 64 * c;
+            const uint32_t t_o2 = tmem + lane_off + col_o(1) + 64 * c;
 #pragma unroll
-                for (int ch = 0; ch < DV / 32; ++ch) {
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(t_o1 + ch * 32, o1);
-                    tmem_ld32(t_o2 + ch * 32, o2);
-                    tmem_wait_ld();
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t o1[32], o2[32];
+                tmem_ld32(t_o1 + ch * 32, o1);
+                tmem_ld32(t_o2 + ch * 32, o2);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float a0 = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
-                        const float a1 = __uint_as_float(o1[i + 1]) * il1 - lam * (__uint_as_float(o2[i + 1]) * il2);
-                        ss0 = fmaf(a0, a0, ss0);
-                        ss1 = fmaf(a1, a1, ss1);
+                for (int i = 0; i < 32; ++i) {
+                    D[ch * 32 + i] = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                    ssp = fmaf(D[ch * 32 + i], D[ch * 32 + i], ssp);
+                }
+                // Training outputs: the normalised attention output of each component,
+                // kept in fp32 (the lambda gradient sums many cancelling terms of them).
+                if (store && p.o1 != nullptr) {
+                    const size_t base = ((size_t)(start + qi) * p.H + h) * DV / 4 + c * 16 + ch * 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        reinterpret_cast<float4*>(p.o1)[base + i] =
+                            make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
+                                        __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
+                        reinterpret_cast<float4*>(p.o2)[base + i] =
+                            make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
+                                        __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
                     }
                 }
-                const float rinv = 1.f / sqrtf((ss0 + ss1) / (float)DV + p.eps);
-                const float post = (1.f - p.lambda_init) * rinv;
-                const bool store = qi < len;
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                      ((size_t)(start + (store ? qi : 0)) * p.H + h) * DV);
-                // pass 2: recompute D, normalise, weight, scale, round to bf16 and store
+            }
+        }
+        xch[2 * BM + c * BM + r] = ssp;
+        named_barrier_sync(1, 256);
+        if (ok) {
+            // RMSNorm over the dv values of the row, weight, (1 - lambda_init), bf16, store
+            const float ss = xch[2 * BM + r] + xch[3 * BM + r];
+            const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DV + p.eps);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                  ((size_t)(start + (store ? qi : 0)) * p.H + h) * DV + 64 * c);
+            const float* wv = p.subln_w + 64 * c;
 #pragma unroll
-                for (int ch = 0; ch < DV / 32; ++ch) {
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(t_o1 + ch * 32, o1);
-                    tmem_ld32(t_o2 + ch * 32, o2);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+            for (int g = 0; g < 8; ++g) {
+                uint32_t pk[4];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const int e = ch * 32 + i;
-                        const float a0 = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
-                        const float a1 = __uint_as_float(o1[i + 1]) * il1 - lam * (__uint_as_float(o2[i + 1]) * il2);
-                        pk[i / 2] = pack_bf16x2(a0 * post * __ldg(p.subln_w + e), a1 * post * __ldg(p.subln_w + e + 1));
-                    }
-                    if (store) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                    }
-                    // Training outputs: the normalised attention output of each component,
-                    // kept in fp32 (the lambda gradient sums many cancelling terms of them).
-                    if (store && p.o1 != nullptr) {
-                        const size_t base = ((size_t)(start + qi) * p.H + h) * DV / 4 + ch * 8;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            reinterpret_cast<float4*>(p.o1)[base + i] =
-                                make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
-                                            __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
-                            reinterpret_cast<float4*>(p.o2)[base + i] =
-                                make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
-                                            __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
-                        }
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const int e = g * 8 + 2 * i;
+                    pk[i] = pack_bf16x2(D[e] * post * __ldg(wv + e), D[e + 1] * post * __ldg(wv + e + 1));
                 }
+                if (store) dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
     }
