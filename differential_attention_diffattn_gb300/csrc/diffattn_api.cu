@@ -231,7 +231,8 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
     FwdTensorMaps maps;
     if (!encode_bf16_rows(&maps.q, q, (uint64_t)ds.num_heads * 2 * ds.d, (uint64_t)p.total_tokens) ||
         !encode_bf16_rows(&maps.k, k, (uint64_t)ds.num_kv_heads * 2 * ds.d, (uint64_t)p.total_tokens) ||
-        !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens))
+        !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens) ||
+        !encode_bf16_rows(&maps.out, out, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
     return launch_fwd_bf16_sm103a(p, maps, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

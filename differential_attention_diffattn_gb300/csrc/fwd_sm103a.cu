@@ -81,6 +81,8 @@ struct Misc {  // lives at OFF_MISC
     uint64_t o_full;
     uint32_t tmem_base;
     int abort_flag;
+    float lam;        // lambda of this head, and the norm weight, staged at setup
+    float w[DV];
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
 
@@ -94,7 +96,8 @@ __device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffff
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                                const FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
@@ -155,6 +158,10 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         mbar_init(bar_o_full, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
+    }
+    if (warp == PRODUCER_WARP) {
+        for (int i = lane; i < DV; i += 32) ms.w[i] = p.subln_w[i];
+        if (lane == 0) ms.lam = p.lambda[h * p.lambda_stride];
     }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
     tc_fence_before();
@@ -352,7 +359,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         float ssp = 0.f;
         if (ok) {
             tc_fence_after();
-            const float lam = p.lambda[h * p.lambda_stride];
+            const float lam = ms.lam;
             const float il1 = xch[r], il2 = xch[BM + r];
             const uint32_t t_o1 = tmem + lane_off + col_o(0) + 64 * c;
             const uint32_t t_o2 = tmem + lane_off + col_o(1) + 64 * c;
@@ -385,22 +392,44 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         }
         xch[2 * BM + c * BM + r] = ssp;
         named_barrier_sync(1, 256);
+        // A tile wholly inside its sequence leaves through a bulk tensor store of the
+        // 128 x 128 bf16 block, staged in the first K box (free: every load of this CTA
+        // has been consumed); a tile past the sequence end (whose rows beyond it may
+        // belong to the next packed sequence) is stored row by row.
+        const bool full_tile = qt * BM + BM <= len;
         if (ok) {
-            // RMSNorm over the dv values of the row, weight, (1 - lambda_init), bf16, store
+            // RMSNorm over the dv values of the row, weight, (1 - lambda_init), bf16
             const float ss = xch[2 * BM + r] + xch[3 * BM + r];
             const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DV + p.eps);
+            const float* wv = ms.w + 64 * c;
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
                                                   ((size_t)(start + (store ? qi : 0)) * p.H + h) * DV + 64 * c);
-            const float* wv = p.subln_w + 64 * c;
+            // box c of the staging area: row r at r * 128 bytes, 16-byte chunk g at (g ^ (r % 8))
+            uint8_t* stage_row = smem + OFF_STAGE0 + (uint32_t)c * BOX_BYTES + (uint32_t)r * 128u;
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = g * 8 + 2 * i;
-                    pk[i] = pack_bf16x2(D[e] * post * __ldg(wv + e), D[e + 1] * post * __ldg(wv + e + 1));
+                    pk[i] = pack_bf16x2(D[e] * post * wv[e], D[e + 1] * post * wv[e + 1]);
                 }
-                if (store) dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if (full_tile)
+                    *reinterpret_cast<uint4*>(stage_row + ((g ^ (r & 7)) << 4)) = v4;
+                else if (store)
+                    dst[g] = v4;
+            }
+        }
+        if (full_tile) {
+            fence_proxy_async_smem();  // the staged rows, visible to the bulk copy
+            named_barrier_sync(1, 256);
+            if (warp == 0 && lane == 0 && ok) {
+                const uint32_t src = sbase + OFF_STAGE0;
+                tma_store_2d(&tm_out, src, h * DV, start + qt * BM);
+                tma_store_2d(&tm_out, src + BOX_BYTES, h * DV + 64, start + qt * BM);
+                bulk_commit_group();
+                bulk_wait_group_read0();  // shared memory stays until the copy has read it
             }
         }
     }
@@ -429,7 +458,7 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
     }
     const int n_qt = (p.max_seqlen + BM - 1) / BM;
     dim3 grid((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
-    diffattn_fwd_bf16_sm103a_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, p);
+    diffattn_fwd_bf16_sm103a_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.out, p);
     return cudaGetLastError();
 }
 

@@ -45,7 +45,7 @@ struct FwdParams {
 
 // TMA descriptors of the bf16 operands, built on the host per call.
 struct FwdTensorMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, out;  // out: [tokens][H * dv] bf16, 64 x 128 boxes (bulk tensor stores)
 };
 
 // One forward against a key/value cache (decode / short query blocks).
