@@ -7,6 +7,7 @@
 // serves both, and per (query row i, key j):
 //   P_c  = 2^(s log2(e) <Q_c[i], K_c[j]> - lse_c[i])                (saved by the forward)
 //   dS_1 = P_1 (dP - delta_1[i]),  dS_2 = -lambda P_2 (dP - delta_2[i])
+//   (the kernels carry dS / s and apply s once to dQ and dK in their epilogues)
 //   delta_c[i] = <dD[i], O_c[i] / l_c[i]>                        (preprocessing)
 //   dQ_c += s dS_c K_c,  dK_c += s dS_c^T Q_c,  dV += (P_1 - lambda P_2)^T dD
 // (the derivative of softmax(...) V through "DiffTransformer.py",
@@ -36,9 +37,9 @@ namespace {
 constexpr int HD = 64;
 constexpr int DV = 128;
 constexpr uint32_t ROW = 128;                      // bytes of one swizzled row (64 bf16)
-constexpr int NT = 192;                            // 4 compute warps + producer + MMA
-constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int NT = 320;                            // 8 compute warps (two warpgroups) + producer + MMA
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t a) { return smem_desc_sw128(a, 16, 1024); }
 // MN-major operand whose N extent is split in 64-wide boxes `box` bytes apart.
@@ -86,8 +87,8 @@ __device__ __forceinline__ void dq_keys32(const uint32_t (&s1)[32], const uint32
             const float pp = __uint_as_float(dp[i + u]);
             const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -rs.x));
             const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -rs.y));
-            a[u] = p1 * (pp - rs.z) * sc;
-            b[u] = -lam * p2 * (pp - rs.w) * sc;
+            a[u] = p1 * (pp - rs.z);            // dS_1 / s
+            b[u] = (lam * p2) * (rs.w - pp);    // dS_2 / s
             if (MASK) {
                 const bool vis = i + u < nvis;
                 a[u] = vis ? a[u] : 0.f;
@@ -110,7 +111,7 @@ constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready, ds_ready, dq_done;
+    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready, ds_ready[2], dq_done;
     uint32_t tmem;
     int abort_flag;
 };
@@ -134,8 +135,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const int n_kv = p.causal ? qt + 1 : (len + BN - 1) / BN;
     const int g = h / (p.H / p.Hkv);
 
-    const uint32_t b_q = smem_u32(&ms.q_full), b_s = smem_u32(&ms.s_ready), b_ds = smem_u32(&ms.ds_ready),
-                   b_dq = smem_u32(&ms.dq_done);
+    const uint32_t b_q = smem_u32(&ms.q_full), b_s = smem_u32(&ms.s_ready), b_dq = smem_u32(&ms.dq_done);
+    auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
     auto b_kf = [&](int s) { return smem_u32(&ms.kv_full[s]); };
     auto b_ke = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
     if (warp == PRODUCER_WARP && lane == 0) {
@@ -145,7 +146,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             mbar_init(b_ke(s), 1);
         }
         mbar_init(b_s, 1);
-        mbar_init(b_ds, 128);
+        mbar_init(b_ds(0), 128);
+        mbar_init(b_ds(1), 128);
         mbar_init(b_dq, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
@@ -207,25 +209,31 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 mma_ss_elect(tmem + 256, dq_dd + (kk >> 2) * BX + (kk & 3) * KS,
                              st_k + 2 * BX + (kk >> 2) * BX + (kk & 3) * KS, id_s, kk > 0);
             mma_commit_elect(b_s);
-            if (!(ok = warp_all(mbar_wait(b_ds, (uint32_t)j & 1u, ab)))) break;
-            tc_fence_after();
-            // dQ_c += dS_c K_c: A = dS_c (bf16 in TMEM, K = keys), B = K_c rows (MN-major)
+            // dQ_c += dS_c K_c: A = dS_c (bf16 in TMEM, K = keys), B = K_c rows (MN-major);
+            // keys 0-63 as soon as the first warpgroup has written them, then keys 64-127
             const uint64_t st_km = dkm + (uint64_t)s * SG;
-            for (int c = 0; c < 2; ++c) {
+            for (int w = 0; w < 2; ++w) {
+                if (!(ok = warp_all(mbar_wait(b_ds(w), (uint32_t)j & 1u, ab)))) break;
+                tc_fence_after();
+                for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts_elect(tmem + 384 + c * 64, tmem + c * 128 + kk * 8, st_km + c * BX + kk * KR, id_dq,
-                                 (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 4 * w; kk < 4 * w + 4; ++kk)  // dS of keys 16 kk.. at column 64 w + 8 (kk % 4)
+                        mma_ts_elect(tmem + 384 + c * 64, tmem + c * 128 + 64 * w + 8 * (kk & 3), st_km + c * BX + kk * KR,
+                                     id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+                }
             }
+            if (!ok) break;
             mma_commit_elect(b_ke(s));
         }
         mma_commit_elect(b_dq);
         mbar_wait_drain(b_dq, 0, p.timeout_ns);
         __syncwarp();
     } else {
-        // ================================================ compute warpgroup ===
-        const int r = warp * 32 + lane;  // query row in the tile = TMEM lane
-        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        // ============================================== compute warpgroups ===
+        // Warpgroup w handles keys [64 w, 64 w + 64) of every tile; thread = query row.
+        const int w = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;  // query row in the tile = TMEM lane
+        const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
         const int qi = qt * BM + r;
         const bool row_ok = qi < len;
         const size_t grow = (size_t)(start + (row_ok ? qi : 0));
@@ -242,7 +250,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             // masking only on tiles where some row of the warp has keys past its limit
             const bool need_mask = __any_sync(0xffffffffu, kb + BN > lim);
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 2 * w; ch < 2 * w + 2; ++ch) {
                 uint32_t s1[32], s2[32], dp[32];
                 tmem_ld32(tmem + lo + ch * 32, s1);
                 tmem_ld32(tmem + lo + 128 + ch * 32, s2);
@@ -253,13 +261,15 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     dq_keys32<true>(s1, s2, dp, rs, lam, sl2, sc, lim - (kb + ch * 32), d1, d2);
                 else
                     dq_keys32<false>(s1, s2, dp, rs, lam, sl2, sc, 0, d1, d2);
-                // dS_c of keys [32 ch, 32 ch + 32) -> columns [16 ch, 16 ch + 16) of S_c (already read)
-                tmem_st16(tmem + lo + ch * 16, d1);
-                tmem_st16(tmem + lo + 128 + ch * 16, d2);
+                // dS_c of keys [32 ch, 32 ch + 32) -> columns [64 w + 16 (ch - 2 w), + 16) of S_c:
+                // already read, and inside this warpgroup's own columns [64 w, 64 w + 64)
+                const uint32_t dcol = 64 * w + 16 * (ch - 2 * w);
+                tmem_st16(tmem + lo + dcol, d1);
+                tmem_st16(tmem + lo + 128 + dcol, d2);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_ds);
+            mbar_arrive(b_ds(w));
         }
         ok = ok && warp_all(mbar_wait(b_dq, 0, ab));
         // ok is warp-uniform; row_ok is not: every lane takes part in the (warp-wide)
@@ -268,13 +278,14 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tc_fence_after();
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (grow * p.H + h) * (2 * HD));
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {  // dQ1 = columns 0..63, dQ2 = 64..127 of the output row
+            for (int ch = 2 * w; ch < 2 * w + 2; ++ch) {  // dQ1 = columns 0..63 (w = 0), dQ2 = 64..127 (w = 1)
                 uint32_t o[32];
                 tmem_ld32(tmem + lo + 384 + ch * 32, o);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[16];  // the softmax scale s, left out of dS, applied here
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * sc, __uint_as_float(o[2 * i + 1]) * sc);
                 if (row_ok) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -305,24 +316,24 @@ constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready, ds_ready, acc_done;
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready, ds_ready[2], acc_done;
     uint32_t tmem;
     int abort_flag;
 };
 }  // namespace dkv
 
-// One thread (= one key) and 32 query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
+// One thread (= one key) and N query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
 // pairs from S_1^T, S_2^T, dP^T and the rows' (lse_1, lse_2, delta_1, delta_2).
 // MASK zeroes rows outside [q_min, q_end); without it every row is visible.
 // The exponentials run on every element and masking is a select after the
 // products, so stale statistics of rows past the end never reach the results.
-template <bool MASK>
-__device__ __forceinline__ void dkv_rows32(const uint32_t (&s1)[32], const uint32_t (&s2)[32],
-                                           const uint32_t (&dp)[32], const float4* stat, float lam, float sl2,
-                                           float sc, int q0, int q_end, int q_min, uint32_t (&pc)[16],
-                                           uint32_t (&d1)[16], uint32_t (&d2)[16]) {
+template <bool MASK, int N>
+__device__ __forceinline__ void dkv_rows(const uint32_t (&s1)[N], const uint32_t (&s2)[N], const uint32_t (&dp)[N],
+                                         const float4* stat, float lam, float sl2, float sc, int q0, int q_end,
+                                         int q_min, uint32_t (&pc)[N / 2], uint32_t (&d1)[N / 2],
+                                         uint32_t (&d2)[N / 2]) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < N; i += 2) {
         float a[2], b1[2], b2[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -330,9 +341,10 @@ __device__ __forceinline__ void dkv_rows32(const uint32_t (&s1)[32], const uint3
             const float pp = __uint_as_float(dp[i + u]);
             const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x));
             const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y));
-            a[u] = p1 - lam * p2;
-            b1[u] = p1 * (pp - st.z) * sc;
-            b2[u] = -lam * p2 * (pp - st.w) * sc;
+            const float q2 = lam * p2;
+            a[u] = p1 - q2;
+            b1[u] = p1 * (pp - st.z);  // dS_1 / s
+            b2[u] = q2 * (st.w - pp);  // dS_2 / s
             if (MASK) {
                 const int qi = q0 + i + u;
                 const bool vis = (qi < q_end) & (qi >= q_min);
@@ -367,8 +379,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const int nqb = (len + BQ - 1) / BQ - qb0;             // query blocks per head
     const int n_items = G * nqb;                            // (head, query block) items
 
-    const uint32_t b_kv = smem_u32(&ms.kv_full), b_s = smem_u32(&ms.s_ready), b_ds = smem_u32(&ms.ds_ready),
-                   b_acc = smem_u32(&ms.acc_done);
+    const uint32_t b_kv = smem_u32(&ms.kv_full), b_s = smem_u32(&ms.s_ready), b_acc = smem_u32(&ms.acc_done);
+    auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
     auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
     auto b_se = [&](int s) { return smem_u32(&ms.st_empty[s]); };
     auto item_head = [&](int it) { return g * G + it / nqb; };
@@ -380,7 +392,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             mbar_init(b_se(s), 1);
         }
         mbar_init(b_s, 1);
-        mbar_init(b_ds, 128);
+        mbar_init(b_ds(0), 128);
+        mbar_init(b_ds(1), 128);
         mbar_init(b_acc, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
@@ -447,29 +460,37 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 mma_ss_elect(tmem + 128, d_v + (kk >> 2) * KB + (kk & 3) * KS, sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS,
                              id_s, kk > 0);
             mma_commit_elect(b_s);
-            if (!(ok = warp_all(mbar_wait(b_ds, (uint32_t)it & 1u, ab)))) break;
-            tc_fence_after();
             const uint64_t sqm = d_qm + (uint64_t)s * SG;
-            // dV += (P1 - lambda P2)^T-rows dD: A = TMEM [0,32), K = 64 query rows
+            // Warpgroup w wrote the bf16 operands of query rows [32 w, 32 w + 32) into its own
+            // columns: 16-row step kk reads columns 32 (kk / 2) + 8 (kk % 2) of each region.
+            for (int w = 0; w < 2; ++w) {
+                if (!(ok = warp_all(mbar_wait(b_ds(w), (uint32_t)it & 1u, ab)))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_ts_elect(tmem + 192, tmem + kk * 8, sqm + 2 * QB + kk * KR, id_v, (it > 0 || kk > 0) ? 1u : 0u);
-            // dK_c += dS_c^T-rows Q_c: A = TMEM [64,96) / [128,160)
-            for (int c = 0; c < 2; ++c) {
+                for (int kk = 2 * w; kk < 2 * w + 2; ++kk) {
+                    const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
+                    // dV += (P1 - lambda P2)^T-rows dD
+                    mma_ts_elect(tmem + 192, tmem + acol, sqm + 2 * QB + kk * KR, id_v, (it > 0 || kk > 0) ? 1u : 0u);
+                    // dK_c += dS_c^T-rows Q_c
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tmem + 320 + c * 64, tmem + 64 + c * 64 + kk * 8, sqm + c * QB + kk * KR, id_k,
-                                 (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int c = 0; c < 2; ++c)
+                        mma_ts_elect(tmem + 320 + c * 64, tmem + 64 + c * 64 + acol, sqm + c * QB + kk * KR, id_k,
+                                     (it > 0 || kk > 0) ? 1u : 0u);
+                }
             }
+            if (!ok) break;
             mma_commit_elect(b_se(s));
         }
         mma_commit_elect(b_acc);
         mbar_wait_drain(b_acc, 0, p.timeout_ns);
         __syncwarp();
     } else {
-        // ================================================ compute warpgroup ===
-        const int k = warp * 32 + lane;  // key in the tile = TMEM lane
-        const uint32_t lo = (uint32_t)(warp * 32) << 16;
+        // ============================================== compute warpgroups ===
+        // Warpgroup w handles query rows [32 w, 32 w + 32) of every block, 16 at a time;
+        // thread = key.
+        const int w = warp >> 2;
+        const int k = (warp & 3) * 32 + lane;  // key in the tile = TMEM lane
+        const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
         const int kj = kt * BK + k;      // key position in the sequence
         const bool key_ok = kj < len;
         const int q_end = key_ok ? len : 0;       // visible query rows of this key: [q_min, q_end)
@@ -488,25 +509,28 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             // precedes a key of the tile: the first two blocks and the last one
             const bool need_mask = row0 + BQ > len || kt * BK + BK > len || (p.causal && row0 < kt * BK + BK - 1);
 #pragma unroll 1
-            for (int ch = 0; ch < 2; ++ch) {  // query rows [32 ch, 32 ch + 32) of the block
-                uint32_t s1[32], s2[32], dp[32];
-                tmem_ld32(tmem + lo + ch * 32, s1);
-                tmem_ld32(tmem + lo + 64 + ch * 32, s2);
-                tmem_ld32(tmem + lo + 128 + ch * 32, dp);
+            for (int sub = 0; sub < 2; ++sub) {  // query rows [q0, q0 + 16) of the block
+                const int q0 = 32 * w + 16 * sub;
+                uint32_t s1[16], s2[16], dp[16];
+                tmem_ld16(tmem + lo + q0, s1);
+                tmem_ld16(tmem + lo + 64 + q0, s2);
+                tmem_ld16(tmem + lo + 128 + q0, dp);
                 tmem_wait_ld();
-                uint32_t pc[16], d1[16], d2[16];
+                uint32_t pc[8], d1[8], d2[8];
                 if (need_mask)
-                    dkv_rows32<true>(s1, s2, dp, stat + ch * 32, lam, sl2, sc, row0 + ch * 32, q_end, q_min, pc, d1, d2);
+                    dkv_rows<true, 16>(s1, s2, dp, stat + q0, lam, sl2, sc, row0 + q0, q_end, q_min, pc, d1, d2);
                 else
-                    dkv_rows32<false>(s1, s2, dp, stat + ch * 32, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
-                // rows [32 ch, +32) -> columns [16 ch, +16) of the S1^T / S2^T / dP^T regions (already read)
-                tmem_st16(tmem + lo + ch * 16, pc);
-                tmem_st16(tmem + lo + 64 + ch * 16, d1);
-                tmem_st16(tmem + lo + 128 + ch * 16, d2);
+                    dkv_rows<false, 16>(s1, s2, dp, stat + q0, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
+                // rows [q0, q0 + 16) -> columns [32 w + 8 sub, + 8) of each region (already read,
+                // and inside this warpgroup's own columns)
+                const uint32_t pcol = 32 * w + 8 * sub;
+                tmem_st8(tmem + lo + pcol, pc);
+                tmem_st8(tmem + lo + 64 + pcol, d1);
+                tmem_st8(tmem + lo + 128 + pcol, d2);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b_ds);
+            mbar_arrive(b_ds(w));
         }
         ok = ok && warp_all(mbar_wait(b_acc, 0, ab));
         // ok is warp-uniform; key_ok is not: every lane takes part in the (warp-wide)
@@ -516,27 +540,22 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             const size_t grow = (size_t)(start + (key_ok ? kj : 0));
             uint4* dvp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + (grow * p.Hkv + g) * DV);
             uint4* dkp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + (grow * p.Hkv + g) * (2 * HD));
+            // warpgroup 0 stores dV (columns 192..319), warpgroup 1 dK1 | dK2 (320..447)
+            uint4* dst = w == 0 ? dvp : dkp;
+            const float f = w == 0 ? 1.f : sc;  // dK: the softmax scale s, left out of dS, applied here
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lo + 192 + ch * 32, o);   // dV columns [32 ch, +32)
+                tmem_ld32(tmem + lo + 192 + 128 * w + ch * 32, o);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
                 if (key_ok) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dvp[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-                tmem_ld32(tmem + lo + 320 + ch * 32, o);   // dK1 | dK2 columns [32 ch, +32)
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-                if (key_ok) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dkp[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        dst[ch * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                 }
             }
         }
