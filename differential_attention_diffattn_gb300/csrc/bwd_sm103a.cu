@@ -322,6 +322,14 @@ struct Misc {
 };
 }  // namespace dkv
 
+// 16-byte load from a shared-window address (the statistics the bulk copy wrote;
+// ordered after the barrier wait that published them).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // One thread (= one key) and N query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
 // pairs from S_1^T, S_2^T, dP^T and the rows' (lse_1, lse_2, delta_1, delta_2).
 // MASK zeroes rows outside [q_min, q_end); without it every row is visible.
@@ -329,7 +337,7 @@ struct Misc {
 // products, so stale statistics of rows past the end never reach the results.
 template <bool MASK, int N>
 __device__ __forceinline__ void dkv_rows(const uint32_t (&s1)[N], const uint32_t (&s2)[N], const uint32_t (&dp)[N],
-                                         const float4* stat, float lam, float sl2, float sc, int q0, int q_end,
+                                         uint32_t stat, float lam, float sl2, float sc, int q0, int q_end,
                                          int q_min, uint32_t (&pc)[N / 2], uint32_t (&d1)[N / 2],
                                          uint32_t (&d2)[N / 2]) {
 #pragma unroll
@@ -337,7 +345,7 @@ __device__ __forceinline__ void dkv_rows(const uint32_t (&s1)[N], const uint32_t
         float a[2], b1[2], b2[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const float4 st = stat[i + u];
+            const float4 st = lds_f4(stat + 16u * (uint32_t)(i + u));
             const float pp = __uint_as_float(dp[i + u]);
             const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x));
             const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y));
@@ -501,7 +509,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)it & 1u, ab)))) break;
             tc_fence_after();
             const int s = it % STAGES;
-            const float4* stat = reinterpret_cast<const float4*>(smem + OFF_ST + (uint32_t)s * STAGE + ST_STAT);
+            // row statistics of the block (shared-window address: explicit shared loads)
+            const uint32_t stat = sb + OFF_ST + (uint32_t)s * STAGE + ST_STAT;
             const int hh = item_head(it);
             const float lam = p.lambda[hh * p.lambda_stride];
             const int row0 = item_row0(it);
@@ -518,9 +527,9 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 tmem_wait_ld();
                 uint32_t pc[8], d1[8], d2[8];
                 if (need_mask)
-                    dkv_rows<true, 16>(s1, s2, dp, stat + q0, lam, sl2, sc, row0 + q0, q_end, q_min, pc, d1, d2);
+                    dkv_rows<true, 16>(s1, s2, dp, stat + 16u * q0, lam, sl2, sc, row0 + q0, q_end, q_min, pc, d1, d2);
                 else
-                    dkv_rows<false, 16>(s1, s2, dp, stat + q0, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
+                    dkv_rows<false, 16>(s1, s2, dp, stat + 16u * q0, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
                 // rows [q0, q0 + 16) -> columns [32 w + 8 sub, + 8) of each region (already read,
                 // and inside this warpgroup's own columns)
                 const uint32_t pcol = 32 * w + 8 * sub;
