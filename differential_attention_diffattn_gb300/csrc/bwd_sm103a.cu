@@ -111,7 +111,7 @@ constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready, ds_ready[2], dq_done;
+    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready[2], ds_ready[2], dq_done;
     uint32_t tmem;
     int abort_flag;
 };
@@ -135,7 +135,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const int n_kv = p.causal ? qt + 1 : (len + BN - 1) / BN;
     const int g = h / (p.H / p.Hkv);
 
-    const uint32_t b_q = smem_u32(&ms.q_full), b_s = smem_u32(&ms.s_ready), b_dq = smem_u32(&ms.dq_done);
+    const uint32_t b_q = smem_u32(&ms.q_full), b_dq = smem_u32(&ms.dq_done);
+    auto b_s = [&](int w) { return smem_u32(&ms.s_ready[w]); };
     auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
     auto b_kf = [&](int s) { return smem_u32(&ms.kv_full[s]); };
     auto b_ke = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
@@ -145,7 +146,8 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             mbar_init(b_kf(s), 1);
             mbar_init(b_ke(s), 1);
         }
-        mbar_init(b_s, 1);
+        mbar_init(b_s(0), 1);
+        mbar_init(b_s(1), 1);
         mbar_init(b_ds(0), 128);
         mbar_init(b_ds(1), 128);
         mbar_init(b_dq, 1);
@@ -187,43 +189,60 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
-        constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false);   // S_c, dP: both operands K-major
+        // Two 64-key halves per tile, pipelined: as soon as warpgroup h has written
+        // dS of half h, its dQ steps go out and then the scores of half h of the next
+        // tile, which overwrite only half h's columns (the pipe runs in issue order,
+        // so the dQ steps have read dS before the new scores land).
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false);    // S_c, dP of a half: both operands K-major
         constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true);    // dQ_c: B = K_c is MN-major (d contiguous)
         const uint64_t dq_q = desc_k(sb + OFF_Q), dq_dd = desc_k(sb + OFF_DD);
         const uint64_t dk0 = desc_k(sb + OFF_ST), dkm = desc_mn(sb + OFF_ST, BOX);
         constexpr uint64_t KS = 32 >> 4, BX = BOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
-        bool ok = warp_all(mbar_wait(b_q, 0, ab));
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const int s = j % STAGES;
-            if (!(ok = warp_all(mbar_wait(b_kf(s), (uint32_t)(j / STAGES) & 1u, ab)))) break;
-            tc_fence_after();
-            const uint64_t st_k = dk0 + (uint64_t)s * SG;
-            for (int c = 0; c < 2; ++c) {  // S_c = Q_c K_c^T, K = d = 64
+        constexpr uint64_t HK = (64 * ROW) >> 4;  // 64 key rows of a K-major box
+        // S_c = Q_c K_c^T and dP = dD V^T for keys [64 h, 64 h + 64) of the tile in stage s
+        auto issue_sdp = [&](int s, int h) {
+            const uint64_t st_k = dk0 + (uint64_t)s * SG + (uint64_t)h * HK;
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ss_elect(tmem + c * 128, dq_q + c * BX + kk * KS, st_k + c * BX + kk * KS, id_s, kk > 0);
+                    mma_ss_elect(tmem + c * 128 + 64 * h, dq_q + c * BX + kk * KS, st_k + c * BX + kk * KS, id_s,
+                                 kk > 0);
             }
-            // dP = dD V^T, K = dv = 128: the two 64-column halves of dD and of V
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ss_elect(tmem + 256, dq_dd + (kk >> 2) * BX + (kk & 3) * KS,
+            for (int kk = 0; kk < 8; ++kk)  // K = dv = 128 over the two 64-column halves of dD and of V
+                mma_ss_elect(tmem + 256 + 64 * h, dq_dd + (kk >> 2) * BX + (kk & 3) * KS,
                              st_k + 2 * BX + (kk >> 2) * BX + (kk & 3) * KS, id_s, kk > 0);
-            mma_commit_elect(b_s);
-            // dQ_c += dS_c K_c: A = dS_c (bf16 in TMEM, K = keys), B = K_c rows (MN-major);
-            // keys 0-63 as soon as the first warpgroup has written them, then keys 64-127
+            mma_commit_elect(b_s(h));
+        };
+        bool ok = warp_all(mbar_wait(b_q, 0, ab)) && warp_all(mbar_wait(b_kf(0), 0, ab));
+        if (ok) {
+            tc_fence_after();
+            issue_sdp(0, 0);
+            issue_sdp(0, 1);
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int s = j % STAGES, s1 = (j + 1) % STAGES;
+            const bool has_next = j + 1 < n_kv;
             const uint64_t st_km = dkm + (uint64_t)s * SG;
-            for (int w = 0; w < 2; ++w) {
-                if (!(ok = warp_all(mbar_wait(b_ds(w), (uint32_t)j & 1u, ab)))) break;
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = warp_all(mbar_wait(b_ds(h), (uint32_t)j & 1u, ab)))) break;
                 tc_fence_after();
+                // dQ_c += dS_c K_c over keys [64 h, 64 h + 64): A = dS_c (bf16 in TMEM, at column
+                // 64 h + 8 (kk % 4) for keys 16 kk..), B = K_c rows (MN-major)
                 for (int c = 0; c < 2; ++c) {
 #pragma unroll
-                    for (int kk = 4 * w; kk < 4 * w + 4; ++kk)  // dS of keys 16 kk.. at column 64 w + 8 (kk % 4)
-                        mma_ts_elect(tmem + 384 + c * 64, tmem + c * 128 + 64 * w + 8 * (kk & 3), st_km + c * BX + kk * KR,
+                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                        mma_ts_elect(tmem + 384 + c * 64, tmem + c * 128 + 64 * h + 8 * (kk & 3), st_km + c * BX + kk * KR,
                                      id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (has_next) {
+                    if (h == 0 && !(ok = warp_all(mbar_wait(b_kf(s1), (uint32_t)((j + 1) / STAGES) & 1u, ab)))) break;
+                    tc_fence_after();
+                    issue_sdp(s1, h);
                 }
             }
             if (!ok) break;
-            mma_commit_elect(b_ke(s));
+            mma_commit_elect(b_ke(s));  // every MMA reading stage s has been issued
         }
         mma_commit_elect(b_dq);
         mbar_wait_drain(b_dq, 0, p.timeout_ns);
@@ -244,7 +263,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         const int lim = row_ok ? (p.causal ? min(qi + 1, len) : len) : 0;  // keys < lim are visible
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)j & 1u, ab)))) break;
+            if (!(ok = warp_all(mbar_wait(b_s(w), (uint32_t)j & 1u, ab)))) break;
             tc_fence_after();
             const int kb = j * BN;
             // masking only on tiles where some row of the warp has keys past its limit
