@@ -335,7 +335,7 @@ constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready, ds_ready[2], acc_done;
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready[2], ds_ready[2], acc_done;
     uint32_t tmem;
     int abort_flag;
 };
@@ -406,7 +406,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const int nqb = (len + BQ - 1) / BQ - qb0;             // query blocks per head
     const int n_items = G * nqb;                            // (head, query block) items
 
-    const uint32_t b_kv = smem_u32(&ms.kv_full), b_s = smem_u32(&ms.s_ready), b_acc = smem_u32(&ms.acc_done);
+    const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done);
+    auto b_s = [&](int w) { return smem_u32(&ms.s_ready[w]); };
     auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
     auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
     auto b_se = [&](int s) { return smem_u32(&ms.st_empty[s]); };
@@ -418,7 +419,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             mbar_init(b_sf(s), 1);
             mbar_init(b_se(s), 1);
         }
-        mbar_init(b_s, 1);
+        mbar_init(b_s(0), 1);
+        mbar_init(b_s(1), 1);
         mbar_init(b_ds(0), 128);
         mbar_init(b_ds(1), 128);
         mbar_init(b_acc, 1);
@@ -464,29 +466,40 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
-        constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false);    // S_c^T, dP^T: N = 64 query rows
+        // Two 32-row halves per query block, pipelined: once warpgroup h has written the
+        // operands of half h, its dV / dK steps go out and then the scores of half h of
+        // the next block, which overwrite only half h's columns (the pipe runs in issue
+        // order, so the dV / dK steps have read them first).
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 32, false);    // S_c^T, dP^T of a half: N = 32 rows
         constexpr uint32_t id_v = idesc_bf16_f32(128, 128, true);    // dV: B = dD rows, MN-major (dv)
         constexpr uint32_t id_k = idesc_bf16_f32(128, 64, true);     // dK_c: B = Q_c rows, MN-major (d)
         constexpr uint64_t KS = 32 >> 4, KB = KBOX >> 4, QB = QBOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
+        constexpr uint64_t HQ = (32 * ROW) >> 4;  // 32 query rows of a K-major box
         const uint64_t d_k = desc_k(sb + OFF_K), d_v = desc_k(sb + OFF_V);
         const uint64_t d_q = desc_k(sb + OFF_ST), d_qm = desc_mn(sb + OFF_ST, QBOX);
-        bool ok = warp_all(mbar_wait(b_kv, 0, ab));
-        for (int it = 0; ok && it < n_items; ++it) {
-            const int s = it % STAGES;
-            if (!(ok = warp_all(mbar_wait(b_sf(s), (uint32_t)(it / STAGES) & 1u, ab)))) break;
-            tc_fence_after();
-            const uint64_t sq = d_q + (uint64_t)s * SG;
-            for (int c = 0; c < 2; ++c) {  // S_c^T = K_c Q_c^T, K = d
+        // S_c^T = K_c Q_c^T and dP^T = V dD^T for query rows [32 h, 32 h + 32) of the block in stage s
+        auto issue_sdp = [&](int s, int h) {
+            const uint64_t sq = d_q + (uint64_t)s * SG + (uint64_t)h * HQ;
+            for (int c = 0; c < 2; ++c) {  // K = d
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ss_elect(tmem + c * 64, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
+                    mma_ss_elect(tmem + c * 64 + 32 * h, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
             }
-            // dP^T = V dD^T, K = dv = 128 over the two 64-column halves
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_ss_elect(tmem + 128, d_v + (kk >> 2) * KB + (kk & 3) * KS, sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS,
-                             id_s, kk > 0);
-            mma_commit_elect(b_s);
+            for (int kk = 0; kk < 8; ++kk)  // K = dv = 128 over the two 64-column halves
+                mma_ss_elect(tmem + 128 + 32 * h, d_v + (kk >> 2) * KB + (kk & 3) * KS,
+                             sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS, id_s, kk > 0);
+            mma_commit_elect(b_s(h));
+        };
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && (n_items == 0 || warp_all(mbar_wait(b_sf(0), 0, ab)));
+        if (ok && n_items > 0) {
+            tc_fence_after();
+            issue_sdp(0, 0);
+            issue_sdp(0, 1);
+        }
+        for (int it = 0; ok && it < n_items; ++it) {
+            const int s = it % STAGES, s1 = (it + 1) % STAGES;
+            const bool has_next = it + 1 < n_items;
             const uint64_t sqm = d_qm + (uint64_t)s * SG;
             // Warpgroup w wrote the bf16 operands of query rows [32 w, 32 w + 32) into its own
             // columns: 16-row step kk reads columns 32 (kk / 2) + 8 (kk % 2) of each region.
@@ -504,9 +517,14 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                         mma_ts_elect(tmem + 320 + c * 64, tmem + 64 + c * 64 + acol, sqm + c * QB + kk * KR, id_k,
                                      (it > 0 || kk > 0) ? 1u : 0u);
                 }
+                if (has_next) {
+                    if (w == 0 && !(ok = warp_all(mbar_wait(b_sf(s1), (uint32_t)((it + 1) / STAGES) & 1u, ab)))) break;
+                    tc_fence_after();
+                    issue_sdp(s1, w);
+                }
             }
             if (!ok) break;
-            mma_commit_elect(b_se(s));
+            mma_commit_elect(b_se(s));  // every MMA reading stage s has been issued
         }
         mma_commit_elect(b_acc);
         mbar_wait_drain(b_acc, 0, p.timeout_ns);
@@ -525,7 +543,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const float sl2 = p.scale_log2, sc = p.scale;
         bool ok = true;
         for (int it = 0; it < n_items; ++it) {
-            if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)it & 1u, ab)))) break;
+            if (!(ok = warp_all(mbar_wait(b_s(w), (uint32_t)it & 1u, ab)))) break;
             tc_fence_after();
             const int s = it % STAGES;
             // row statistics of the block (shared-window address: explicit shared loads)
