@@ -22,7 +22,8 @@
 //   dKV kernel: CTA = 128 keys of one kv head; walks the heads of its group and
 //               the 64-row query blocks that see its keys. With keys as the MMA
 //               rows: S_c^T [0,64) [64,128), dP^T [128,192), dV [192,320),
-//               dK1 [320,384), dK2 [384,448); the bf16 operands P_1 - lambda P_2,
+//               dK1 [320,384), dK2 [384,448), K1 | K2 (bf16 pairs, the A operand
+//               of the score MMAs) [448,512); the bf16 operands P_1 - lambda P_2,
 //               dS_1^T, dS_2^T go over S1^T, S2^T, dP^T.
 // Every wait is bounded; on a timeout a CTA records the error, lets its copies
 // and MMAs land, frees TMEM and returns.
@@ -324,6 +325,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // ============================================================== dKV ===
 namespace dkv {
 constexpr int BK = 128, BQ = 64, STAGES = 3;
+constexpr uint32_t KT_COL = 448;                   // K1 | K2 as bf16 pairs: TMEM columns [448, 512)
 constexpr uint32_t KBOX = 128 * ROW;               // [128 keys x 64] 16 KB
 constexpr uint32_t QBOX = 64 * ROW;                // [64 rows x 64] 8 KB
 constexpr uint32_t OFF_K = 0;                      // K1 | K2
@@ -335,7 +337,7 @@ constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready[2], ds_ready[2], acc_done;
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready[2], ds_ready[2], acc_done, kt_ready;
     uint32_t tmem;
     int abort_flag;
 };
@@ -406,7 +408,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const int nqb = (len + BQ - 1) / BQ - qb0;             // query blocks per head
     const int n_items = G * nqb;                            // (head, query block) items
 
-    const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done);
+    const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done), b_kt = smem_u32(&ms.kt_ready);
     auto b_s = [&](int w) { return smem_u32(&ms.s_ready[w]); };
     auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
     auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
@@ -415,6 +417,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     auto item_row0 = [&](int it) { return (qb0 + it % nqb) * BQ; };  // first query position of the block
     if (warp == PRODUCER_WARP && lane == 0) {
         mbar_init(b_kv, 1);
+        mbar_init(b_kt, 256);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(b_sf(s), 1);
             mbar_init(b_se(s), 1);
@@ -477,13 +480,18 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         constexpr uint64_t HQ = (32 * ROW) >> 4;  // 32 query rows of a K-major box
         const uint64_t d_k = desc_k(sb + OFF_K), d_v = desc_k(sb + OFF_V);
         const uint64_t d_q = desc_k(sb + OFF_ST), d_qm = desc_mn(sb + OFF_ST, QBOX);
-        // S_c^T = K_c Q_c^T and dP^T = V dD^T for query rows [32 h, 32 h + 32) of the block in stage s
+        // S_c^T = K_c Q_c^T and dP^T = V dD^T for query rows [32 h, 32 h + 32) of the block in
+        // stage s. K_c, the same for every block of the CTA, is read from tensor memory (columns
+        // KT_COL + 32 c, bf16 pairs), so these MMAs read only the 1 KB Q_c slice from shared
+        // memory: from shared memory both, an M128 N32 K16 MMA costs 40 cycles of shared-memory
+        // bandwidth instead of its 16 on the tensor pipe.
         auto issue_sdp = [&](int s, int h) {
             const uint64_t sq = d_q + (uint64_t)s * SG + (uint64_t)h * HQ;
             for (int c = 0; c < 2; ++c) {  // K = d
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ss_elect(tmem + c * 64 + 32 * h, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
+                    mma_ts_elect(tmem + c * 64 + 32 * h, tmem + KT_COL + 32 * c + 8 * kk, sq + c * QB + kk * KS, id_s,
+                                 kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // K = dv = 128 over the two 64-column halves
@@ -491,7 +499,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                              sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS, id_s, kk > 0);
             mma_commit_elect(b_s(h));
         };
-        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && (n_items == 0 || warp_all(mbar_wait(b_sf(0), 0, ab)));
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && warp_all(mbar_wait(b_kt, 0, ab)) &&
+                  (n_items == 0 || warp_all(mbar_wait(b_sf(0), 0, ab)));
         if (ok && n_items > 0) {
             tc_fence_after();
             issue_sdp(0, 0);
@@ -541,8 +550,26 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const int q_end = key_ok ? len : 0;       // visible query rows of this key: [q_min, q_end)
         const int q_min = p.causal ? kj : 0;
         const float sl2 = p.scale_log2, sc = p.scale;
-        bool ok = true;
-        for (int it = 0; it < n_items; ++it) {
+        // K_w (this thread's key row, bf16 pairs) into tensor memory columns KT_COL + 32 w: the
+        // A operand of the score MMAs. The row sits in the 128-byte-swizzled TMA box.
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab));
+        if (ok) {
+            const uint32_t row = sb + OFF_K + (uint32_t)w * KBOX + (uint32_t)k * ROW;
+            uint32_t kw[32];
+#pragma unroll
+            for (int jc = 0; jc < 8; ++jc) {
+                const float4 v = lds_f4(row + ((uint32_t)(jc ^ (k & 7)) << 4));
+                kw[4 * jc] = __float_as_uint(v.x);
+                kw[4 * jc + 1] = __float_as_uint(v.y);
+                kw[4 * jc + 2] = __float_as_uint(v.z);
+                kw[4 * jc + 3] = __float_as_uint(v.w);
+            }
+            tmem_st32(tmem + lo + KT_COL + 32 * w, kw);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(b_kt);
+        for (int it = 0; ok && it < n_items; ++it) {
             if (!(ok = warp_all(mbar_wait(b_s(w), (uint32_t)it & 1u, ab)))) break;
             tc_fence_after();
             const int s = it % STAGES;
