@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "sm103a_ptx.cuh"
 
 namespace diffattn {
 namespace {
@@ -54,15 +55,6 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int byt
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
 
 struct DecodeSmemLayout {
     static constexpr size_t k_tile = (size_t)TK * KROW * 2;
@@ -171,27 +163,27 @@ diffattn_decode_split_kernel(const KvParams p) {
         {
             const int j = tid & (TK - 1), c = tid >> 6;
             const __nv_bfloat16* krow = ks + (size_t)buf * TK * KROW + j * KROW + c * DK;
-            float kf[DK];
+            uint64_t kf[DK / 2];  // packed (k[2i], k[2i+1])
 #pragma unroll
             for (int e = 0; e < DK; e += 8) {
-                float f8[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4*>(krow + e), f8);
+                const uint4 u = *reinterpret_cast<const uint4*>(krow + e);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) kf[e + i] = f8[i];
+                for (int i = 0; i < 4; ++i)
+                    kf[e / 2 + i] = f2_pack(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
             }
             const int key = kt + j;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float* qr = qs + r * 2 * DK + c * DK;
-                float s0 = 0.f, s1 = 0.f;
+                // even and odd coordinates summed separately, in one packed multiply-add per pair
+                const uint64_t* qr = reinterpret_cast<const uint64_t*>(qs + r * 2 * DK + c * DK);
+                uint64_t s2 = f2_pack(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < DK; e += 2) {
-                    s0 = fmaf(qr[e], kf[e], s0);
-                    s1 = fmaf(qr[e + 1], kf[e + 1], s1);
-                }
+                for (int e = 0; e < DK / 2; ++e) s2 = ffma2(qr[e], kf[e], s2);
+                const float2 sv = f2_unpack(s2);
                 const int t = r / G;
                 const bool vis = key < k1 && (!p.causal || key <= q_off + t);
-                ps[(r * 2 + c) * TK + j] = vis ? (s0 + s1) * sl2 : -INFINITY;
+                ps[(r * 2 + c) * TK + j] = vis ? (sv.x + sv.y) * sl2 : -INFINITY;
             }
         }
         __syncthreads();
@@ -223,6 +215,8 @@ diffattn_decode_split_kernel(const KvParams p) {
                 acc[pr][0] *= alpha_s[pr];
                 acc[pr][1] *= alpha_s[pr];
             }
+            // (Packed fp32 pairs here, with the probabilities stored twice per key, measured
+            // slower: the doubled probability traffic cost more than the halved FMA count.)
 #pragma unroll 2
             for (int j = kh * (TK / 2); j < kh * (TK / 2) + TK / 2; j += 4) {
                 float vx[4], vy[4];
