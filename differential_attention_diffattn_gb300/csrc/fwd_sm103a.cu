@@ -264,6 +264,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         const uint32_t t_o = tmem + lane_off + col_o(c);
         const int qi = qt * BM + r;
         const float sl2 = p.scale_log2;
+        const uint64_t sl2p = f2_pack(sl2, sl2);
         float m = -INFINITY;  // running max of scores * scale * log2(e)
         float l = 0.f;        // running sum of 2^(x - m)
         bool ok = true;
@@ -272,12 +273,12 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             tc_fence_after();
             float x[BN];
             {
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) tmem_ld32(t_s + ch * 32, sr[ch]);
+                // one wide load (measured faster than four 32-column loads)
+                uint32_t sr[BN];
+                tmem_ld128(t_s, sr);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
+                for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e]);
             }
             const int kbase = j * BN;
             if ((p.causal && j == qt) || kbase + BN > len) {
@@ -302,29 +303,32 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 alpha = ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
                 m = m_tile;
             }
-            const float neg_m = -m;
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            // x * scale * log2(e) - m and the row sum as packed fp32 pairs (half the
+            // instructions of the scalar forms)
+            const uint64_t nmp = f2_pack(-m, -m);
+            uint64_t sa = 0, sb = 0;
             // P_c (bf16 pairs: column i holds keys 2i (low half) and 2i+1) over S_c, stored
             // 32 keys at a time so the TMEM stores overlap the next chunk's exponentials.
 #pragma unroll
             for (int ch = 0; ch < BN / 32; ++ch) {
 #pragma unroll
                 for (int e = ch * 32; e < ch * 32 + 32; e += 4) {
-                    x[e] = ex2_approx(fmaf(x[e], sl2, neg_m));
-                    x[e + 1] = ex2_approx(fmaf(x[e + 1], sl2, neg_m));
-                    x[e + 2] = ex2_approx(fmaf(x[e + 2], sl2, neg_m));
-                    x[e + 3] = ex2_approx(fmaf(x[e + 3], sl2, neg_m));
-                    s0 += x[e];
-                    s1 += x[e + 1];
-                    s2 += x[e + 2];
-                    s3 += x[e + 3];
+                    const float2 u0 = f2_unpack(ffma2(f2_pack(x[e], x[e + 1]), sl2p, nmp));
+                    const float2 u1 = f2_unpack(ffma2(f2_pack(x[e + 2], x[e + 3]), sl2p, nmp));
+                    x[e] = ex2_approx(u0.x);
+                    x[e + 1] = ex2_approx(u0.y);
+                    x[e + 2] = ex2_approx(u1.x);
+                    x[e + 3] = ex2_approx(u1.y);
+                    sa = fadd2(sa, f2_pack(x[e], x[e + 1]));
+                    sb = fadd2(sb, f2_pack(x[e + 2], x[e + 3]));
                 }
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(x[ch * 32 + 2 * i], x[ch * 32 + 2 * i + 1]);
                 tmem_st16(t_s + ch * 16, pk);
             }
-            l = l * alpha + ((s0 + s1) + (s2 + s3));
+            const float2 sab = f2_unpack(fadd2(sa, sb));
+            l = l * alpha + (sab.x + sab.y);
             // O_c holds the sum through tile j-1 here: S_c(j) was issued after PV_c(j-1).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
