@@ -675,7 +675,7 @@ def run_ours_kv(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
                      "frac": round(achieved / float(pk["hbm_gbs"]), 4), "traffic": None,
                      "peak_kind": f"{pk_kind} HBM copy bandwidth",
-                     "kernel": "diffattn_decode_split_kernel + diffattn_decode_combine_kernel",
+                     "kernel": "diffattn_decode_tc_kernel + diffattn_decode_combine_kernel",
                      "launch_ms": round(fwd_ms, 5)},
         "clocks": clocks, "gpu_launches": 3 * args.steps, "impl": "ours",
     }

@@ -91,7 +91,7 @@ bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
     if (n == 0) {
         const long long ctas = (long long)d.batch * d.num_kv_heads;
         const int rows = d.q_len * (d.num_heads / d.num_kv_heads);
-        const long long slots = 152LL * (decode_rows_supported(rows) ? decode_ctas_per_sm(rows) : 1);
+        const long long slots = 152LL * (decode_rows_supported(rows) ? decode_ctas_per_sm() : 1);
         const long long max_n = (cap + 255) / 256;
         double best = -1.0;
         n = 1;
@@ -275,6 +275,7 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
     if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
     if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
     if ((long long)ds.batch * ds.cache_capacity * ds.num_kv_heads * ds.dv >= (1LL << 40) ||
+        (long long)ds.batch * ds.cache_capacity > INT32_MAX - 64 ||
         (long long)ds.batch * ds.q_len * ds.num_heads > INT32_MAX || ds.batch > 65535 || ds.num_kv_heads > 65535)
         return DIFFATTN_ERR_INVALID_ARG;
     const int rows = ds.q_len * (ds.num_heads / ds.num_kv_heads);
@@ -315,7 +316,13 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
     p.lambda_init = lambda_init;
     p.eps = ds.eps;
     p.scale = (float)(1.0 / std::sqrt((double)ds.d));
-    return launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+    p.timeout_ns = g_timeout_ns;
+    KvTensorMaps maps;
+    const uint64_t cache_rows = (uint64_t)ds.batch * ds.cache_capacity;
+    if (!encode_bf16_rows(&maps.k, k_cache, (uint64_t)ds.num_kv_heads * 2 * ds.d, cache_rows, 64) ||
+        !encode_bf16_rows(&maps.v, v_cache, (uint64_t)ds.num_kv_heads * ds.dv, cache_rows, 64))
+        return DIFFATTN_ERR_CUDA;
+    return launch_decode(p, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -69,6 +69,13 @@ struct KvParams {
     float lambda_init;
     float eps;
     float scale;               // d^-0.5
+    unsigned long long timeout_ns;
+};
+
+// TMA descriptors of the caches: [batch * capacity][Hkv * 2d] and
+// [batch * capacity][Hkv * dv], boxes of 64 columns x 64 rows.
+struct KvTensorMaps {
+    CUtensorMap k, v;
 };
 
 // Backward pass (bf16, d = 64, dv = 128).
@@ -157,7 +164,8 @@ cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, 
                           int n_sets, int d, float lambda_init, float* out, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
-cudaError_t launch_decode(const KvParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const KvParams& p, const KvTensorMaps& maps, cudaStream_t stream);
+cudaError_t launch_decode_tc(const KvParams& p, const KvTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
@@ -169,8 +177,10 @@ cudaError_t launch_rope_qk(const RopeParams& p, bool bf16, bool interleaved, cud
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_out_proj(const GemmParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             cudaStream_t stream);
-int decode_rows_supported(int rows);
-int decode_ctas_per_sm(int rows);  // resident split CTAs per SM for R = rows
-int decode_max_splits();           // most key splits the combine kernel merges
+int decode_rows_supported(int rows);  // R = q_len * (H / Hkv) the cache forward takes
+int decode_ctas_per_sm();             // resident split CTAs per SM
+int decode_max_splits();              // most key splits the combine kernel merges
+int decode_tc_rows_supported(int rows);
+int decode_tc_ctas_per_sm();
 
 }  // namespace diffattn

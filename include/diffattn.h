@@ -239,10 +239,13 @@ unsigned long long diffattn_fwd_kvcache_workspace_size(const diffattn_kv_desc* d
  *  workspace : device, >= diffattn_fwd_kvcache_workspace_size(desc) bytes,
  *              16-byte aligned, owned by the caller; its contents are scratch
  *  out     : [batch][q_len][H][dv] bf16
- * Two launches on `stream`: a key-split kernel writing partial (max, sum, O) of
- * both components to the workspace, and a combine kernel (per-component
- * log-sum-exp merge, O1/l1 - lambda O2/l2, RMSNorm, weight, (1 - lambda_init)).
- * Supported: bf16, d = 64, dv = 128, q_len * (H / Hkv) in {1, 2, 4, 8, 16}.
+ * Two launches on `stream`: a key-split kernel (tensor cores; the cache read
+ * through TMA) writing partial (max, sum, O) of both components to the
+ * workspace, and a combine kernel (per-component log-sum-exp merge,
+ * O1/l1 - lambda O2/l2, RMSNorm, weight, (1 - lambda_init)). Cache rows past
+ * cache_seqlens[b] are read but never used: they may hold any bits.
+ * Supported: bf16, d = 64, dv = 128, 1 <= q_len * (H / Hkv) <= 32, and
+ * batch * cache_capacity below 2^31 - 64.
  * Errors: INVALID_ARG (null / misaligned pointers, bad sizes, workspace too
  * small), UNSUPPORTED, CUDA; cache_seqlens out of range -> BAD_SEQLENS through
  * diffattn_get_device_status (those sequences are not written).

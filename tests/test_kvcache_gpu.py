@@ -25,8 +25,10 @@ def kvw(**kw):
     return W.KvWorkload("t", **base)
 
 
+# R = q_len * H / Hkv query rows per kv head: 1 ... 32, powers of two or not
 @pytest.mark.parametrize("H,Hkv,ql", [(16, 4, 1), (4, 4, 1), (8, 4, 1), (16, 16, 2), (16, 4, 2), (16, 4, 4),
-                                      (16, 1, 1), (8, 8, 2)])
+                                      (16, 1, 1), (8, 8, 2), (16, 4, 3), (12, 4, 5), (4, 4, 7), (16, 4, 8),
+                                      (32, 1, 1)])
 def test_rows_per_kv_head(H, Hkv, ql):
     wl = kvw(num_heads=H, num_kv_heads=Hkv, q_len=ql)
     inp = W.generate_kv(wl, seed=H + Hkv + ql, lengths=[1000, 517, ql])
@@ -69,7 +71,7 @@ def test_bad_cache_lengths_reported():
 
 
 def test_unsupported_rows():
-    inp = W.generate_kv(kvw(q_len=3), seed=53)  # 3 * 4 = 12 rows per kv head
+    inp = W.generate_kv(kvw(q_len=9), seed=53)  # 9 * 4 = 36 rows per kv head (at most 32)
     with pytest.raises(da.DiffAttnError) as e:
         run_gpu_kv(inp)
     assert e.value.status == 2
@@ -80,3 +82,23 @@ def test_deterministic_and_workspace_reuse():
     a = run_gpu_kv(inp)
     b = run_gpu_kv(inp)
     assert torch.equal(a, b)
+
+
+def test_poisoned_rows_beyond_lengths_are_never_used():
+    # cache rows past each length (read by the last tile of a split) hold NaN and
+    # Inf: a zero probability times NaN would still be NaN
+    inp = W.generate_kv(kvw(batch=3, q_len=2), seed=55, lengths=[1000, 517, 70])
+    for b, L in enumerate(inp.cache_seqlens.tolist()):
+        inp.k_cache[b, L:] = float("nan")
+        inp.v_cache[b, L::2] = float("nan")
+        inp.v_cache[b, L + 1::2] = float("inf")
+    got = run_gpu_kv(inp)
+    assert torch.isfinite(got.float()).all()
+    compare(got, oracle_kv(inp), "bf16")
+
+
+def test_split_past_the_visible_keys_of_early_rows():
+    # 4 new tokens, chunks of 256 keys: with L = 258 the split [256, 258) sees no
+    # key visible to the first new query (position 254): an empty partial
+    inp = W.generate_kv(kvw(batch=3, q_len=4), seed=56, lengths=[258, 130, 1000])
+    compare(run_gpu_kv(inp, num_splits=4), oracle_kv(inp), "bf16")
