@@ -16,20 +16,22 @@
 // (decode_simt.cu) merges the splits and applies lambda and the RMSNorm.
 //
 // Both components in one pair of MMA chains. The query rows are stacked into
-// two zero-padded 128-row boxes: box 1 holds Q1 of row r at row r, box 2 holds
-// Q2 of row r at row 32 + r. Then
+// two zero-padded boxes: box 1 holds Q1 of row r at row r, box 2 holds Q2 of
+// row r at row 32 + r. Then
 //   S = box1 K1^T + box2 K2^T          (M 128, N 64 keys, K 2 x 64)
 // has S_1 of row r in TMEM lane r and S_2 of row r in lane 32 + r (every other
 // product is with a zero row), and after the softmax
 //   O += P V                           (M 128, N 128, K 64 keys, P from TMEM)
 // accumulates O_1 and O_2 in the same lanes: an output row depends only on its
-// own P row, and the rows the softmax does not write are exactly zero. The
-// padding costs tensor work only; the path is bound by streaming the cache.
+// own P row. The boxes hold rows 0-63 only (8 KB each): rows 64-127 of an
+// M = 128 operand are the next 8 KB of shared memory (box 2, then a K box),
+// whose products land in TMEM lanes 64-127, which nothing reads. The padding
+// costs tensor work only; the path is bound by streaming the cache.
 //
 // Roles (128 threads):
 //   warp 0  softmax of component 1 (TMEM lanes 0-31, rows r < R);
 //   warp 1  softmax of component 2 (lanes 32-63);
-//   warp 2  TMA producer (K1|K2 and V boxes of [64 keys x 64] per tile, 2 stages);
+//   warp 2  TMA producer (K1|K2 and V boxes of [64 keys x 64] per tile, 3 stages);
 //   warp 3  TMEM allocator and MMA issuer.
 // Tensor memory (256 columns, so two CTAs share an SM): S / P double-buffered
 // at [0, 64) and [64, 128), O at [128, 256). S(j + 1) is issued before P(j) V,
@@ -47,11 +49,11 @@ namespace {
 constexpr int TK = 64;                 // keys per tile
 constexpr int HD = 64;                 // component dim d
 constexpr int DV = 128;                // value dim
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;
 constexpr int MAX_ROWS = 32;
 constexpr int NUM_THREADS = 128;
 constexpr int SOFTMAX_WARPS = 2, PRODUCER_WARP = 2, MMA_WARP = 3;
-constexpr uint32_t QBOX_BYTES = 128 * HD * 2;        // one component's stacked query box: 16 KB
+constexpr uint32_t QBOX_BYTES = 64 * HD * 2;         // one component's stacked query box: 8 KB
 constexpr uint32_t KVBOX_BYTES = TK * 64 * 2;        // [64 keys x 64] bf16: 8 KB
 constexpr uint32_t K_BYTES = 2 * KVBOX_BYTES;
 constexpr uint32_t V_BYTES = 2 * KVBOX_BYTES;
@@ -60,8 +62,11 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_STAGE0 = 2 * QBOX_BYTES;
 constexpr uint32_t OFF_MISC = OFF_STAGE0 + STAGES * STAGE_BYTES;
 constexpr uint32_t MISC_BYTES = 256;
-constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + OFF_MISC + MISC_BYTES;
-static_assert(2 * (SMEM_BYTES + 1024) <= 232448, "two CTAs per SM");
+// No alignment slack (two CTAs per SM need every byte): the kernel checks that
+// the dynamic shared memory starts on a 1024-byte boundary (the swizzle atoms'
+// alignment) and reports an error otherwise.
+constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES;
+static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_O = 128;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units; P stays below 2^8
@@ -84,8 +89,11 @@ __device__ __forceinline__ bool warp_all(bool p) { return __all_sync(0xffffffffu
 __global__ void __launch_bounds__(NUM_THREADS)
 diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const KvParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ uint8_t smem[];
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(p.error_word, kErrLayout);
+        return;
+    }
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -123,8 +131,8 @@ diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid
     // chunk c of the row at physical chunk c ^ (x % 8)); every other row zero
     {
         const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q);
-        for (int i = tid; i < 2 * 128 * 8; i += NUM_THREADS) {
-            const int box = i >> 10, x = (i >> 3) & 127, pc = i & 7;
+        for (int i = tid; i < 2 * 64 * 8; i += NUM_THREADS) {
+            const int box = i >> 9, x = (i >> 3) & 63, pc = i & 7;
             const int lc = pc ^ (x & 7);
             const int r = x - 32 * box;  // box 1: rows 0..R-1; box 2: rows 32..32+R-1
             uint4 v = make_uint4(0u, 0u, 0u, 0u);

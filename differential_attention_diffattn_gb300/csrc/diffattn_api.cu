@@ -624,6 +624,7 @@ diffattn_status diffattn_get_device_status(void* stream) {
     if (word & kErrBadSeqlens) return DIFFATTN_ERR_BAD_SEQLENS;
     if (word & kErrBadPositions) return DIFFATTN_ERR_BAD_POSITIONS;
     if (word & kErrTimeout) return DIFFATTN_ERR_TIMEOUT;
+    if (word & kErrLayout) return DIFFATTN_ERR_CUDA;  // a kernel found its shared memory misaligned
     return DIFFATTN_OK;
 }
 

@@ -8,7 +8,7 @@
 namespace diffattn {
 
 // Bits of the per-device error word written by kernels.
-enum : uint32_t { kErrTimeout = 1u, kErrBadSeqlens = 2u, kErrBadPositions = 4u };
+enum : uint32_t { kErrTimeout = 1u, kErrBadSeqlens = 2u, kErrBadPositions = 4u, kErrLayout = 8u };
 
 // Default limit of every bounded pipeline wait inside a kernel.
 constexpr unsigned long long kDefaultWaitTimeoutNs = 2000000000ull;
