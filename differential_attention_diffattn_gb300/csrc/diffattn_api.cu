@@ -73,9 +73,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Key-split plan of a cache forward: (number of splits, keys per split), with
 // splits of at least 256 keys (64-key multiples). Without a requested count it
-// tries 1 to 4 full waves of resident split CTAs on the 152 SMs and keeps the
-// count that leaves the fewest idle CTA slots in the last wave (later waves
-// win ties: finer splits balance ragged caches). Deterministic in the shape.
+// takes the fewest waves of resident split CTAs on the 152 SMs (1 to 4) whose
+// last wave is at least 80 % full, else the fullest: every wave repeats the
+// per-CTA setup and pipeline ramp, which measured costlier than a few idle
+// slots (decode_b8_c16384: 9 splits in one wave 5221 GB/s, 19 in two 5009).
+// Deterministic in the shape.
 bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
     if (d.batch < 0 || d.q_len < 1 || d.cache_capacity < d.q_len || d.num_heads <= 0 || d.num_kv_heads <= 0 ||
         d.num_heads % d.num_kv_heads != 0 || d.num_splits < 0)
@@ -103,10 +105,11 @@ bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
             cand = round_plan(cand, &cc);
             const long long total = cand * ctas;
             const double fill = (double)total / (double)(((total + slots - 1) / slots) * slots);
-            if (fill >= best - 1e-9) {
+            if (fill > best + 1e-9) {
                 best = fill;
                 n = cand;
             }
+            if (fill >= 0.8) break;
         }
     }
     n = round_plan(n, &c);
