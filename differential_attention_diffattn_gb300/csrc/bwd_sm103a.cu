@@ -76,28 +76,33 @@ __device__ __forceinline__ bool seq_bounds(const BwdParams& p, int seq, int* sta
 // One thread (= one query row) and 32 keys: dS_1, dS_2 as bf16 pairs from S_1,
 // S_2, dP and the row's (lse_1, lse_2, delta_1, delta_2). MASK zeroes keys at or
 // past `nvis` (the number of visible keys in this group of 32, any value).
+// Adjacent keys go through packed fp32 pairs (half the multiply/add
+// instructions of the scalar form); the second component's factor
+// lambda (delta_2 - dP) is one fused multiply-add, -lambda dP + lambda delta_2.
 template <bool MASK>
 __device__ __forceinline__ void dq_keys32(const uint32_t (&s1)[32], const uint32_t (&s2)[32],
                                           const uint32_t (&dp)[32], const float4 rs, float lam, float sl2, float sc,
                                           int nvis, uint32_t (&d1)[16], uint32_t (&d2)[16]) {
+    const uint64_t sl2p = f2_pack(sl2, sl2), nl1 = f2_pack(-rs.x, -rs.x), nl2 = f2_pack(-rs.y, -rs.y);
+    const uint64_t nd1 = f2_pack(-rs.z, -rs.z), nlam = f2_pack(-lam, -lam), lamd2 = f2_pack(lam * rs.w, lam * rs.w);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
-        float a[2], b[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const float pp = __uint_as_float(dp[i + u]);
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -rs.x));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -rs.y));
-            a[u] = p1 * (pp - rs.z);            // dS_1 / s
-            b[u] = (lam * p2) * (rs.w - pp);    // dS_2 / s
-            if (MASK) {
-                const bool vis = i + u < nvis;
-                a[u] = vis ? a[u] : 0.f;
-                b[u] = vis ? b[u] : 0.f;
-            }
+        const float2 x1 = f2_unpack(ffma2(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])), sl2p, nl1));
+        const float2 x2 = f2_unpack(ffma2(f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])), sl2p, nl2));
+        const uint64_t p1 = f2_pack(ex2_approx(x1.x), ex2_approx(x1.y));
+        const uint64_t p2 = f2_pack(ex2_approx(x2.x), ex2_approx(x2.y));
+        const uint64_t pp = f2_pack(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1]));
+        float2 a = f2_unpack(fmul2(p1, fadd2(pp, nd1)));          // dS_1 / s
+        float2 b = f2_unpack(fmul2(p2, ffma2(pp, nlam, lamd2)));  // dS_2 / s
+        if (MASK) {
+            const bool v0 = i < nvis, v1 = i + 1 < nvis;
+            a.x = v0 ? a.x : 0.f;
+            a.y = v1 ? a.y : 0.f;
+            b.x = v0 ? b.x : 0.f;
+            b.y = v1 ? b.y : 0.f;
         }
-        d1[i / 2] = pack_bf16x2(a[0], a[1]);
-        d2[i / 2] = pack_bf16x2(b[0], b[1]);
+        d1[i / 2] = pack_bf16x2(a.x, a.y);
+        d2[i / 2] = pack_bf16x2(b.x, b.y);
     }
 }
 
