@@ -19,20 +19,34 @@ namespace diffattn {
 namespace {
 
 constexpr int WARPS = 8;
-constexpr int MAX_V4 = 4;  // dv <= 4 * 32 * 4 = 512 values per row
+constexpr int PARTS_PER_ROUND = 4;  // parts whose loads are in flight together
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
+
+__device__ __forceinline__ void axpy4(float4& acc, float w, const float4& x) {
+    acc.x = fmaf(w, x.x, acc.x);
+    acc.y = fmaf(w, x.y, acc.y);
+    acc.z = fmaf(w, x.z, acc.z);
+    acc.w = fmaf(w, x.w, acc.w);
+}
+__device__ __forceinline__ void scale4(float4& acc, float r) {
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
 }
 
 // One warp per (token, head) row; lane l owns the float4 columns l, l + 32, ...
+// (V of them: dv <= 128 V). The parts are merged online, PARTS_PER_ROUND at a
+// time: their lse and outputs are loaded together, the running maximum of each
+// component is raised to the round's largest lse and the running sums rescaled.
+// A part in which the row sees no key has lse = -inf (and an undefined output):
+// its weight is 0 and its values are dropped by a select, never multiplied.
+template <int V>
 __global__ void __launch_bounds__(32 * WARPS) diffattn_merge_kernel(const MergeParams p) {
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
@@ -40,54 +54,65 @@ __global__ void __launch_bounds__(32 * WARPS) diffattn_merge_kernel(const MergeP
     const int h = (int)(row % p.H);
     const int nv4 = p.dv / 4;
     const size_t part_rows = (size_t)p.tokens * p.H;
-    // per component: the largest lse over the parts (lanes stride over the parts)
-    float L[2] = {-INFINITY, -INFINITY};
-    for (int j = lane; j < p.n_parts; j += 32) {
-        const float2 l2 = reinterpret_cast<const float2*>(p.lse)[(size_t)j * part_rows + row];
-        L[0] = fmaxf(L[0], l2.x);
-        L[1] = fmaxf(L[1], l2.y);
-    }
-    L[0] = warp_max(L[0]);
-    L[1] = warp_max(L[1]);
-    float4 acc[2][MAX_V4];
+    float M[2] = {-INFINITY, -INFINITY};  // running maxima of lse
+    float W[2] = {0.f, 0.f};              // running sums of 2^(lse - M)
+    float4 acc[2][V];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int i = 0; i < MAX_V4; ++i) acc[c][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float W[2] = {0.f, 0.f};
-    for (int j = 0; j < p.n_parts; ++j) {
-        const float2 l2 = reinterpret_cast<const float2*>(p.lse)[(size_t)j * part_rows + row];
-        // a part in which the row sees no key has lse = -inf and weight 0
-        const float w0 = l2.x == -INFINITY ? 0.f : exp2f(l2.x - L[0]);
-        const float w1 = l2.y == -INFINITY ? 0.f : exp2f(l2.y - L[1]);
-        W[0] += w0;
-        W[1] += w1;
-        const float4* a = reinterpret_cast<const float4*>(p.o1) + ((size_t)j * part_rows + row) * nv4;
-        const float4* b = reinterpret_cast<const float4*>(p.o2) + ((size_t)j * part_rows + row) * nv4;
+        for (int i = 0; i < V; ++i) acc[c][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < p.n_parts; j0 += PARTS_PER_ROUND) {
+        float2 l[PARTS_PER_ROUND];
+        float4 x[PARTS_PER_ROUND][V], y[PARTS_PER_ROUND][V];
 #pragma unroll
-        for (int i = 0; i < MAX_V4; ++i) {
-            const int c4 = lane + 32 * i;
-            if (c4 < nv4) {
-                if (w0 != 0.f) {
-                    const float4 x = a[c4];
-                    acc[0][i].x = fmaf(w0, x.x, acc[0][i].x); acc[0][i].y = fmaf(w0, x.y, acc[0][i].y);
-                    acc[0][i].z = fmaf(w0, x.z, acc[0][i].z); acc[0][i].w = fmaf(w0, x.w, acc[0][i].w);
-                }
-                if (w1 != 0.f) {
-                    const float4 y = b[c4];
-                    acc[1][i].x = fmaf(w1, y.x, acc[1][i].x); acc[1][i].y = fmaf(w1, y.y, acc[1][i].y);
-                    acc[1][i].z = fmaf(w1, y.z, acc[1][i].z); acc[1][i].w = fmaf(w1, y.w, acc[1][i].w);
+        for (int u = 0; u < PARTS_PER_ROUND; ++u) {
+            const int j = j0 + u;
+            const bool in = j < p.n_parts;
+            const size_t prow = (size_t)(in ? j : 0) * part_rows + row;
+            l[u] = in ? reinterpret_cast<const float2*>(p.lse)[prow] : make_float2(-INFINITY, -INFINITY);
+            const float4* a = reinterpret_cast<const float4*>(p.o1) + prow * nv4;
+            const float4* b = reinterpret_cast<const float4*>(p.o2) + prow * nv4;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int c4 = lane + 32 * i;
+                const bool ok = in && c4 < nv4;
+                x[u][i] = ok ? a[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                y[u][i] = ok ? b[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float m = M[c];
+#pragma unroll
+            for (int u = 0; u < PARTS_PER_ROUND; ++u) m = fmaxf(m, c ? l[u].y : l[u].x);
+            if (m == -INFINITY) continue;  // no visible key so far
+            const float r = M[c] == -INFINITY ? 0.f : exp2f(M[c] - m);
+            W[c] *= r;
+#pragma unroll
+            for (int i = 0; i < V; ++i) scale4(acc[c][i], r);
+#pragma unroll
+            for (int u = 0; u < PARTS_PER_ROUND; ++u) {
+                const float lu = c ? l[u].y : l[u].x;
+                const bool vis = lu != -INFINITY;
+                const float w = vis ? exp2f(lu - m) : 0.f;
+                W[c] += w;
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    float4 v = c ? y[u][i] : x[u][i];
+                    v = vis ? v : make_float4(0.f, 0.f, 0.f, 0.f);
+                    axpy4(acc[c][i], w, v);
                 }
             }
+            M[c] = m;
         }
     }
     // no visible key in any part: the component's output is taken as 0
     const float i0 = W[0] > 0.f ? 1.f / W[0] : 0.f, i1 = W[1] > 0.f ? 1.f / W[1] : 0.f;
     const float lam = p.lambda[h * p.lambda_stride];
     float ss = 0.f;
-    float4 D[MAX_V4];
+    float4 D[V];
 #pragma unroll
-    for (int i = 0; i < MAX_V4; ++i) {
+    for (int i = 0; i < V; ++i) {
         D[i].x = acc[0][i].x * i0 - lam * (acc[1][i].x * i1);
         D[i].y = acc[0][i].y * i0 - lam * (acc[1][i].y * i1);
         D[i].z = acc[0][i].z * i0 - lam * (acc[1][i].z * i1);
@@ -97,7 +122,7 @@ __global__ void __launch_bounds__(32 * WARPS) diffattn_merge_kernel(const MergeP
     ss = warp_sum(ss);
     const float scale = (1.f - p.lambda_init) / sqrtf(ss / (float)p.dv + p.eps);
 #pragma unroll
-    for (int i = 0; i < MAX_V4; ++i) {
+    for (int i = 0; i < V; ++i) {
         const int c4 = lane + 32 * i;
         if (c4 < nv4) {
             const float4 w = reinterpret_cast<const float4*>(p.subln_w)[c4];
@@ -120,7 +145,13 @@ __global__ void __launch_bounds__(32 * WARPS) diffattn_merge_kernel(const MergeP
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     const long long rows = p.tokens * p.H;
-    diffattn_merge_kernel<<<(unsigned)((rows + WARPS - 1) / WARPS), 32 * WARPS, 0, stream>>>(p);
+    const unsigned grid = (unsigned)((rows + WARPS - 1) / WARPS);
+    if (p.dv <= 128)
+        diffattn_merge_kernel<1><<<grid, 32 * WARPS, 0, stream>>>(p);
+    else if (p.dv <= 256)
+        diffattn_merge_kernel<2><<<grid, 32 * WARPS, 0, stream>>>(p);
+    else
+        diffattn_merge_kernel<4><<<grid, 32 * WARPS, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

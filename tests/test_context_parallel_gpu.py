@@ -24,7 +24,10 @@ def _lib():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("bounds,per_head", [([0, 96], False), ([0, 30, 31, 96], True), ([0, 48, 96], False)])
+# more than four parts: the merge kernel takes them four at a time and rescales
+@pytest.mark.parametrize("bounds,per_head", [([0, 96], False), ([0, 30, 31, 96], True), ([0, 48, 96], False),
+                                             ([0, 5, 9, 13, 17, 21, 96], True),
+                                             ([0, 10, 20, 30, 40, 50, 60, 70, 96], False)])
 def test_merge_kernel_matches_oracle(bounds, per_head):
     wl = W.Workload("m", "bf16", num_heads=4, num_kv_heads=2, d=64, dv=128, depth=6, causal=True, batch=1,
                     seqlen=1, random_subln=True, lambda_per_head=per_head)
