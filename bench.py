@@ -188,7 +188,7 @@ def run_ours(args, rank, world, local_rank):
     rope_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] if rope is not None else None
 
-    def fwd(s, i=None):
+    def fwd(s, i=None, lam=lam, w=w, cu=cu):
         q, k = s["q"], s["k"]
         if rope is not None:
             if i is not None:
@@ -279,41 +279,76 @@ def run_ours(args, rank, world, local_rank):
     value = step_flops * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----------------
+    # Every step copies its inputs from pinned host memory, runs lambda + forward
+    # and reads its output back into pinned host memory. The copies run on two
+    # copy streams (host -> device, device -> host) over the two device sets, so
+    # step i + 1's inputs and step i - 1's output move while step i computes;
+    # events keep a set's inputs until its forward has read them and its output
+    # until it has been read back.
     host = {n: getattr(inp, n).pin_memory() for n in ("q", "k", "v", "subln_w", "cu_seqlens")}
     host_l = [x.pin_memory() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
-    out_h = torch.empty(tokens, wl.num_heads, wl.dv, dtype=sets[0]["q"].dtype).pin_memory()
+    out_hs = [torch.empty(tokens, wl.num_heads, wl.dv, dtype=sets[0]["q"].dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + host_l)
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = out_hs[0].numel() * out_hs[0].element_size()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e = [dict(lvec=[torch.empty_like(x) for x in lvec], w=torch.empty_like(w), cu=torch.empty_like(cu),
+                lam=torch.empty_like(lam)) for _ in range(2)]
+    ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        s = sets[0]
-        for n in ("q", "k", "v"):
-            s[n].copy_(dense_view(host[n], inp), non_blocking=True)
-        for dst, src in zip(lvec, host_l):
-            dst.copy_(src, non_blocking=True)
-        w.copy_(host["subln_w"], non_blocking=True)
-        cu.copy_(host["cu_seqlens"], non_blocking=True)
-        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
-        fwd(s)
-        out_h.copy_(s["out"].view(out_h.shape), non_blocking=True)
+    def e2e_h2d(b):
+        s, x = sets[b], e2e[b]
+        s_in.wait_event(ev_done[b])  # the set's previous forward has read its inputs
+        with torch.cuda.stream(s_in):
+            for n in ("q", "k", "v"):
+                s[n].copy_(dense_view(host[n], inp), non_blocking=True)
+            for dst, src in zip(x["lvec"], host_l):
+                dst.copy_(src, non_blocking=True)
+            x["w"].copy_(host["subln_w"], non_blocking=True)
+            x["cu"].copy_(host["cu_seqlens"], non_blocking=True)
+        ev_in[b].record(s_in)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_compute(b):
+        x = e2e[b]
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # the set's previous output has been read back
+        da.diffattn_lambda(*x["lvec"], li, out=x["lam"], stream=stream)
+        fwd(sets[b], lam=x["lam"], w=x["w"], cu=x["cu"])
+        ev_done[b].record(stream)
+
+    def e2e_d2h(b):
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            res = sets[b]["y"] if args.out_proj else sets[b]["out"]  # the step's result
+            out_hs[b].copy_(res.view(out_hs[b].shape), non_blocking=True)
+        ev_out[b].record(s_out)
+
+    def e2e_run(n, start=None, end=None):
+        if start is not None:
+            start.record(s_in)
+        e2e_h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                e2e_h2d((i + 1) % 2)
+            e2e_compute(i % 2)
+            e2e_d2h(i % 2)
+        if end is not None:
+            end.record(s_out)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_run(args.e2e_steps, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = shard.max_over_ranks(e2e_ms)
     e2e_value = step_flops * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
     if da.diffattn_get_device_status() != 0:
         raise RuntimeError("device reported an error in the end-to-end region")
-    if not torch.isfinite(out_h[:: max(1, tokens // 64)].float()).all():
+    if not torch.isfinite(out_hs[(args.e2e_steps - 1) % 2][:: max(1, tokens // 64)].float()).all():
         raise RuntimeError("non-finite output")
 
     if rank != 0:
