@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "sm103a_ptx.cuh"
 
 namespace diffattn {
 namespace {
@@ -36,6 +37,7 @@ constexpr int CWARPS = 8;
 
 __global__ void __launch_bounds__(32 * CWARPS)
 diffattn_decode_combine_kernel(const KvParams p) {
+    griddep_wait();  // a programmatic dependent of the split kernel: its partials are complete
     const int row = blockIdx.x;  // ((b * q_len) + t) * H + h
     const int h = row % p.H;
     const int b = row / (p.H * p.q_len);
@@ -125,8 +127,16 @@ int decode_ctas_per_sm() { return decode_tc_ctas_per_sm(); }
 cudaError_t launch_decode(const KvParams& p, const KvTensorMaps& maps, cudaStream_t stream) {
     cudaError_t err = launch_decode_tc(p, maps, stream);
     if (err != cudaSuccess) return err;
-    diffattn_decode_combine_kernel<<<(unsigned)(p.batch * p.q_len * p.H), 32 * CWARPS, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.batch * p.q_len * p.H));
+    cfg.blockDim = dim3(32 * CWARPS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, diffattn_decode_combine_kernel, p);
 }
 
 }  // namespace diffattn

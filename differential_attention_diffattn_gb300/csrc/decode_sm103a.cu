@@ -98,6 +98,12 @@ diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // Launched as a programmatic dependent of the previous kernel on the stream:
+    // nothing is read before that kernel has completed. The combine kernel may
+    // then be placed as soon as every split CTA is running (it waits for this
+    // grid to complete before it reads a partial).
+    griddep_wait();
+    griddep_launch_dependents();
     const int G = p.H / p.Hkv;
     const int R = p.q_len * G;
     const int L = p.cache_seqlens ? p.cache_seqlens[b] : p.capacity;
@@ -402,9 +408,17 @@ cudaError_t launch_decode_tc(const KvParams& p, const KvTensorMaps& maps, cudaSt
         if (err != cudaSuccess) return err;
         attr_done[dev] = true;
     }
-    dim3 grid((unsigned)p.num_splits, (unsigned)p.Hkv, (unsigned)p.batch);
-    diffattn_decode_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps.k, maps.v, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.num_splits, (unsigned)p.Hkv, (unsigned)p.batch);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, diffattn_decode_tc_kernel, maps.k, maps.v, p);
 }
 
 }  // namespace diffattn

@@ -5,6 +5,7 @@
 // sqrtf as compiled without fast-math) because its acceptance bound is 1e-5
 // max-abs, below what tf32 tensor cores reach.
 #include "internal.h"
+#include "sm103a_ptx.cuh"
 
 namespace diffattn {
 namespace {
@@ -26,6 +27,9 @@ __device__ __forceinline__ float warp_max(float x) {
 __global__ void diffattn_lambda_kernel(const float* __restrict__ lq1, const float* __restrict__ lk1,
                                        const float* __restrict__ lq2, const float* __restrict__ lk2, int n_sets,
                                        int d, float lambda_init, float* __restrict__ out) {
+    // a forward launched next on the stream as a programmatic dependent may start
+    // its setup now; it reads lambda only after this grid has completed
+    griddep_launch_dependents();
     const int set = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (set >= n_sets) return;

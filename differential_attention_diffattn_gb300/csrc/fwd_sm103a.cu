@@ -103,6 +103,10 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sbase = smem_u32(smem);
 
+    // Launched as a programmatic dependent of the previous kernel on the stream
+    // (typically the lambda kernel): nothing is read before it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int h = blockIdx.x;
@@ -461,9 +465,17 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
         attr_done[dev] = true;
     }
     const int n_qt = (p.max_seqlen + BM - 1) / BM;
-    dim3 grid((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
-    diffattn_fwd_bf16_sm103a_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.out, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_kernel, maps.q, maps.k, maps.v, maps.out, p);
 }
 
 }  // namespace diffattn

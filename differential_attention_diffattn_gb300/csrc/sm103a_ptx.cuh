@@ -136,6 +136,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// Programmatic dependent launch. griddep_wait() returns once the kernels this
+// grid depends on (the previous launch on the stream, when launched with
+// programmatic stream serialization) have completed and their memory is
+// visible; before it a kernel may only set itself up. griddep_launch_dependents()
+// lets the next such launch on the stream start its own setup early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- tcgen05 ---
 
 // Whole warp: allocate `ncols` TMEM columns; the base address lands in *slot.
