@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
     diffattn_bwd,
     diffattn_bwd_workspace_size,
     diffattn_fwd,
+    diffattn_fwd_kernel,
     diffattn_fwd_train,
     diffattn_fwd_kvcache,
     diffattn_fwd_kvcache_noalloc,

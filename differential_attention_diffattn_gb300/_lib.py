@@ -22,7 +22,8 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_bwd_workspace_size", "diffattn_bwd", "diffattn_lambda_bwd", "diffattn_fwd_kvcache_workspace_size",
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
-            "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj")
+            "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj",
+            "diffattn_fwd_kernel")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -80,6 +81,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_lambda_init.argtypes = [ctypes.c_int]
         lib.diffattn_lambda.restype = ctypes.c_int
         lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp]
+        lib.diffattn_fwd_kernel.restype = ctypes.c_char_p
+        lib.diffattn_fwd_kernel.argtypes = [ctypes.POINTER(DiffAttnDesc), ctypes.c_int]
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                      vp, ctypes.c_int, vp, vp, vp]
@@ -173,6 +176,15 @@ def diffattn_lambda(lq1, lk1, lq2, lk2, lambda_init: float, out=None, stream=Non
     if st != OK:
         raise DiffAttnError(st, "diffattn_lambda")
     return out
+
+
+def diffattn_fwd_kernel(q, k, v, lam, subln_w, cu_seqlens=None, max_seqlen: Optional[int] = None,
+                        eps: float = 1e-5) -> Optional[str]:
+    """Name of the kernel diffattn_fwd / diffattn_fwd_train launch for these
+    tensors (arguments as for diffattn_fwd; nothing is launched)."""
+    desc, _ = _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps)
+    name = load_library().diffattn_fwd_kernel(ctypes.byref(desc), 1 if cu_seqlens is not None else 0)
+    return name.decode() if name else None
 
 
 def _fwd_desc(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps):

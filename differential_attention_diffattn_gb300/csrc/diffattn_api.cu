@@ -71,6 +71,31 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, ui
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count of the current device (looked up once per device).
+int sm_count() {
+    static int counts[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+    if (counts[dev] == 0) {
+        int n = 0;
+        counts[dev] = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0 ? n : 152;
+    }
+    return counts[dev];
+}
+
+// Which bf16 forward kernel runs. Unpacked inputs with 2 to 10 (query tile,
+// head, sequence) items per SM go to the persistent kernel: it hides the
+// per-CTA setup and the gap between CTAs (measured x1.07 at B = 4, T = 2048,
+// 6.7 items per SM; even at T = 16384, 13.5 per SM). Packed sequences stay on
+// the one-item-per-CTA kernel (their empty items unbalance the persistent
+// kernel's static schedule: x0.98), and so do grids of about one item per SM.
+bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
+    if (packed) return false;
+    const long long items = (long long)((max_seqlen + 127) / 128) * heads * num_seqs;
+    const long long sms = sm_count();
+    return items >= 2 * sms && items <= 10 * sms;
+}
+
 // Key-split plan of a cache forward: (number of splits, keys per split), with
 // splits of at least 256 keys (64-key multiples). Without a requested count it
 // takes the fewest waves of resident split CTAs on the 152 SMs (1 to 4) whose
@@ -237,11 +262,25 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens) ||
         !encode_bf16_rows(&maps.out, out, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
-    return launch_fwd_bf16_sm103a(p, maps, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+    const cudaError_t err = fwd_use_persistent(cu_seqlens != nullptr, p.max_seqlen, p.H, p.num_seqs)
+                                ? launch_fwd_bf16_persistent(p, maps, st)
+                                : launch_fwd_bf16_sm103a(p, maps, st);
+    return err == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 }  // namespace
 
 extern "C" {
+
+const char* diffattn_fwd_kernel(const diffattn_desc* desc, int packed) {
+    if (!desc || desc->num_heads <= 0) return nullptr;
+    const diffattn_desc& ds = *desc;
+    if (ds.dtype == DIFFATTN_DTYPE_F32 && (ds.d == 16 || ds.d == 32 || ds.d == 64)) return "diffattn_fwd_f32_kernel";
+    if (ds.dtype != DIFFATTN_DTYPE_BF16 || ds.d != 64) return nullptr;
+    const int max_seqlen = packed ? ds.max_seqlen : ds.seqlen;
+    const int num_seqs = packed ? ds.num_seqs : ds.batch;
+    return fwd_use_persistent(packed != 0, max_seqlen, ds.num_heads, num_seqs) ? "diffattn_fwd_bf16_persistent_kernel"
+                                                                               : "diffattn_fwd_bf16_sm103a_kernel";
+}
 
 diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
                              const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,

@@ -1,0 +1,480 @@
+// Persistent form of the fused differential-attention forward for sm_103a
+// (bf16 in, fp32 accumulate, bf16 out), d = 64, dv = 128, used for unpacked
+// inputs with a few (query tile, sequence, head) items per SM: one CTA per SM
+// walks the items in a static snake order over items sorted longest first (every
+// CTA gets about the same number of key tiles), and the next item's Q and K / V
+// loads and its first scores run while the softmax warpgroups finish the current
+// item's epilogue. That hides the per-CTA setup and the gap between CTAs, which
+// weigh most when each item has few key tiles.
+//
+// Per item the arithmetic is that of the one-item-per-CTA kernel (fwd_sm103a.cu):
+// S_c = Q_c K_c^T, two online softmaxes, O_c += P_c V on the tensor cores, then
+// O1/l1 - lambda O2/l2, RMSNorm over dv, weight, (1 - lambda_init)
+// ("DiffTransformer.py", forward; "LlamaDiffSdpaAttention.py", forward).
+//
+// Roles (320 threads): warps 0-3 / 4-7 softmax of component 1 / 2 and the
+// epilogue; warp 8 TMA producer; warp 9 TMEM allocator and MMA issuer.
+// Barriers that advance once per item: q_full / q_empty (the Q box), o_full /
+// o_empty (the O accumulators: an item's first P V waits until the epilogue of
+// the previous one has read them); once per key tile over all items: the K / V
+// ring, s_full, p_ready. The epilogue reads O twice (the sum of squares, then
+// the normalised output) so that D is not held across the exchange between the
+// warpgroups: held, it pushed the kernel past the 168-register cap of ten warps.
+// Every wait is bounded; a warp whose wait ran out still passes the epilogue's
+// barriers, where the warpgroups decide together to stop.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace diffattn {
+namespace {
+
+constexpr int BM = 128, BN = 128, HD = 64, DV = 128, STAGES = 3;
+constexpr int NUM_THREADS = 320, PRODUCER_WARP = 8, MMA_WARP = 9;
+constexpr uint32_t BOX_BYTES = BM * HD * 2;
+constexpr uint32_t Q_BYTES = 2 * BOX_BYTES, K_BYTES = 2 * BOX_BYTES, V_BYTES = 2 * BOX_BYTES;
+constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;
+constexpr uint32_t OFF_Q = 0, OFF_STAGE0 = Q_BYTES;
+constexpr uint32_t OFF_MISC = OFF_STAGE0 + STAGES * STAGE_BYTES;
+constexpr uint32_t MISC_BYTES = 3072;
+// No alignment slack: every byte up to the per-block limit is in use; the
+// kernel checks that its dynamic shared memory starts on a 1024-byte boundary.
+constexpr uint32_t SMEM_BYTES = OFF_MISC + MISC_BYTES;
+static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared memory limit");
+constexpr uint32_t TMEM_COLS = 512;
+__device__ __forceinline__ uint32_t col_s(int c) { return (uint32_t)c * 128u; }
+__device__ __forceinline__ uint32_t col_o(int c) { return 256u + (uint32_t)c * 128u; }
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+struct Misc {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
+    uint64_t s_full[2], p_ready[2];
+    uint64_t o_full, o_empty;
+    uint32_t tmem_base;
+    int abort_flag;
+    float xch[4 * BM];  // 1/l_c and the partial sums of squares, between the two warpgroups
+    float w[DV];
+};
+static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_value(uint32_t saddr) { return smem_desc_sw128(saddr, BOX_BYTES, 1024); }
+__device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffffffu, pred); }
+// Named barrier over n threads that also returns the AND of `v` over them.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// One work item: 128 query rows of one diff head of one sequence.
+struct Item {
+    int h, qt, start, len, n_kv;
+};
+// Item `idx` in longest-first order (query tile descending, then sequence, then
+// head); false when it is empty (past its sequence) or its sequence bounds are bad.
+__device__ __forceinline__ bool item_at(const FwdParams& p, int n_qt, int idx, Item& it) {
+    const int per_qt = p.H * p.num_seqs;
+    const int qt = n_qt - 1 - idx / per_qt;
+    const int rem = idx % per_qt;
+    const int seq = rem / p.H;
+    it.h = rem % p.H;
+    it.qt = qt;
+    if (p.cu_seqlens != nullptr) {
+        const int s0 = p.cu_seqlens[seq], s1 = p.cu_seqlens[seq + 1];
+        const bool bad = s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen ||
+                         (seq == 0 && s0 != 0) || (seq == p.num_seqs - 1 && s1 != p.total_tokens);
+        if (bad) {
+            if (threadIdx.x == 0) atomicOr(p.error_word, kErrBadSeqlens);
+            return false;
+        }
+        it.start = s0;
+        it.len = s1 - s0;
+    } else {
+        it.start = seq * p.seqlen;
+        it.len = p.seqlen;
+    }
+    if (qt * BM >= it.len) return false;
+    it.n_kv = p.causal ? qt + 1 : (it.len + BN - 1) / BN;
+    return true;
+}
+// The r-th item slot of this CTA in the snake order (-1 past the end of round r).
+__device__ __forceinline__ int snake(int r, int n_items) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    const int idx = r * G + ((r & 1) ? G - 1 - c : c);
+    return idx < n_items ? idx : -1;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_qt, int n_items) {
+    extern __shared__ uint8_t smem[];
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(p.error_word, kErrLayout);
+        return;
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rounds = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+
+    const uint32_t bar_q_full = smem_u32(&ms.q_full), bar_q_empty = smem_u32(&ms.q_empty);
+    auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
+    auto bar_v_full = [&](int s) { return smem_u32(&ms.v_full[s]); };
+    auto bar_kv_empty = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
+    auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
+    const uint32_t bar_o_full = smem_u32(&ms.o_full), bar_o_empty = smem_u32(&ms.o_empty);
+    const uint32_t sq = sbase + OFF_Q;
+    auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
+    auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
+
+    if (warp == PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_init(bar_q_full, 1);
+        mbar_init(bar_q_empty, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_k_full(s), 1);
+            mbar_init(bar_v_full(s), 1);
+            mbar_init(bar_kv_empty(s), 1);
+        }
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(bar_s_full(c), 1);
+            mbar_init(bar_p_ready(c), 128);
+        }
+        mbar_init(bar_o_full, 1);
+        mbar_init(bar_o_empty, 256);
+        ms.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == PRODUCER_WARP)
+        for (int i = lane; i < DV; i += 32) ms.w[i] = p.subln_w[i];
+    if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem_base;
+    const AbortState ab{&ms.abort_flag, p.error_word, p.timeout_ns};
+
+    if (warp == PRODUCER_WARP) {
+        // ================================================= TMA producer ===
+        if (lane == 0 && p.inject != 1) {
+            const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
+            int tile = 0, items = 0;  // key tiles and items of this CTA so far
+            bool ok = true;
+            for (int r = 0; ok && r < rounds; ++r) {
+                Item it;
+                const int idx = snake(r, n_items);
+                if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
+                const int g = it.h / (p.H / p.Hkv);
+                if (!(ok = mbar_wait(bar_q_empty, ((uint32_t)items & 1u) ^ 1u, ab))) break;
+                const int row_q = it.start + it.qt * BM;
+                mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
+                tma_load_2d(sq, &tm_q, bar_q_full, it.h * 2 * HD, row_q, pol_q);
+                tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, it.h * 2 * HD + HD, row_q, pol_q);
+                for (int j = 0; j < it.n_kv; ++j, ++tile) {
+                    const int s = tile % STAGES;
+                    if (!(ok = mbar_wait(bar_kv_empty(s), ((uint32_t)(tile / STAGES) & 1u) ^ 1u, ab))) break;
+                    const int row = it.start + j * BN;
+                    mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
+                    tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
+                    tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
+                    mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
+                    tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
+                    tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+                }
+                ++items;
+            }
+            // Let every copy this CTA started land before shared memory goes away.
+            if (items > 0) mbar_wait_drain(bar_q_full, (uint32_t)(items - 1) & 1u, p.timeout_ns);
+            for (int j = tile > STAGES ? tile - STAGES : 0; j < tile; ++j) {
+                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+                mbar_wait_drain(bar_k_full(j % STAGES), ph, p.timeout_ns);
+                mbar_wait_drain(bar_v_full(j % STAGES), ph, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ==================================================== MMA issuer ===
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
+        constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, STG = STAGE_BYTES >> 4, BOX = BOX_BYTES >> 4;
+        const uint64_t qdesc = desc_kmajor(sq), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
+        auto issue_s = [&](int c, int tile) {
+            const uint64_t a0 = qdesc + (uint64_t)c * BOX;
+            const uint64_t b0 = kdesc + (uint64_t)(tile % STAGES) * STG + (uint64_t)c * BOX;
+            const uint32_t d = tmem + col_s(c);
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a0 + kk * KSTEP, b0 + kk * KSTEP, idesc_s, kk > 0 ? 1u : 0u);
+            mma_commit_elect(bar_s_full(c));
+        };
+        auto issue_pv = [&](int c, int tile, bool first) {
+            const uint64_t b0 = vdesc + (uint64_t)(tile % STAGES) * STG;
+            const uint32_t d = tmem + col_o(c), a = tmem + col_s(c);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, (kk > 0 || !first) ? 1u : 0u);
+        };
+        int tile = 0, items = 0;
+        bool ok = true;
+        for (int r = 0; ok && r < rounds; ++r) {
+            Item it;
+            const int idx = snake(r, n_items);
+            if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
+            // S of the item's first tile: the S columns are free (the previous item's last
+            // P V was issued before, and the tensor pipe completes in issue order)
+            if (!(ok = warp_all(mbar_wait(bar_q_full, (uint32_t)items & 1u, ab)))) break;
+            if (!(ok = warp_all(mbar_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
+            tc_fence_after();
+            issue_s(0, tile);
+            issue_s(1, tile);
+            for (int j = 0; j < it.n_kv; ++j, ++tile) {
+                const int s = tile % STAGES;
+                const bool has_next = j + 1 < it.n_kv;
+                const int t1 = tile + 1;
+                if (!(ok = warp_all(mbar_wait(bar_v_full(s), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
+                if (j == 0 && !(ok = warp_all(mbar_wait(bar_o_empty, ((uint32_t)items & 1u) ^ 1u, ab)))) break;
+                if (!(ok = warp_all(mbar_wait(bar_p_ready(0), (uint32_t)tile & 1u, ab)))) break;
+                tc_fence_after();
+                issue_pv(0, tile, j == 0);
+                if (has_next) {
+                    if (!(ok = warp_all(mbar_wait(bar_k_full(t1 % STAGES), (uint32_t)(t1 / STAGES) & 1u, ab)))) break;
+                    issue_s(0, t1);
+                }
+                if (!(ok = warp_all(mbar_wait(bar_p_ready(1), (uint32_t)tile & 1u, ab)))) break;
+                tc_fence_after();
+                issue_pv(1, tile, j == 0);
+                mma_commit_elect(bar_kv_empty(s));
+                if (has_next) issue_s(1, t1);
+            }
+            if (!ok) break;
+            mma_commit_elect(bar_q_empty);  // every MMA reading this item's Q has been issued
+            mma_commit_elect(bar_o_full);
+            ++items;
+        }
+        // every MMA issued has completed before TMEM is released
+        mma_commit_elect(bar_q_empty);
+        mbar_wait_drain(bar_q_empty, (uint32_t)items & 1u, p.timeout_ns);
+        __syncwarp();
+    } else {
+        // ============================ softmax and epilogue (warps 0-7) ===
+        const int c = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;  // query row in the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + col_s(c);
+        const uint32_t t_o = tmem + lane_off + col_o(c);
+        const float sl2 = p.scale_log2;
+        const uint64_t sl2p = f2_pack(sl2, sl2);
+        int tile = 0, items = 0;
+        bool ok = true;
+        for (int rd = 0; rd < rounds; ++rd) {
+            Item it;
+            const int idx = snake(rd, n_items);
+            if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
+            const int qi = it.qt * BM + r;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; ok && j < it.n_kv; ++j, ++tile) {
+                if (!(ok = warp_all(mbar_wait(bar_s_full(c), (uint32_t)tile & 1u, ab)))) break;
+                tc_fence_after();
+                float x[BN];
+                {
+                    uint32_t sr[BN];
+                    tmem_ld128(t_s, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e]);
+                }
+                const int kbase = j * BN;
+                if ((p.causal && j == it.qt) || kbase + BN > it.len) {
+                    int lim = p.causal ? min(qi + 1, it.len) : it.len;
+                    lim -= kbase;
+#pragma unroll
+                    for (int e = 0; e < BN; ++e)
+                        if (e >= lim) x[e] = -INFINITY;
+                }
+                float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]), mx3 = fmaxf(x[6], x[7]);
+#pragma unroll
+                for (int e = 8; e < BN; e += 8) {
+                    mx0 = fmax3(mx0, x[e], x[e + 1]);
+                    mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
+                    mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
+                    mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
+                }
+                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+                float alpha = 1.f;
+                if (m_tile > m + RESCALE_THRESHOLD) {
+                    alpha = ex2_approx(m - m_tile);
+                    m = m_tile;
+                }
+                const uint64_t nmp = f2_pack(-m, -m);
+                uint64_t sa = 0, sb = 0;
+#pragma unroll
+                for (int ch = 0; ch < BN / 32; ++ch) {
+#pragma unroll
+                    for (int e = ch * 32; e < ch * 32 + 32; e += 4) {
+                        const float2 u0 = f2_unpack(ffma2(f2_pack(x[e], x[e + 1]), sl2p, nmp));
+                        const float2 u1 = f2_unpack(ffma2(f2_pack(x[e + 2], x[e + 3]), sl2p, nmp));
+                        x[e] = ex2_approx(u0.x);
+                        x[e + 1] = ex2_approx(u0.y);
+                        x[e + 2] = ex2_approx(u1.x);
+                        x[e + 3] = ex2_approx(u1.y);
+                        sa = fadd2(sa, f2_pack(x[e], x[e + 1]));
+                        sb = fadd2(sb, f2_pack(x[e + 2], x[e + 3]));
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(x[ch * 32 + 2 * i], x[ch * 32 + 2 * i + 1]);
+                    tmem_st16(t_s + ch * 16, pk);
+                }
+                const float2 sab = f2_unpack(fadd2(sa, sb));
+                l = l * alpha + (sab.x + sab.y);
+                // O_c holds this item's sum through tile j-1 (S_c(j) was issued after PV_c(j-1))
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int ch = 0; ch < DV / 32; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + ch * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_o + ch * 32, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar_p_ready(c));
+            }
+            // Every warp passes both epilogue barriers, also after a wait of its own ran
+            // out (ok false); the decision to stop is taken at the second one, jointly.
+            if (ok && p.lse != nullptr && qi < it.len) p.lse[((size_t)(it.start + qi) * p.H + it.h) * 2 + c] = m + __log2f(l);
+            // ---- epilogue: warpgroup c handles values [64c, 64c + 64) of every row
+            ms.xch[c * BM + r] = 1.f / l;
+            named_barrier_sync(1, 256);
+            ok = warp_all(ok && mbar_wait(bar_o_full, (uint32_t)items & 1u, ab));
+            const bool store = qi < it.len;
+            // Two passes over O (D is not kept across the exchange, which keeps the
+            // register count under the cap of ten warps): the sum of squares of this
+            // warpgroup's half of D, then D again, normalised and stored.
+            const float lam = p.lambda[it.h * p.lambda_stride];
+            const float il1 = ms.xch[r], il2 = ms.xch[BM + r];
+            const uint32_t t_o1 = tmem + lane_off + col_o(0) + 64 * c;
+            const uint32_t t_o2 = tmem + lane_off + col_o(1) + 64 * c;
+            float ssp = 0.f;
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(t_o1 + ch * 32, o1);
+                    tmem_ld32(t_o2 + ch * 32, o2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float d = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                        ssp = fmaf(d, d, ssp);
+                    }
+                    if (store && p.o1 != nullptr) {
+                        const size_t base = ((size_t)(it.start + qi) * p.H + it.h) * DV / 4 + c * 16 + ch * 8;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            reinterpret_cast<float4*>(p.o1)[base + i] =
+                                make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
+                                            __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
+                            reinterpret_cast<float4*>(p.o2)[base + i] =
+                                make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
+                                            __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
+                        }
+                    }
+                }
+            }
+            ms.xch[2 * BM + c * BM + r] = ssp;
+            ok = named_barrier_and(1, 256, ok);
+            if (ok) {
+                const float ss = ms.xch[2 * BM + r] + ms.xch[3 * BM + r];
+                const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DV + p.eps);
+                const float* wv = ms.w + 64 * c;
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                      ((size_t)(it.start + (store ? qi : 0)) * p.H + it.h) * DV + 64 * c);
+#pragma unroll 1
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(t_o1 + ch * 32, o1);
+                    tmem_ld32(t_o2 + ch * 32, o2);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int e = ch * 32 + 2 * i;
+                        const float d0 = __uint_as_float(o1[2 * i]) * il1 - lam * (__uint_as_float(o2[2 * i]) * il2);
+                        const float d1 = __uint_as_float(o1[2 * i + 1]) * il1 - lam * (__uint_as_float(o2[2 * i + 1]) * il2);
+                        pk[i] = pack_bf16x2(d0 * post * wv[e], d1 * post * wv[e + 1]);
+                    }
+                    if (store) {
+#pragma unroll
+                        for (int g4 = 0; g4 < 4; ++g4)
+                            dst[ch * 4 + g4] = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
+                    }
+                }
+            }
+            // O has been read: the next item's first P V may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar_o_empty);
+            if (!ok) break;
+            ++items;
+        }
+    }
+
+    // ---- teardown: all TMEM traffic of this CTA is complete -----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16_persistent(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream) {
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !attr_done[dev]) {
+        err = cudaFuncSetAttribute(diffattn_fwd_bf16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        attr_done[dev] = true;
+    }
+    int sms = 0;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const int n_qt = (p.max_seqlen + BM - 1) / BM;
+    const long long n_items = (long long)n_qt * p.H * p.num_seqs;
+    if (n_items <= 0 || n_items > INT32_MAX) return cudaErrorInvalidValue;
+    const int grid = (int)(n_items < sms ? n_items : sms);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_persistent_kernel, maps.q, maps.k, maps.v, p, n_qt,
+                              (int)n_items);
+}
+
+}  // namespace diffattn

@@ -164,6 +164,7 @@ cudaError_t launch_lambda(const float* lq1, const float* lk1, const float* lq2, 
                           int n_sets, int d, float lambda_init, float* out, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_persistent(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_decode(const KvParams& p, const KvTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_decode_tc(const KvParams& p, const KvTensorMaps& maps, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);

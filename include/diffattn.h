@@ -105,6 +105,17 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
                                 float* lambda_out, void* stream);
 
 /*
+ * Name of the kernel diffattn_fwd / diffattn_fwd_train launch for `desc`
+ * (packed nonzero: with cu_seqlens), or NULL for an unsupported dtype / d.
+ * bf16 inputs run "diffattn_fwd_bf16_sm103a_kernel" (one CTA per 128 query rows
+ * of one head of one sequence) or, unpacked with 2 to 10 of those items per SM,
+ * "diffattn_fwd_bf16_persistent_kernel" (one CTA per SM walking the items); the
+ * two compute the same function. fp32 inputs run "diffattn_fwd_f32_kernel".
+ * Host-only: no launch; the returned string is static.
+ */
+const char* diffattn_fwd_kernel(const diffattn_desc* desc, int packed);
+
+/*
  * Differential-attention forward (one launch of the fused kernel).
  * Source: as in the file header; the output-difference form
  * O1/l1 - lambda O2/l2 of "LlamaDiffSdpaAttention.py", forward, with the

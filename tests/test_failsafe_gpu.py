@@ -27,15 +27,18 @@ def _lib():
     da.diffattn_set_wait_timeout_ns(0)
 
 
-def test_wait_timeout_reported_and_context_usable():
-    inp = W.generate(W.WORKLOADS["b2_t512_gqa"], seed=71, seq_lens=[256, 100])
+# packed: the one-item-per-CTA kernel; an unpacked batch of 3 x 1000 tokens
+# (384 items): the persistent kernel, whose warps must all leave their loops
+@pytest.mark.parametrize("lens,packed", [([256, 100], True), ([1000, 1000, 1000], False)])
+def test_wait_timeout_reported_and_context_usable(lens, packed):
+    inp = W.generate(W.WORKLOADS["b2_t512_gqa"], seed=71, seq_lens=lens)
     da.diffattn_set_wait_timeout_ns(20_000_000)  # 20 ms
     da.diffattn_set_fault_injection(1)
     try:
         with pytest.raises(AssertionError, match="timed out"):
-            run_gpu(inp)
+            run_gpu(inp, packed=packed)
     finally:
         da.diffattn_set_fault_injection(0)
         da.diffattn_set_wait_timeout_ns(0)
     assert da.diffattn_get_device_status() == 0  # the read cleared it
-    compare(run_gpu(inp), oracle_out(inp), "bf16")
+    compare(run_gpu(inp, packed=packed), oracle_out(inp), "bf16")

@@ -115,6 +115,23 @@ def test_bf16_large_scores():
     compare(run_gpu(inp), oracle_out(inp), "bf16")
 
 
+# -------------------------------------- persistent kernel (unpacked) ---
+
+@pytest.mark.parametrize("B,T,H,Hkv,causal", [(3, 1000, 16, 4, True), (5, 700, 12, 3, True),
+                                              (4, 2048, 16, 4, False), (12, 256, 16, 16, True)])
+def test_bf16_persistent_kernel(B, T, H, Hkv, causal):
+    """Unpacked batches with 2 to 10 (query tile, head, sequence) items per SM run
+    on the persistent kernel: ragged last tiles, grouped kv heads, non-causal,
+    many short items."""
+    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, random_subln=True)
+    inp = W.generate(wl, seed=B * 100 + T, seq_lens=[T] * B)
+    sh = lambda x: x.cuda().view(B, T, *x.shape[1:])  # noqa: E731
+    lam = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert da.diffattn_fwd_kernel(sh(inp.q), sh(inp.k), sh(inp.v), lam,
+                                  inp.subln_w.cuda()) == "diffattn_fwd_bf16_persistent_kernel"
+    compare(run_gpu(inp, packed=False), oracle_out(inp), "bf16")
+
+
 @pytest.mark.parametrize("d,lens", [(16, [64, 3]), (32, [100]), (64, [70, 1])])
 def test_f32_shapes(d, lens):
     wl = W.with_overrides(W.WORKLOADS["tiny_f32"], d=d, dv=2 * d, num_heads=4, num_kv_heads=2,
