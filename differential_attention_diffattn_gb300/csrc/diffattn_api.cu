@@ -83,17 +83,17 @@ int sm_count() {
     return counts[dev];
 }
 
-// Which bf16 forward kernel runs. Unpacked inputs with 2 to 10 (query tile,
-// head, sequence) items per SM go to the persistent kernel: it hides the
-// per-CTA setup and the gap between CTAs (measured x1.07 at B = 4, T = 2048,
-// 6.7 items per SM; even at T = 16384, 13.5 per SM). Packed sequences stay on
-// the one-item-per-CTA kernel (their empty items unbalance the persistent
-// kernel's static schedule: x0.98), and so do grids of about one item per SM.
+// Which bf16 forward kernel runs. Items of at most 32 key tiles (sequences of
+// at most 4096 tokens), at least two (query tile, head, sequence) items per SM
+// and at most 64 packed sequences go to the persistent kernel: it hides the
+// per-CTA setup and the gap between CTAs, a large share when items are short
+// (measured x1.07 at B = 4, T = 2048; x1.08 on 32768 tokens packed in 14
+// sequences of 128..4096). Longer sequences stay on the one-item-per-CTA kernel
+// (at T = 16384 the two tie), and so do grids of about one item per SM.
 bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
-    if (packed) return false;
-    const long long items = (long long)((max_seqlen + 127) / 128) * heads * num_seqs;
-    const long long sms = sm_count();
-    return items >= 2 * sms && items <= 10 * sms;
+    const long long n_qt = (max_seqlen + 127) / 128;
+    if (n_qt > 32 || (packed && num_seqs > 64)) return false;
+    return n_qt * heads * num_seqs >= 2LL * sm_count();
 }
 
 // Key-split plan of a cache forward: (number of splits, keys per split), with

@@ -1,11 +1,14 @@
 // Persistent form of the fused differential-attention forward for sm_103a
-// (bf16 in, fp32 accumulate, bf16 out), d = 64, dv = 128, used for unpacked
-// inputs with a few (query tile, sequence, head) items per SM: one CTA per SM
-// walks the items in a static snake order over items sorted longest first (every
-// CTA gets about the same number of key tiles), and the next item's Q and K / V
-// loads and its first scores run while the softmax warpgroups finish the current
-// item's epilogue. That hides the per-CTA setup and the gap between CTAs, which
-// weigh most when each item has few key tiles.
+// (bf16 in, fp32 accumulate, bf16 out), d = 64, dv = 128, used when the (query
+// tile, sequence, head) items have few key tiles each: one CTA per SM walks the
+// non-empty items in a static snake order over the items sorted longest first
+// (every CTA gets about the same number of key tiles), and the next item's Q and
+// K / V loads and its first scores run while the softmax warpgroups finish the
+// current item's epilogue. That hides the per-CTA setup and the gap between
+// CTAs, which weigh most when each item has few key tiles. The producer warp
+// enumerates the items (for packed sequences from their tile counts, staged in
+// shared memory; at most MAX_PACKED_SEQS sequences) and hands each to the other
+// roles through a two-slot ring.
 //
 // Per item the arithmetic is that of the one-item-per-CTA kernel (fwd_sm103a.cu):
 // S_c = Q_c K_c^T, two online softmaxes, O_c += P_c V on the tensor cores, then
@@ -14,7 +17,8 @@
 //
 // Roles (320 threads): warps 0-3 / 4-7 softmax of component 1 / 2 and the
 // epilogue; warp 8 TMA producer; warp 9 TMEM allocator and MMA issuer.
-// Barriers that advance once per item: q_full / q_empty (the Q box), o_full /
+// Barriers that advance once per item: item_full / item_empty (the ring of
+// items), q_full / q_empty (the Q box), o_full /
 // o_empty (the O accumulators: an item's first P V waits until the epilogue of
 // the previous one has read them); once per key tile over all items: the K / V
 // ring, s_full, p_ready. The epilogue reads O twice (the sum of squares, then
@@ -46,8 +50,17 @@ constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ uint32_t col_s(int c) { return (uint32_t)c * 128u; }
 __device__ __forceinline__ uint32_t col_o(int c) { return 256u + (uint32_t)c * 128u; }
 constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr int MAX_PACKED_SEQS = 64;
+
+// One work item: 128 query rows of one diff head of one sequence (n_kv < 0: no
+// more items).
+struct Item {
+    int h, qt, start, len, n_kv;
+    int pad[3];
+};
 
 struct Misc {
+    uint64_t item_full[2], item_empty[2];
     uint64_t q_full, q_empty;
     uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
     uint64_t s_full[2], p_ready[2];
@@ -56,6 +69,8 @@ struct Misc {
     int abort_flag;
     float xch[4 * BM];  // 1/l_c and the partial sums of squares, between the two warpgroups
     float w[DV];
+    Item work[2];                       // the item ring
+    uint16_t tiles[MAX_PACKED_SEQS];    // 128-row tiles of each packed sequence (0: none or bad bounds)
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
 
@@ -73,47 +88,9 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t n, bool 
     return r != 0;
 }
 
-// One work item: 128 query rows of one diff head of one sequence.
-struct Item {
-    int h, qt, start, len, n_kv;
-};
-// Item `idx` in longest-first order (query tile descending, then sequence, then
-// head); false when it is empty (past its sequence) or its sequence bounds are bad.
-__device__ __forceinline__ bool item_at(const FwdParams& p, int n_qt, int idx, Item& it) {
-    const int per_qt = p.H * p.num_seqs;
-    const int qt = n_qt - 1 - idx / per_qt;
-    const int rem = idx % per_qt;
-    const int seq = rem / p.H;
-    it.h = rem % p.H;
-    it.qt = qt;
-    if (p.cu_seqlens != nullptr) {
-        const int s0 = p.cu_seqlens[seq], s1 = p.cu_seqlens[seq + 1];
-        const bool bad = s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen ||
-                         (seq == 0 && s0 != 0) || (seq == p.num_seqs - 1 && s1 != p.total_tokens);
-        if (bad) {
-            if (threadIdx.x == 0) atomicOr(p.error_word, kErrBadSeqlens);
-            return false;
-        }
-        it.start = s0;
-        it.len = s1 - s0;
-    } else {
-        it.start = seq * p.seqlen;
-        it.len = p.seqlen;
-    }
-    if (qt * BM >= it.len) return false;
-    it.n_kv = p.causal ? qt + 1 : (it.len + BN - 1) / BN;
-    return true;
-}
-// The r-th item slot of this CTA in the snake order (-1 past the end of round r).
-__device__ __forceinline__ int snake(int r, int n_items) {
-    const int G = (int)gridDim.x, c = (int)blockIdx.x;
-    const int idx = r * G + ((r & 1) ? G - 1 - c : c);
-    return idx < n_items ? idx : -1;
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_qt, int n_items) {
+                                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_qt) {
     extern __shared__ uint8_t smem[];
     if ((smem_u32(smem) & 1023u) != 0) {
         if (threadIdx.x == 0) atomicOr(p.error_word, kErrLayout);
@@ -124,7 +101,8 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rounds = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto bar_item_full = [&](int i) { return smem_u32(&ms.item_full[i]); };
+    auto bar_item_empty = [&](int i) { return smem_u32(&ms.item_empty[i]); };
 
     const uint32_t bar_q_full = smem_u32(&ms.q_full), bar_q_empty = smem_u32(&ms.q_empty);
     auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
@@ -141,6 +119,10 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_item_full(i), 1);
+            mbar_init(bar_item_empty(i), 9);  // the MMA warp and the eight softmax warps
+        }
         mbar_init(bar_q_full, 1);
         mbar_init(bar_q_empty, 1);
         for (int s = 0; s < STAGES; ++s) {
@@ -157,8 +139,19 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         ms.abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == PRODUCER_WARP)
+    if (warp == PRODUCER_WARP) {
         for (int i = lane; i < DV; i += 32) ms.w[i] = p.subln_w[i];
+        // packed sequences: tile counts, and the bounds checked once
+        if (p.cu_seqlens != nullptr) {
+            for (int sq_i = lane; sq_i < p.num_seqs; sq_i += 32) {
+                const int s0 = p.cu_seqlens[sq_i], s1 = p.cu_seqlens[sq_i + 1];
+                const bool bad = s0 < 0 || s1 < s0 || s1 > p.total_tokens || s1 - s0 > p.max_seqlen ||
+                                 (sq_i == 0 && s0 != 0) || (sq_i == p.num_seqs - 1 && s1 != p.total_tokens);
+                if (bad && blockIdx.x == 0) atomicOr(p.error_word, kErrBadSeqlens);
+                ms.tiles[sq_i] = (uint16_t)(bad ? 0 : (s1 - s0 + BM - 1) / BM);
+            }
+        }
+    }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -168,24 +161,67 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
 
     if (warp == PRODUCER_WARP) {
         // ================================================= TMA producer ===
-        if (lane == 0 && p.inject != 1) {
+        // Item k of the longest-first order (query tile descending, then sequence,
+        // then head, empty (tile, sequence) pairs left out): rank q = n_qt - 1 - qt
+        // holds the sequences with at least n_qt - q tiles; a cursor walks the ranks
+        // as k grows. This CTA takes k = r G + c on even rounds r, r G + G - 1 - c
+        // on odd ones.
+        if (lane == 0) {
             const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
-            int tile = 0, items = 0;  // key tiles and items of this CTA so far
+            const bool packed = p.cu_seqlens != nullptr;
+            auto tiles_of = [&](int sq_i) { return packed ? (int)ms.tiles[sq_i] : n_qt; };
+            auto count_rank = [&](int q) {  // sequences with at least n_qt - q tiles
+                if (!packed) return p.num_seqs;
+                int n = 0;
+                for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) n += tiles_of(sq_i) >= n_qt - q;
+                return n;
+            };
+            long long total = 0;
+            for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) total += tiles_of(sq_i);
+            const long long n_valid = total * p.H;
+            const long long G = gridDim.x;
+            int q = 0, cq = count_rank(0);
+            long long P = 0;
+            int tile = 0, items = 0;
             bool ok = true;
-            for (int r = 0; ok && r < rounds; ++r) {
-                Item it;
-                const int idx = snake(r, n_items);
-                if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
-                const int g = it.h / (p.H / p.Hkv);
+            for (long long r = 0; ok && r * G < n_valid; ++r) {
+                const long long k = r * G + ((r & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+                if (k >= n_valid) continue;
+                while (k >= P + (long long)cq * p.H) {
+                    P += (long long)cq * p.H;
+                    cq = count_rank(++q);
+                }
+                const int j = (int)((k - P) / p.H), h = (int)((k - P) % p.H);
+                int sq_i = j;
+                if (packed) {
+                    int cnt = -1;
+                    for (sq_i = 0; sq_i < p.num_seqs; ++sq_i)
+                        if (tiles_of(sq_i) >= n_qt - q && ++cnt == j) break;
+                }
+                Item it{};
+                it.h = h;
+                it.qt = n_qt - 1 - q;
+                it.start = packed ? p.cu_seqlens[sq_i] : sq_i * p.seqlen;
+                it.len = packed ? p.cu_seqlens[sq_i + 1] - it.start : p.seqlen;
+                it.n_kv = p.causal ? it.qt + 1 : (it.len + BN - 1) / BN;
+                const int slot = items & 1;
+                if (!(ok = mbar_wait(bar_item_empty(slot), ((uint32_t)(items >> 1) & 1u) ^ 1u, ab))) break;
+                ms.work[slot] = it;
+                mbar_arrive(bar_item_full(slot));
+                if (p.inject == 1) {  // test hook: no loads, so the other roles' waits run out
+                    ++items;
+                    continue;
+                }
+                const int g = h / (p.H / p.Hkv);
                 if (!(ok = mbar_wait(bar_q_empty, ((uint32_t)items & 1u) ^ 1u, ab))) break;
                 const int row_q = it.start + it.qt * BM;
                 mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
-                tma_load_2d(sq, &tm_q, bar_q_full, it.h * 2 * HD, row_q, pol_q);
-                tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, it.h * 2 * HD + HD, row_q, pol_q);
-                for (int j = 0; j < it.n_kv; ++j, ++tile) {
+                tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
+                tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
+                for (int jj = 0; jj < it.n_kv; ++jj, ++tile) {
                     const int s = tile % STAGES;
                     if (!(ok = mbar_wait(bar_kv_empty(s), ((uint32_t)(tile / STAGES) & 1u) ^ 1u, ab))) break;
-                    const int row = it.start + j * BN;
+                    const int row = it.start + jj * BN;
                     mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
                     tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
                     tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
@@ -195,12 +231,21 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 }
                 ++items;
             }
+            // end of the items: a sentinel in the next slot
+            const int slot = items & 1;
+            if (ok && mbar_wait(bar_item_empty(slot), ((uint32_t)(items >> 1) & 1u) ^ 1u, ab)) {
+                Item end{};
+                end.n_kv = -1;
+                ms.work[slot] = end;
+                mbar_arrive(bar_item_full(slot));
+            }
             // Let every copy this CTA started land before shared memory goes away.
-            if (items > 0) mbar_wait_drain(bar_q_full, (uint32_t)(items - 1) & 1u, p.timeout_ns);
-            for (int j = tile > STAGES ? tile - STAGES : 0; j < tile; ++j) {
-                const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
-                mbar_wait_drain(bar_k_full(j % STAGES), ph, p.timeout_ns);
-                mbar_wait_drain(bar_v_full(j % STAGES), ph, p.timeout_ns);
+            const int loaded = p.inject == 1 ? 0 : items;
+            if (loaded > 0) mbar_wait_drain(bar_q_full, (uint32_t)(loaded - 1) & 1u, p.timeout_ns);
+            for (int jj = tile > STAGES ? tile - STAGES : 0; jj < tile; ++jj) {
+                const uint32_t ph = (uint32_t)(jj / STAGES) & 1u;
+                mbar_wait_drain(bar_k_full(jj % STAGES), ph, p.timeout_ns);
+                mbar_wait_drain(bar_v_full(jj % STAGES), ph, p.timeout_ns);
             }
         }
         __syncwarp();
@@ -227,10 +272,13 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         };
         int tile = 0, items = 0;
         bool ok = true;
-        for (int r = 0; ok && r < rounds; ++r) {
-            Item it;
-            const int idx = snake(r, n_items);
-            if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
+        for (;;) {
+            const int slot = items & 1;
+            if (!(ok = warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(items >> 1) & 1u, ab)))) break;
+            const Item it = ms.work[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_item_empty(slot));
+            if (it.n_kv < 0) break;
             // S of the item's first tile: the S columns are free (the previous item's last
             // P V was issued before, and the tensor pipe completes in issue order)
             if (!(ok = warp_all(mbar_wait(bar_q_full, (uint32_t)items & 1u, ab)))) break;
@@ -277,10 +325,16 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         const uint64_t sl2p = f2_pack(sl2, sl2);
         int tile = 0, items = 0;
         bool ok = true;
-        for (int rd = 0; rd < rounds; ++rd) {
-            Item it;
-            const int idx = snake(rd, n_items);
-            if (idx < 0 || !item_at(p, n_qt, idx, it)) continue;
+        for (;;) {
+            const int slot = items & 1;
+            ok = warp_all(ok && mbar_wait(bar_item_full(slot), (uint32_t)(items >> 1) & 1u, ab));
+            // the eight warps go on or stop together (each later passes the epilogue barriers)
+            ok = named_barrier_and(2, 256, ok);
+            if (!ok) break;
+            const Item it = ms.work[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_item_empty(slot));
+            if (it.n_kv < 0) break;
             const int qi = it.qt * BM + r;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; ok && j < it.n_kv; ++j, ++tile) {
@@ -337,7 +391,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                     tmem_st16(t_s + ch * 16, pk);
                 }
                 const float2 sab = f2_unpack(fadd2(sa, sb));
-                l = l * alpha + (sab.x + sab.y);
+                l = __fmaf_rn(l, alpha, __fadd_rn(sab.x, sab.y));
                 // O_c holds this item's sum through tile j-1 (S_c(j) was issued after PV_c(j-1))
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -380,7 +434,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float d = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                        const float d = diff_combine(__uint_as_float(o1[i]), il1, __uint_as_float(o2[i]), il2, lam);
                         ssp = fmaf(d, d, ssp);
                     }
                     if (store && p.o1 != nullptr) {
@@ -415,8 +469,8 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int e = ch * 32 + 2 * i;
-                        const float d0 = __uint_as_float(o1[2 * i]) * il1 - lam * (__uint_as_float(o2[2 * i]) * il2);
-                        const float d1 = __uint_as_float(o1[2 * i + 1]) * il1 - lam * (__uint_as_float(o2[2 * i + 1]) * il2);
+                        const float d0 = diff_combine(__uint_as_float(o1[2 * i]), il1, __uint_as_float(o2[2 * i]), il2, lam);
+                        const float d1 = diff_combine(__uint_as_float(o1[2 * i + 1]), il1, __uint_as_float(o2[2 * i + 1]), il2, lam);
                         pk[i] = pack_bf16x2(d0 * post * wv[e], d1 * post * wv[e + 1]);
                     }
                     if (store) {
@@ -460,7 +514,8 @@ cudaError_t launch_fwd_bf16_persistent(const FwdParams& p, const FwdTensorMaps& 
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
     const int n_qt = (p.max_seqlen + BM - 1) / BM;
-    const long long n_items = (long long)n_qt * p.H * p.num_seqs;
+    if (p.cu_seqlens != nullptr && p.num_seqs > MAX_PACKED_SEQS) return cudaErrorInvalidValue;
+    const long long n_items = (long long)n_qt * p.H * p.num_seqs;  // upper bound (packed: some are empty)
     if (n_items <= 0 || n_items > INT32_MAX) return cudaErrorInvalidValue;
     const int grid = (int)(n_items < sms ? n_items : sms);
     cudaLaunchConfig_t cfg = {};
@@ -473,8 +528,7 @@ cudaError_t launch_fwd_bf16_persistent(const FwdParams& p, const FwdTensorMaps& 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_persistent_kernel, maps.q, maps.k, maps.v, p, n_qt,
-                              (int)n_items);
+    return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_persistent_kernel, maps.q, maps.k, maps.v, p, n_qt);
 }
 
 }  // namespace diffattn

@@ -332,7 +332,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 tmem_st16(t_s + ch * 16, pk);
             }
             const float2 sab = f2_unpack(fadd2(sa, sb));
-            l = l * alpha + (sab.x + sab.y);
+            l = __fmaf_rn(l, alpha, __fadd_rn(sab.x, sab.y));
             // O_c holds the sum through tile j-1 here: S_c(j) was issued after PV_c(j-1).
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -379,7 +379,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    D[ch * 32 + i] = __uint_as_float(o1[i]) * il1 - lam * (__uint_as_float(o2[i]) * il2);
+                    D[ch * 32 + i] = diff_combine(__uint_as_float(o1[i]), il1, __uint_as_float(o2[i]), il2, lam);
                     ssp = fmaf(D[ch * 32 + i], D[ch * 32 + i], ssp);
                 }
                 // Training outputs: the normalised attention output of each component,

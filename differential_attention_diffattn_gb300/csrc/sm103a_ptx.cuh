@@ -340,6 +340,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
            ((M >> 4) << 24);
 }
 
+// D = O1 / l1 - lambda O2 / l2 for one value, every rounding spelled out (no
+// compiler contraction), so that the forward kernels give the same bits for
+// the same row whichever of them computes it.
+__device__ __forceinline__ float diff_combine(float o1, float il1, float o2, float il2, float lam) {
+    return __fmaf_rn(-lam, __fmul_rn(o2, il2), __fmul_rn(o1, il1));
+}
+
 // ------------------------------------------------------------ conversions ---
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
