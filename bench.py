@@ -393,6 +393,14 @@ def run_ours(args, rank, world, local_rank):
                    "inputs": "seeded N(0,1) q/k/v rounded to bf16, lambda vectors N(0,0.1^2) fp32, subln w = 1"},
         "per_step_ms": {"median": round(statistics.median(step_times), 5), "min": round(min(step_times), 5),
                         "covers": "lambda + forward launches of one step, CUDA events"},
+        # the same rate under the other counts of the pages' workloads, for information:
+        # T^2 / 2 pairs per head instead of T (T + 1) / 2, and the 512 flop per pair of
+        # the probability-map form (which one pass cannot run: it needs the row
+        # statistics before P V)
+        "other_flop_counts": {
+            "tflops_t2_over_2_pairs": round(value * sum(L * L / 2 for L in inp.seq_lens) /
+                                            sum(L * (L + 1) / 2 for L in inp.seq_lens), 2),
+            "tflops_512_per_pair": round(value * 512 / FLOP_PER_PAIR, 2)} if not args.out_proj else None,
         "tokens_per_s": round(tokens * world * args.steps / (elapsed_ms * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -867,7 +875,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--seed", type=int, default=0)

@@ -98,7 +98,7 @@ bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
 
 // Key-split plan of a cache forward: (number of splits, keys per split), with
 // splits of at least 256 keys (64-key multiples). Without a requested count it
-// takes the fewest waves of resident split CTAs on the 152 SMs (1 to 4) whose
+// takes the fewest waves of resident split CTAs on the device's SMs (1 to 4) whose
 // last wave is at least 80 % full, else the fullest: every wave repeats the
 // per-CTA setup and pipeline ramp, which measured costlier than a few idle
 // slots (decode_b8_c16384: 9 splits in one wave 5221 GB/s, 19 in two 5009).
@@ -118,7 +118,7 @@ bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
     if (n == 0) {
         const long long ctas = (long long)d.batch * d.num_kv_heads;
         const int rows = d.q_len * (d.num_heads / d.num_kv_heads);
-        const long long slots = 152LL * (decode_rows_supported(rows) ? decode_ctas_per_sm() : 1);
+        const long long slots = (long long)sm_count() * (decode_rows_supported(rows) ? decode_ctas_per_sm() : 1);
         const long long max_n = (cap + 255) / 256;
         double best = -1.0;
         n = 1;
