@@ -62,6 +62,16 @@ def test_workload_sampled(name):
             inp.wl.dtype)
 
 
+def test_bf16_long_sequence_65536():
+    """The longest case: one 65536-token sequence (16 heads over 4 kv heads, 512
+    query tiles, 268 MB per q / out tensor), compared on sampled rows."""
+    inp = W.generate(W.with_overrides(W.WORKLOADS["b2_t512_gqa"], random_subln=True), seed=65, seq_lens=[65536])
+    got = run_gpu(inp, packed=False)
+    assert torch.isfinite(got).all()
+    tt, hh = sample_rows(inp, every=997, edge=64)
+    compare(got[torch.as_tensor(tt).long(), torch.as_tensor(hh).long()], oracle_out(inp, rows=(tt, hh)), "bf16")
+
+
 # ---------------------------------------------------------- edge cases ---
 
 BF = W.WORKLOADS["b2_t512_gqa"]
