@@ -404,7 +404,9 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x, seq = blockIdx.z;
-    const int kt = gridDim.y - 1 - blockIdx.y;
+    // causal: key tile kt is seen by the query blocks from kt on, so the first tiles
+    // carry the most work and are scheduled first
+    const int kt = blockIdx.y;
     int start = 0, len = 0;
     if (!seq_bounds(p, seq, &start, &len)) return;
     if (kt * BK >= len) return;
