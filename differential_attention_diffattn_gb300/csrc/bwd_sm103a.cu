@@ -133,8 +133,11 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.x, seq = blockIdx.z;
-    const int qt = gridDim.y - 1 - blockIdx.y;
+    // grid (head, query tile, sequence), or with the tiles outermost (head, sequence,
+    // query tile); either way the longest query tiles of a sequence are scheduled first
+    const bool outer = p.dq_tiles_outer != 0;
+    const int h = blockIdx.x, seq = outer ? blockIdx.y : blockIdx.z;
+    const int qt = outer ? gridDim.z - 1 - blockIdx.z : gridDim.y - 1 - blockIdx.y;
     int start = 0, len = 0;
     if (!seq_bounds(p, seq, &start, &len)) return;
     if (qt * BM >= len) return;
@@ -403,10 +406,12 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.x, seq = blockIdx.z;
-    // causal: key tile kt is seen by the query blocks from kt on, so the first tiles
-    // carry the most work and are scheduled first
-    const int kt = blockIdx.y;
+    // grid (kv head, key tile, sequence), or with the tiles outermost (kv head,
+    // sequence, key tile). Causal: key tile kt is seen by the query blocks from kt on,
+    // so the first tiles carry the most work and are scheduled first
+    const bool outer = p.dkv_tiles_outer != 0;
+    const int g = blockIdx.x, seq = outer ? blockIdx.y : blockIdx.z;
+    const int kt = outer ? blockIdx.z : blockIdx.y;
     int start = 0, len = 0;
     if (!seq_bounds(p, seq, &start, &len)) return;
     if (kt * BK >= len) return;
@@ -670,11 +675,15 @@ cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& m, cudaSt
     err = set_smem(diffattn_bwd_dkv_kernel, dkv::SMEM, dkv_done);
     if (err != cudaSuccess) return err;
     const int n_qt = (p.max_seqlen + dq::BM - 1) / dq::BM;
-    diffattn_bwd_dq_kernel<<<dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs), NT, dq::SMEM, stream>>>(
+    const dim3 dq_grid = p.dq_tiles_outer ? dim3((unsigned)p.H, (unsigned)p.num_seqs, (unsigned)n_qt)
+                                          : dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
+    diffattn_bwd_dq_kernel<<<dq_grid, NT, dq::SMEM, stream>>>(
         m.q128, m.k128, m.v128, m.dd128, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const int n_kt = (p.max_seqlen + dkv::BK - 1) / dkv::BK;
-    diffattn_bwd_dkv_kernel<<<dim3((unsigned)p.Hkv, (unsigned)n_kt, (unsigned)p.num_seqs), NT, dkv::SMEM, stream>>>(
+    const dim3 dkv_grid = p.dkv_tiles_outer ? dim3((unsigned)p.Hkv, (unsigned)p.num_seqs, (unsigned)n_kt)
+                                            : dim3((unsigned)p.Hkv, (unsigned)n_kt, (unsigned)p.num_seqs);
+    diffattn_bwd_dkv_kernel<<<dkv_grid, NT, dkv::SMEM, stream>>>(
         m.q64, m.k128, m.v128, m.dd64, p);
     return cudaGetLastError();
 }

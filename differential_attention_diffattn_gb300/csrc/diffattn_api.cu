@@ -96,6 +96,26 @@ bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
     return n_qt * heads * num_seqs >= 2LL * sm_count();
 }
 
+// Launch order of a causal backward kernel, whose CTA for tile t of a sequence of n
+// 128-row tiles visits t + 1 (dQ) or n - t (dK/dV) tiles. Sequence-major order keeps
+// the CTAs in flight on one or two sequences, so the operands they stream are shared
+// in L2; but the last sequence's longest CTA is then handed out only after the rest of
+// the grid and can end well after the average SM. Estimate that end (one CTA per SM,
+// each costing the tiles it visits plus half a tile of setup, the sequences taken as
+// max_seqlen long) and go tiles-outermost, the longest tiles of every sequence first,
+// when it is more than 10 % past the average. Measured on 16 / 4 heads, T = 2048:
+// backward x1.18 at B = 4 (dK/dV grid of 256 CTAs); at B = 8, T = 4096 with 16 kv heads
+// the tiles-outermost order was 6 % slower (no tail, less L2 reuse) and is not chosen.
+bool bwd_tiles_outermost(int num_seqs, int heads, int max_seqlen) {
+    if (num_seqs < 2) return false;
+    const double n = (double)((max_seqlen + 127) / 128);
+    const double per_seq = heads * (n * (n + 1) / 2 + 0.5 * n);
+    const double slots = (double)sm_count();
+    const double avg_end = per_seq * num_seqs / slots;
+    const double last_end = per_seq * (num_seqs - 1) / slots + n + 0.5;
+    return last_end > 1.1 * avg_end;
+}
+
 // Key-split plan of a cache forward: (number of splits, keys per split), with
 // splits of at least 256 keys (64-key multiples). Without a requested count it
 // takes the fewest waves of resident split CTAs on the device's SMs (1 to 4) whose
@@ -508,6 +528,8 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     p.dv = dv;
     p.error_word = err_word;
     p.timeout_ns = g_timeout_ns;
+    p.dq_tiles_outer = causal && bwd_tiles_outermost(num_seqs, p.H, max_seqlen) ? 1 : 0;
+    p.dkv_tiles_outer = causal && bwd_tiles_outermost(num_seqs, p.Hkv, max_seqlen) ? 1 : 0;
     BwdTensorMaps m;
     const uint64_t qw = (uint64_t)ds.num_heads * 2 * ds.d, kw = (uint64_t)ds.num_kv_heads * 2 * ds.d;
     const uint64_t vw = (uint64_t)ds.num_kv_heads * ds.dv, dw = (uint64_t)ds.num_heads * ds.dv;

@@ -93,6 +93,8 @@ struct BwdParams {
     void* dv;                  // [tokens][Hkv][dv]
     unsigned int* error_word;
     unsigned long long timeout_ns;
+    int dq_tiles_outer;        // grid order of the dQ kernel: 1 (head, sequence, tile), 0 (head, tile, sequence)
+    int dkv_tiles_outer;       // the same for the dK/dV kernel (kv heads)
 };
 
 // TMA descriptors of the backward kernels: q and dD with 128- and 64-row boxes,

@@ -116,3 +116,30 @@ def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
     grad_close(dw, want["w"], "dw")
     for got, name in zip(dl, ("lq1", "lk1", "lq2", "lk2")):
         grad_close(got, want[name], name)
+
+
+# Full-size batches against the same sequences one call each: dQ, dK and dV of a
+# token depend only on its own sequence, so the bits must agree. The two shapes
+# take the two launch orders of the backward kernels: 2 x 8192 tokens with 16 kv
+# heads launches sequence-major (many waves, no tail); 4 x 2048 tokens with 4 kv
+# heads puts the key tiles outermost (a dK/dV grid of 256 CTAs); a single
+# sequence is the same grid either way.
+@pytest.mark.parametrize("lens,H,Hkv", [([8192] * 2, 16, 16), ([2048] * 4, 16, 4)])
+def test_backward_batch_equals_separate_calls_bitwise(lens, H, Hkv):
+    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, random_subln=True)
+    inp = W.generate(wl, seed=131, seq_lens=lens)
+    B, T = len(lens), lens[0]
+    dev = "cuda"
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(*(x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)), li)
+    q, k, v = (x.to(dev).view(B, T, *x.shape[1:]) for x in (inp.q, inp.k, inp.v))
+    w = inp.subln_w.to(dev)
+    out, lse, o1, o2 = da.diffattn_fwd_train(q, k, v, lam, li, w, causal=True, eps=wl.eps)
+    dy = (torch.randn(out.shape, generator=torch.Generator().manual_seed(132)) * 0.1).to(torch.bfloat16).to(dev)
+    batch = da.diffattn_bwd(q, k, v, lam, li, w, dy, lse, o1, o2, causal=True, eps=wl.eps)[:3]
+    for b in range(B):
+        one = da.diffattn_bwd(q[b:b + 1], k[b:b + 1], v[b:b + 1], lam, li, w, dy[b:b + 1], lse[b:b + 1],
+                              o1[b:b + 1], o2[b:b + 1], causal=True, eps=wl.eps)[:3]
+        for got, want, name in zip(batch, one, ("dq", "dk", "dv")):
+            assert torch.equal(got[b:b + 1], want), (name, b)
+    assert da.diffattn_get_device_status() == 0
