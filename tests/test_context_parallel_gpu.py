@@ -24,7 +24,7 @@ def _lib():
     torch.cuda.set_device(0)
 
 
-# more than four parts: the merge kernel takes them four at a time and rescales
+# more than two parts: the merge kernel takes them two at a time and rescales
 @pytest.mark.parametrize("bounds,per_head", [([0, 96], False), ([0, 30, 31, 96], True), ([0, 48, 96], False),
                                              ([0, 5, 9, 13, 17, 21, 96], True),
                                              ([0, 10, 20, 30, 40, 50, 60, 70, 96], False)])
@@ -50,6 +50,34 @@ def test_merge_kernel_matches_oracle(bounds, per_head):
         ((want / (inp.subln_w.double().numpy() * (1 - li))) ** 2).mean(-1) + 1e-30)
     err = np.abs(got.double().cpu().numpy() - want).max(-1)
     assert (err <= 2e-5 * np.maximum(1.0, kappa) * np.abs(want).max()).all(), float(err.max())
+
+
+# every kernel shape (rows of up to 64, 128, 256 and 512 values; row counts that
+# leave the last block part-filled; one to seven parts) on random partials. Parts
+# a row does not see (lse = -inf) carry NaN outputs, which must be dropped; every
+# row sees at least one part per component.
+@pytest.mark.parametrize("n,T,H,dv", [(1, 37, 3, 36), (2, 37, 3, 64), (3, 29, 5, 128), (5, 23, 3, 200),
+                                      (2, 19, 3, 512), (7, 11, 2, 256)])
+def test_merge_kernel_shapes(n, T, H, dv):
+    rng = np.random.default_rng(1000 + 10 * dv + n)
+    f32 = lambda a: np.asarray(a, dtype=np.float32).astype(np.float64)  # noqa: E731
+    lse = f32(rng.normal(0.0, 3.0, (n, T, H, 2)))
+    hide = rng.random((n, T, H, 2)) < 0.3
+    keep = rng.integers(0, n, (T, H, 2))
+    hide[keep, np.arange(T)[:, None, None], np.arange(H)[None, :, None], np.arange(2)[None, None, :]] = False
+    lse[hide] = -np.inf
+    o1, o2 = f32(rng.normal(size=(n, T, H, dv))), f32(rng.normal(size=(n, T, H, dv)))
+    lam, w, li, eps = f32(rng.normal(0.0, 0.3, H)), f32(rng.normal(size=dv)), 0.35, 1e-5
+    want = op.merge(lse, np.where(hide[..., :1], 0.0, o1), np.where(hide[..., 1:], 0.0, o2), lam, li, w, eps)
+    dev = lambda a: torch.tensor(a, dtype=torch.float32).cuda()  # noqa: E731
+    got = da.diffattn_merge_partials(dev(lse), dev(np.where(hide[..., :1], np.nan, o1)),
+                                     dev(np.where(hide[..., 1:], np.nan, o2)), dev(lam), li, dev(w), eps=eps,
+                                     out_dtype=torch.float32)
+    assert da.diffattn_get_device_status() == 0
+    got = got.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - want).max(-1)
+    assert (err <= 1e-4 * np.abs(want).max(-1)).all(), float(err.max())
 
 
 @pytest.mark.parametrize("world,chunk,H,Hkv", [(1, 256, 16, 4), (2, 256, 16, 4), (4, 128, 8, 8), (3, 200, 4, 1)])
