@@ -53,6 +53,13 @@ def peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
+def check_device(da, where):
+    """Raise if the library's device status word reports an error (it is read and cleared)."""
+    st = da.diffattn_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device reported {da.diffattn_status_string(st)} {where}")
+
+
 def dense_view(t, inp):
     """Token-major [tokens, ...] as [B, T, ...] for a dense batch of equal
     sequences (several sequences, no cu_seqlens); unchanged otherwise."""
@@ -131,6 +138,22 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+# dense bf16 tensor-core rate of one SM per clock (M128 N128 K16 in 64 cycles)
+BF16_FLOP_PER_CLK_SM = 8192
+
+
+def clock_peak_tflops(clocks):
+    """SMs x 8192 flop per clock x the largest SM clock nvidia-smi reported
+    during the timed region: the tensor pipe's ceiling at that clock (the
+    measured cuBLAS figure is the headline denominator; this one is for
+    information)."""
+    import torch
+    if not clocks or not clocks.get("sm_max_mhz"):
+        return None
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * BF16_FLOP_PER_CLK_SM * clocks["sm_max_mhz"] * 1e6 / 1e12
 
 
 # ------------------------------------------------------------ ours (GPU) ---
@@ -226,8 +249,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error during warm-up")
+    check_device(da, "during warm-up")
     warm = None
     if flush is not None:
         # Warm figure: consecutive steps replayed from CUDA graphs (lambda + forward
@@ -250,8 +272,7 @@ def run_ours(args, rank, world, local_rank):
             graphs[i % 2].replay()
         w1.record(stream)
         torch.cuda.synchronize()
-        if da.diffattn_get_device_status() != 0:
-            raise RuntimeError("device reported an error in the graph replays")
+        check_device(da, "in the graph replays")
         warm_ms = w0.elapsed_time(w1) / args.steps
         warm = {"ms_per_step": round(warm_ms, 5), "value": round(flops_step / (warm_ms * 1e-3) / 1e12, 2),
                 "l2": "warm: consecutive steps, no flush", "launch": "CUDA graph replay per step"}
@@ -288,8 +309,7 @@ def run_ours(args, rank, world, local_rank):
     rope_ms = sum(a.elapsed_time(b) for a, b in rope_ev) / args.steps if rope is not None else 0.0
     proj_ms = sum(a.elapsed_time(b) for a, b in proj_ev) / args.steps if args.out_proj else 0.0
     fwd_ms -= rope_ms + proj_ms  # the attention kernel alone
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the timed region")
+    check_device(da, "in the timed region")
     elapsed_ms = shard.max_over_ranks(elapsed_ms)
     ms_step = elapsed_ms / args.steps
     step_flops = flops_step + (2 * tokens * hidden * hidden if args.out_proj else 0)
@@ -363,8 +383,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = shard.max_over_ranks(e2e_ms)
     e2e_value = step_flops * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e12
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the end-to-end region")
+    check_device(da, "in the end-to-end region")
     if not torch.isfinite(out_hs[(args.e2e_steps - 1) % 2][:: max(1, tokens // 64)].float()).all():
         raise RuntimeError("non-finite output")
 
@@ -409,6 +428,8 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{pk_kind} bf16 dense burst",
                      "frac_of_sustained": round(achieved / float(pk["bf16_tflops_sustained"]), 4),
+                     "frac_of_clock_peak": (round(achieved / clock_peak_tflops(clocks), 4)
+                                            if clock_peak_tflops(clocks) else None),
                      "kernel": kernel_name, "launch_ms": round(fwd_ms, 4),
                      "algorithmic_flop_per_launch": flops_step},
         "clocks": clocks,
@@ -499,8 +520,7 @@ def run_ours_bwd(args, rank, world, local_rank):
         bwd(s)
         lam_bwd(s)
     torch.cuda.synchronize()
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error during warm-up")
+    check_device(da, "during warm-up")
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     ev = [(mk(), mk(), mk()) for _ in range(args.steps)]
     t0, t1 = mk(), mk()
@@ -523,8 +543,7 @@ def run_ours_bwd(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the timed region")
+    check_device(da, "in the timed region")
     elapsed_ms = shard.max_over_ranks(t0.elapsed_time(t1))
     fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
     bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
@@ -563,8 +582,7 @@ def run_ours_bwd(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = shard.max_over_ranks(e0.elapsed_time(e1))
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the end-to-end region")
+    check_device(da, "in the end-to-end region")
     if not all(torch.isfinite(t.float()).all() for t in hg):
         raise RuntimeError("non-finite gradient")
     if rank != 0:
@@ -587,6 +605,9 @@ def run_ours_bwd(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "achieved": round(bwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(bwd_achieved / peak, 4), "traffic": None,
                      "peak_kind": f"{pk_kind} bf16 dense burst",
+                     "frac_of_sustained": round(bwd_achieved / float(pk["bf16_tflops_sustained"]), 4),
+                     "frac_of_clock_peak": (round(bwd_achieved / clock_peak_tflops(clocks), 4)
+                                            if clock_peak_tflops(clocks) else None),
                      "kernel": "diffattn_bwd (preprocessing + dQ + dK/dV kernels)", "launch_ms": round(bwd_ms, 4),
                      "algorithmic_flop_per_launch": bwd_flop},
         "clocks": clocks, "gpu_launches": 6 * args.steps, "impl": "ours",
@@ -663,8 +684,7 @@ def run_ours_cp(args, rank, world, local_rank):
         outs = step()
     t1.record(stream)
     torch.cuda.synchronize()
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the timed region")
+    check_device(da, "in the timed region")
     elapsed = shard.max_over_ranks(t0.elapsed_time(t1))
     merge_ms = sum(a.elapsed_time(b) for a, b, _ in merge_ev) / args.steps
     merge_bytes = sum(n * chunk * wl.num_heads * (2 * wl.dv * 4 + 8) + chunk * wl.num_heads * wl.dv * 2
@@ -752,8 +772,7 @@ def run_ours_kv(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the timed region")
+    check_device(da, "in the timed region")
     elapsed_ms = shard.max_over_ranks(t0.elapsed_time(t1))
     for i in range(args.steps):
         da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
@@ -761,8 +780,7 @@ def run_ours_kv(args, rank, world, local_rank):
         fwd(sets[i % 2])
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    if da.diffattn_get_device_status() != 0:
-        raise RuntimeError("device reported an error in the per-call timing")
+    check_device(da, "in the per-call timing")
     fwd_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     value = bytes_step * world * args.steps / (elapsed_ms * 1e-3) / 1e9
     if rank != 0:

@@ -83,16 +83,18 @@ int sm_count() {
     return counts[dev];
 }
 
-// Which bf16 forward kernel runs. Items of at most 32 key tiles (sequences of
-// at most 4096 tokens), at least two (query tile, head, sequence) items per SM
+// Which bf16 forward kernel runs. Items of at most 64 key tiles (sequences of
+// at most 8192 tokens), at least two (query tile, head, sequence) items per SM
 // and at most 64 packed sequences go to the persistent kernel: it hides the
-// per-CTA setup and the gap between CTAs, a large share when items are short
-// (measured x1.07 at B = 4, T = 2048; x1.08 on 32768 tokens packed in 14
-// sequences of 128..4096). Longer sequences stay on the one-item-per-CTA kernel
-// (at T = 16384 the two tie), and so do grids of about one item per SM.
+// per-CTA setup, the epilogue and the gap between CTAs, a large share when items
+// are short (measured against the one-item-per-CTA kernel: x1.13 at B = 4,
+// T = 2048, 16 / 4 heads; x1.14 on 32768 tokens packed in 14 sequences of
+// 128..4096; x1.01-1.03 at T = 8192). Longer sequences stay on the
+// one-item-per-CTA kernel (T = 16384: a tie; T = 32768: x0.975 for the
+// persistent one), and so do grids of about one item per SM.
 bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
     const long long n_qt = (max_seqlen + 127) / 128;
-    if (n_qt > 32 || (packed && num_seqs > 64)) return false;
+    if (n_qt > 64 || (packed && num_seqs > 64)) return false;
     return n_qt * heads * num_seqs >= 2LL * sm_count();
 }
 

@@ -3,29 +3,36 @@
 // tile, sequence, head) items have few key tiles each: one CTA per SM walks the
 // non-empty items in a static snake order over the items sorted longest first
 // (every CTA gets about the same number of key tiles), and the next item's Q and
-// K / V loads and its first scores run while the softmax warpgroups finish the
-// current item's epilogue. That hides the per-CTA setup and the gap between
-// CTAs, which weigh most when each item has few key tiles. The producer warp
-// enumerates the items (for packed sequences from their tile counts, staged in
-// shared memory; at most MAX_PACKED_SEQS sequences) and hands each to the other
-// roles through a two-slot ring.
+// K / V loads, its first scores and its softmax run while the epilogue
+// warpgroup finishes the current item. That hides the per-CTA setup, the
+// epilogue and the gap between CTAs, which weigh most when each item has few
+// key tiles. The producer warp enumerates the items (for packed sequences from
+// their tile counts, staged in shared memory; at most MAX_PACKED_SEQS
+// sequences) and hands each to the other roles through a four-slot ring.
 //
 // Per item the arithmetic is that of the one-item-per-CTA kernel (fwd_sm103a.cu):
 // S_c = Q_c K_c^T, two online softmaxes, O_c += P_c V on the tensor cores, then
 // O1/l1 - lambda O2/l2, RMSNorm over dv, weight, (1 - lambda_init)
 // ("DiffTransformer.py", forward; "LlamaDiffSdpaAttention.py", forward).
 //
-// Roles (320 threads): warps 0-3 / 4-7 softmax of component 1 / 2 and the
-// epilogue; warp 8 TMA producer; warp 9 TMEM allocator and MMA issuer.
-// Barriers that advance once per item: item_full / item_empty (the ring of
-// items), q_full / q_empty (the Q box), o_full /
-// o_empty (the O accumulators: an item's first P V waits until the epilogue of
-// the previous one has read them); once per key tile over all items: the K / V
-// ring, s_full, p_ready. The epilogue reads O twice (the sum of squares, then
-// the normalised output) so that D is not held across the exchange between the
-// warpgroups: held, it pushed the kernel past the 168-register cap of ten warps.
-// Every wait is bounded; a warp whose wait ran out still passes the epilogue's
-// barriers, where the warpgroups decide together to stop.
+// Roles (512 threads, four warpgroups): warps 0-3 / 4-7 softmax of component
+// 1 / 2; warps 8-11 the epilogue (warp 8 + q reads TMEM lanes 32q..32q+31); warp
+// 12 TMA producer; warp 13 TMEM allocator and MMA issuer; warps 14-15 idle. With
+// the epilogue in its own warpgroup the softmax warps go on to the next item as
+// soon as their last P is stored, and the epilogue of one item runs under the
+// next item's key tiles; it still has to read O before the next item's first
+// P V overwrites it. Sixteen warps leave 128 registers a thread at launch; the
+// warpgroups then move registers with setmaxnreg: softmax 168, epilogue 88,
+// producer / MMA 88 (8 x 32 x 168 + 4 x 32 x (88 + 88) = the 65,536 the launch
+// holds; each SM sub-partition runs two softmax warps, one epilogue warp and one
+// of warps 12-15: 2 x 168 + 88 + 88 = 512 registers a lane, its whole share).
+// Barriers that advance once per item: item_full / item_empty (a four-slot ring
+// of items), q_full / q_empty (the Q box), stats_full (1/l_c per row from the
+// softmax warps), o_full / o_empty (the O accumulators: an item's first P V
+// waits until the epilogue of the previous one has read them); once per key
+// tile over all items: the K / V ring, s_full, p_ready. Every wait is bounded;
+// the eight softmax warps decide together, at each item's start and end,
+// whether to go on, so that none is left waiting at a barrier another has left.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -35,7 +42,13 @@ namespace diffattn {
 namespace {
 
 constexpr int BM = 128, BN = 128, HD = 64, DV = 128, STAGES = 3;
-constexpr int NUM_THREADS = 320, PRODUCER_WARP = 8, MMA_WARP = 9;
+constexpr int NUM_THREADS = 512, EPI_WARP0 = 8, PRODUCER_WARP = 12, MMA_WARP = 13;
+constexpr int NSLOT = 4;  // item ring
+// registers a thread: at launch (65,536 / 512) and after the split
+constexpr int REG_LAUNCH = 128, REG_SOFTMAX = 168, REG_EPI = 88, REG_COPY = 88;
+constexpr int REG_NEED = 8 * 32 * REG_SOFTMAX + 4 * 32 * REG_EPI + 4 * 32 * REG_COPY;
+static_assert(REG_NEED <= NUM_THREADS * REG_LAUNCH, "the register split exceeds the launch's registers");
+static_assert(2 * REG_SOFTMAX + REG_EPI + REG_COPY <= 4 * REG_LAUNCH, "the split exceeds one sub-partition's share");
 constexpr uint32_t BOX_BYTES = BM * HD * 2;
 constexpr uint32_t Q_BYTES = 2 * BOX_BYTES, K_BYTES = 2 * BOX_BYTES, V_BYTES = 2 * BOX_BYTES;
 constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;
@@ -60,16 +73,16 @@ struct Item {
 };
 
 struct Misc {
-    uint64_t item_full[2], item_empty[2];
+    uint64_t item_full[NSLOT], item_empty[NSLOT];
     uint64_t q_full, q_empty;
     uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
     uint64_t s_full[2], p_ready[2];
-    uint64_t o_full, o_empty;
+    uint64_t o_full, o_empty, stats_full;
     uint32_t tmem_base;
     int abort_flag;
-    float xch[4 * BM];  // 1/l_c and the partial sums of squares, between the two warpgroups
+    float il[2][2][BM];                 // 1/l_c per row, by item parity and component
     float w[DV];
-    Item work[2];                       // the item ring
+    Item work[NSLOT];                   // the item ring
     uint16_t tiles[MAX_PACKED_SEQS];    // 128-row tiles of each packed sequence (0: none or bad bounds)
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
@@ -111,6 +124,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
     auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full), bar_o_empty = smem_u32(&ms.o_empty);
+    const uint32_t bar_stats_full = smem_u32(&ms.stats_full);
     const uint32_t sq = sbase + OFF_Q;
     auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
     auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
@@ -119,9 +133,9 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NSLOT; ++i) {
             mbar_init(bar_item_full(i), 1);
-            mbar_init(bar_item_empty(i), 9);  // the MMA warp and the eight softmax warps
+            mbar_init(bar_item_empty(i), 13);  // the MMA warp, the eight softmax and four epilogue warps
         }
         mbar_init(bar_q_full, 1);
         mbar_init(bar_q_empty, 1);
@@ -135,7 +149,8 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
             mbar_init(bar_p_ready(c), 128);
         }
         mbar_init(bar_o_full, 1);
-        mbar_init(bar_o_empty, 256);
+        mbar_init(bar_o_empty, 128);     // every epilogue thread
+        mbar_init(bar_stats_full, 256);  // every softmax thread
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -159,163 +174,11 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
     const uint32_t tmem = ms.tmem_base;
     const AbortState ab{&ms.abort_flag, p.error_word, p.timeout_ns};
 
-    if (warp == PRODUCER_WARP) {
-        // ================================================= TMA producer ===
-        // Item k of the longest-first order (query tile descending, then sequence,
-        // then head, empty (tile, sequence) pairs left out): rank q = n_qt - 1 - qt
-        // holds the sequences with at least n_qt - q tiles; a cursor walks the ranks
-        // as k grows. This CTA takes k = r G + c on even rounds r, r G + G - 1 - c
-        // on odd ones.
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
-            const bool packed = p.cu_seqlens != nullptr;
-            auto tiles_of = [&](int sq_i) { return packed ? (int)ms.tiles[sq_i] : n_qt; };
-            auto count_rank = [&](int q) {  // sequences with at least n_qt - q tiles
-                if (!packed) return p.num_seqs;
-                int n = 0;
-                for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) n += tiles_of(sq_i) >= n_qt - q;
-                return n;
-            };
-            long long total = 0;
-            for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) total += tiles_of(sq_i);
-            const long long n_valid = total * p.H;
-            const long long G = gridDim.x;
-            int q = 0, cq = count_rank(0);
-            long long P = 0;
-            int tile = 0, items = 0;
-            bool ok = true;
-            for (long long r = 0; ok && r * G < n_valid; ++r) {
-                const long long k = r * G + ((r & 1) ? G - 1 - blockIdx.x : blockIdx.x);
-                if (k >= n_valid) continue;
-                while (k >= P + (long long)cq * p.H) {
-                    P += (long long)cq * p.H;
-                    cq = count_rank(++q);
-                }
-                const int j = (int)((k - P) / p.H), h = (int)((k - P) % p.H);
-                int sq_i = j;
-                if (packed) {
-                    int cnt = -1;
-                    for (sq_i = 0; sq_i < p.num_seqs; ++sq_i)
-                        if (tiles_of(sq_i) >= n_qt - q && ++cnt == j) break;
-                }
-                Item it{};
-                it.h = h;
-                it.qt = n_qt - 1 - q;
-                it.start = packed ? p.cu_seqlens[sq_i] : sq_i * p.seqlen;
-                it.len = packed ? p.cu_seqlens[sq_i + 1] - it.start : p.seqlen;
-                it.n_kv = p.causal ? it.qt + 1 : (it.len + BN - 1) / BN;
-                const int slot = items & 1;
-                if (!(ok = mbar_wait(bar_item_empty(slot), ((uint32_t)(items >> 1) & 1u) ^ 1u, ab))) break;
-                ms.work[slot] = it;
-                mbar_arrive(bar_item_full(slot));
-                if (p.inject == 1) {  // test hook: no loads, so the other roles' waits run out
-                    ++items;
-                    continue;
-                }
-                const int g = h / (p.H / p.Hkv);
-                if (!(ok = mbar_wait(bar_q_empty, ((uint32_t)items & 1u) ^ 1u, ab))) break;
-                const int row_q = it.start + it.qt * BM;
-                mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
-                tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
-                tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
-                for (int jj = 0; jj < it.n_kv; ++jj, ++tile) {
-                    const int s = tile % STAGES;
-                    if (!(ok = mbar_wait(bar_kv_empty(s), ((uint32_t)(tile / STAGES) & 1u) ^ 1u, ab))) break;
-                    const int row = it.start + jj * BN;
-                    mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
-                    tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
-                    tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
-                    mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
-                    tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
-                    tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
-                }
-                ++items;
-            }
-            // end of the items: a sentinel in the next slot
-            const int slot = items & 1;
-            if (ok && mbar_wait(bar_item_empty(slot), ((uint32_t)(items >> 1) & 1u) ^ 1u, ab)) {
-                Item end{};
-                end.n_kv = -1;
-                ms.work[slot] = end;
-                mbar_arrive(bar_item_full(slot));
-            }
-            // Let every copy this CTA started land before shared memory goes away.
-            const int loaded = p.inject == 1 ? 0 : items;
-            if (loaded > 0) mbar_wait_drain(bar_q_full, (uint32_t)(loaded - 1) & 1u, p.timeout_ns);
-            for (int jj = tile > STAGES ? tile - STAGES : 0; jj < tile; ++jj) {
-                const uint32_t ph = (uint32_t)(jj / STAGES) & 1u;
-                mbar_wait_drain(bar_k_full(jj % STAGES), ph, p.timeout_ns);
-                mbar_wait_drain(bar_v_full(jj % STAGES), ph, p.timeout_ns);
-            }
-        }
-        __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ==================================================== MMA issuer ===
-        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
-        constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, STG = STAGE_BYTES >> 4, BOX = BOX_BYTES >> 4;
-        const uint64_t qdesc = desc_kmajor(sq), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
-        auto issue_s = [&](int c, int tile) {
-            const uint64_t a0 = qdesc + (uint64_t)c * BOX;
-            const uint64_t b0 = kdesc + (uint64_t)(tile % STAGES) * STG + (uint64_t)c * BOX;
-            const uint32_t d = tmem + col_s(c);
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a0 + kk * KSTEP, b0 + kk * KSTEP, idesc_s, kk > 0 ? 1u : 0u);
-            mma_commit_elect(bar_s_full(c));
-        };
-        auto issue_pv = [&](int c, int tile, bool first) {
-            const uint64_t b0 = vdesc + (uint64_t)(tile % STAGES) * STG;
-            const uint32_t d = tmem + col_o(c), a = tmem + col_s(c);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, (kk > 0 || !first) ? 1u : 0u);
-        };
-        int tile = 0, items = 0;
-        bool ok = true;
-        for (;;) {
-            const int slot = items & 1;
-            if (!(ok = warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(items >> 1) & 1u, ab)))) break;
-            const Item it = ms.work[slot];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_item_empty(slot));
-            if (it.n_kv < 0) break;
-            // S of the item's first tile: the S columns are free (the previous item's last
-            // P V was issued before, and the tensor pipe completes in issue order)
-            if (!(ok = warp_all(mbar_wait(bar_q_full, (uint32_t)items & 1u, ab)))) break;
-            if (!(ok = warp_all(mbar_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
-            tc_fence_after();
-            issue_s(0, tile);
-            issue_s(1, tile);
-            for (int j = 0; j < it.n_kv; ++j, ++tile) {
-                const int s = tile % STAGES;
-                const bool has_next = j + 1 < it.n_kv;
-                const int t1 = tile + 1;
-                if (!(ok = warp_all(mbar_wait(bar_v_full(s), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
-                if (j == 0 && !(ok = warp_all(mbar_wait(bar_o_empty, ((uint32_t)items & 1u) ^ 1u, ab)))) break;
-                if (!(ok = warp_all(mbar_wait(bar_p_ready(0), (uint32_t)tile & 1u, ab)))) break;
-                tc_fence_after();
-                issue_pv(0, tile, j == 0);
-                if (has_next) {
-                    if (!(ok = warp_all(mbar_wait(bar_k_full(t1 % STAGES), (uint32_t)(t1 / STAGES) & 1u, ab)))) break;
-                    issue_s(0, t1);
-                }
-                if (!(ok = warp_all(mbar_wait(bar_p_ready(1), (uint32_t)tile & 1u, ab)))) break;
-                tc_fence_after();
-                issue_pv(1, tile, j == 0);
-                mma_commit_elect(bar_kv_empty(s));
-                if (has_next) issue_s(1, t1);
-            }
-            if (!ok) break;
-            mma_commit_elect(bar_q_empty);  // every MMA reading this item's Q has been issued
-            mma_commit_elect(bar_o_full);
-            ++items;
-        }
-        // every MMA issued has completed before TMEM is released
-        mma_commit_elect(bar_q_empty);
-        mbar_wait_drain(bar_q_empty, (uint32_t)items & 1u, p.timeout_ns);
-        __syncwarp();
-    } else {
-        // ============================ softmax and epilogue (warps 0-7) ===
+    // Each warpgroup moves to its register count first (setmaxnreg applies to the
+    // whole warpgroup, so warps 12-15 share one branch).
+    if (warp < EPI_WARP0) {
+        setmaxnreg_inc<REG_SOFTMAX>();
+        // ====================================================== softmax (warps 0-7) ===
         const int c = warp >> 2;
         const int r = (warp & 3) * 32 + lane;  // query row in the tile = TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -326,15 +189,17 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         int tile = 0, items = 0;
         bool ok = true;
         for (;;) {
-            const int slot = items & 1;
-            ok = warp_all(ok && mbar_wait(bar_item_full(slot), (uint32_t)(items >> 1) & 1u, ab));
-            // the eight warps go on or stop together (each later passes the epilogue barriers)
+            const int slot = items % NSLOT;
+            ok = warp_all(ok && mbar_wait(bar_item_full(slot), (uint32_t)(items / NSLOT) & 1u, ab));
+            // the eight warps go on or stop together
             ok = named_barrier_and(2, 256, ok);
             if (!ok) break;
             const Item it = ms.work[slot];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_item_empty(slot));
-            if (it.n_kv < 0) break;
+            if (it.n_kv < 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_item_empty(slot));
+                break;
+            }
             const int qi = it.qt * BM + r;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; ok && j < it.n_kv; ++j, ++tile) {
@@ -342,11 +207,14 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 tc_fence_after();
                 float x[BN];
                 {
-                    uint32_t sr[BN];
-                    tmem_ld128(t_s, sr);
+                    // two 64-column loads: one 128-column load needs more registers than
+                    // the kernel's launch count, against which every instruction is checked
+                    uint32_t sr[2][64];
+                    tmem_ld64(t_s, sr[0]);
+                    tmem_ld64(t_s + 64, sr[1]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e]);
+                    for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e >> 6][e & 63]);
                 }
                 const int kbase = j * BN;
                 if ((p.causal && j == it.qt) || kbase + BN > it.len) {
@@ -408,26 +276,59 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 tc_fence_before();
                 mbar_arrive(bar_p_ready(c));
             }
-            // Every warp passes both epilogue barriers, also after a wait of its own ran
-            // out (ok false); the decision to stop is taken at the second one, jointly.
-            if (ok && p.lse != nullptr && qi < it.len) p.lse[((size_t)(it.start + qi) * p.H + it.h) * 2 + c] = m + __log2f(l);
-            // ---- epilogue: warpgroup c handles values [64c, 64c + 64) of every row
-            ms.xch[c * BM + r] = 1.f / l;
-            named_barrier_sync(1, 256);
-            ok = warp_all(ok && mbar_wait(bar_o_full, (uint32_t)items & 1u, ab));
+            ok = named_barrier_and(2, 256, ok);
+            if (!ok) break;
+            // Training outputs: lse_c = m_c + log2(l_c), so that P_c = 2^(S_c scale log2(e) - lse_c).
+            // The item's start and head are read again from its slot (the softmax warps
+            // release the slot only below): held across the tile loop they pushed the
+            // softmax warps past their registers.
+            if (p.lse != nullptr && qi < it.len) {
+                const volatile Item* iv = &ms.work[slot];
+                p.lse[((size_t)(iv->start + qi) * p.H + iv->h) * 2 + c] = m + __log2f(l);
+            }
+            // 1/l_c for the epilogue; the buffer of this parity was read by the epilogue
+            // of item - 2 before it released O for item - 1, whose first P V precedes
+            // every score of this item
+            ms.il[items & 1][c][r] = 1.f / l;
+            mbar_arrive(bar_stats_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_item_empty(slot));
+            ++items;
+        }
+    } else if (warp < PRODUCER_WARP) {
+        setmaxnreg_dec<REG_EPI>();
+        // =================================================== epilogue (warps 8-11) ===
+        // One thread per row, all dv values: D = O1/l1 - lambda O2/l2, RMSNorm over dv,
+        // weight, (1 - lambda_init), bf16. O is read twice (the sum of squares, then the
+        // normalised output) so that D is not held in registers. Each half of the row is
+        // summed on its own and the halves added, the order of the one-item-per-CTA
+        // kernel's two warpgroups, so the two kernels give the same bits.
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_o1 = tmem + lane_off + col_o(0), t_o2 = tmem + lane_off + col_o(1);
+        int items = 0;
+        for (;;) {
+            const int slot = items % NSLOT;
+            if (!warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(items / NSLOT) & 1u, ab))) break;
+            const Item it = ms.work[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_item_empty(slot));
+            if (it.n_kv < 0) break;
+            const int par = items & 1;
+            if (!warp_all(mbar_wait(bar_stats_full, (uint32_t)par, ab))) break;
+            if (!warp_all(mbar_wait(bar_o_full, (uint32_t)par, ab))) break;
+            tc_fence_after();
+            const int qi = it.qt * BM + r;
             const bool store = qi < it.len;
-            // Two passes over O (D is not kept across the exchange, which keeps the
-            // register count under the cap of ten warps): the sum of squares of this
-            // warpgroup's half of D, then D again, normalised and stored.
             const float lam = p.lambda[it.h * p.lambda_stride];
-            const float il1 = ms.xch[r], il2 = ms.xch[BM + r];
-            const uint32_t t_o1 = tmem + lane_off + col_o(0) + 64 * c;
-            const uint32_t t_o2 = tmem + lane_off + col_o(1) + 64 * c;
-            float ssp = 0.f;
-            if (ok) {
-                tc_fence_after();
+            const float il1 = ms.il[par][0][r], il2 = ms.il[par][1][r];
+            float ss_half[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float ssp = 0.f;
 #pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) {
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int ch = hf * 2 + c2;
                     uint32_t o1[32], o2[32];
                     tmem_ld32(t_o1 + ch * 32, o1);
                     tmem_ld32(t_o2 + ch * 32, o2);
@@ -437,8 +338,10 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                         const float d = diff_combine(__uint_as_float(o1[i]), il1, __uint_as_float(o2[i]), il2, lam);
                         ssp = fmaf(d, d, ssp);
                     }
+                    // Training outputs: the normalised attention output of each component,
+                    // kept in fp32 (the lambda gradient sums many cancelling terms of them).
                     if (store && p.o1 != nullptr) {
-                        const size_t base = ((size_t)(it.start + qi) * p.H + it.h) * DV / 4 + c * 16 + ch * 8;
+                        const size_t base = ((size_t)(it.start + qi) * p.H + it.h) * DV / 4 + ch * 8;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             reinterpret_cast<float4*>(p.o1)[base + i] =
@@ -450,41 +353,196 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                         }
                     }
                 }
+                ss_half[hf] = ssp;
             }
-            ms.xch[2 * BM + c * BM + r] = ssp;
-            ok = named_barrier_and(1, 256, ok);
-            if (ok) {
-                const float ss = ms.xch[2 * BM + r] + ms.xch[3 * BM + r];
-                const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DV + p.eps);
-                const float* wv = ms.w + 64 * c;
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                      ((size_t)(it.start + (store ? qi : 0)) * p.H + it.h) * DV + 64 * c);
+            const float ss = ss_half[0] + ss_half[1];
+            const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DV + p.eps);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                  ((size_t)(it.start + (store ? qi : 0)) * p.H + it.h) * DV);
 #pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(t_o1 + ch * 32, o1);
-                    tmem_ld32(t_o2 + ch * 32, o2);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+            for (int ch = 0; ch < DV / 32; ++ch) {
+                uint32_t o1[32], o2[32];
+                tmem_ld32(t_o1 + ch * 32, o1);
+                tmem_ld32(t_o2 + ch * 32, o2);
+                tmem_wait_ld();
+                if (ch == DV / 32 - 1) {  // O has been read: the next item's first P V may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(bar_o_empty);
+                }
+                uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int e = ch * 32 + 2 * i;
-                        const float d0 = diff_combine(__uint_as_float(o1[2 * i]), il1, __uint_as_float(o2[2 * i]), il2, lam);
-                        const float d1 = diff_combine(__uint_as_float(o1[2 * i + 1]), il1, __uint_as_float(o2[2 * i + 1]), il2, lam);
-                        pk[i] = pack_bf16x2(d0 * post * wv[e], d1 * post * wv[e + 1]);
-                    }
-                    if (store) {
+                for (int i = 0; i < 16; ++i) {
+                    const int e = ch * 32 + 2 * i;
+                    const float d0 = diff_combine(__uint_as_float(o1[2 * i]), il1, __uint_as_float(o2[2 * i]), il2, lam);
+                    const float d1 =
+                        diff_combine(__uint_as_float(o1[2 * i + 1]), il1, __uint_as_float(o2[2 * i + 1]), il2, lam);
+                    pk[i] = pack_bf16x2(d0 * post * ms.w[e], d1 * post * ms.w[e + 1]);
+                }
+                if (store) {
 #pragma unroll
-                        for (int g4 = 0; g4 < 4; ++g4)
-                            dst[ch * 4 + g4] = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
-                    }
+                    for (int g4 = 0; g4 < 4; ++g4)
+                        dst[ch * 4 + g4] = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
                 }
             }
-            // O has been read: the next item's first P V may overwrite it
-            tc_fence_before();
-            mbar_arrive(bar_o_empty);
-            if (!ok) break;
             ++items;
+        }
+    } else {
+        setmaxnreg_dec<REG_COPY>();
+        if (warp == PRODUCER_WARP) {
+            // ================================================= TMA producer ===
+            // Item k of the longest-first order (query tile descending, then sequence,
+            // then head, empty (tile, sequence) pairs left out): rank q = n_qt - 1 - qt
+            // holds the sequences with at least n_qt - q tiles; a cursor walks the ranks
+            // as k grows. This CTA takes k = r G + c on even rounds r, r G + G - 1 - c
+            // on odd ones.
+            if (lane == 0) {
+                const uint64_t pol_q = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
+                const bool packed = p.cu_seqlens != nullptr;
+                auto tiles_of = [&](int sq_i) { return packed ? (int)ms.tiles[sq_i] : n_qt; };
+                auto count_rank = [&](int q) {  // sequences with at least n_qt - q tiles
+                    if (!packed) return p.num_seqs;
+                    int n = 0;
+                    for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) n += tiles_of(sq_i) >= n_qt - q;
+                    return n;
+                };
+                long long total = 0;
+                for (int sq_i = 0; sq_i < p.num_seqs; ++sq_i) total += tiles_of(sq_i);
+                const long long n_valid = total * p.H;
+                const long long G = gridDim.x;
+                int q = 0, cq = count_rank(0);
+                long long P = 0;
+                int tile = 0, items = 0;
+                bool ok = true;
+                for (long long r = 0; ok && r * G < n_valid; ++r) {
+                    const long long k = r * G + ((r & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+                    if (k >= n_valid) continue;
+                    while (k >= P + (long long)cq * p.H) {
+                        P += (long long)cq * p.H;
+                        cq = count_rank(++q);
+                    }
+                    const int j = (int)((k - P) / p.H), h = (int)((k - P) % p.H);
+                    int sq_i = j;
+                    if (packed) {
+                        int cnt = -1;
+                        for (sq_i = 0; sq_i < p.num_seqs; ++sq_i)
+                            if (tiles_of(sq_i) >= n_qt - q && ++cnt == j) break;
+                    }
+                    Item it{};
+                    it.h = h;
+                    it.qt = n_qt - 1 - q;
+                    it.start = packed ? p.cu_seqlens[sq_i] : sq_i * p.seqlen;
+                    it.len = packed ? p.cu_seqlens[sq_i + 1] - it.start : p.seqlen;
+                    it.n_kv = p.causal ? it.qt + 1 : (it.len + BN - 1) / BN;
+                    const int slot = items % NSLOT;
+                    if (!(ok = mbar_wait(bar_item_empty(slot), ((uint32_t)(items / NSLOT) & 1u) ^ 1u, ab))) break;
+                    ms.work[slot] = it;
+                    mbar_arrive(bar_item_full(slot));
+                    if (p.inject == 1) {  // test hook: no loads, so the other roles' waits run out
+                        ++items;
+                        continue;
+                    }
+                    const int g = h / (p.H / p.Hkv);
+                    if (!(ok = mbar_wait(bar_q_empty, ((uint32_t)items & 1u) ^ 1u, ab))) break;
+                    const int row_q = it.start + it.qt * BM;
+                    mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
+                    tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
+                    tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
+                    for (int jj = 0; jj < it.n_kv; ++jj, ++tile) {
+                        const int s = tile % STAGES;
+                        if (!(ok = mbar_wait(bar_kv_empty(s), ((uint32_t)(tile / STAGES) & 1u) ^ 1u, ab))) break;
+                        const int row = it.start + jj * BN;
+                        mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
+                        tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
+                        tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
+                        mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
+                        tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
+                        tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+                    }
+                    ++items;
+                }
+                // end of the items: a sentinel in the next slot
+                const int slot = items % NSLOT;
+                if (ok && mbar_wait(bar_item_empty(slot), ((uint32_t)(items / NSLOT) & 1u) ^ 1u, ab)) {
+                    Item end{};
+                    end.n_kv = -1;
+                    ms.work[slot] = end;
+                    mbar_arrive(bar_item_full(slot));
+                }
+                // Let every copy this CTA started land before shared memory goes away.
+                const int loaded = p.inject == 1 ? 0 : items;
+                if (loaded > 0) mbar_wait_drain(bar_q_full, (uint32_t)(loaded - 1) & 1u, p.timeout_ns);
+                for (int jj = tile > STAGES ? tile - STAGES : 0; jj < tile; ++jj) {
+                    const uint32_t ph = (uint32_t)(jj / STAGES) & 1u;
+                    mbar_wait_drain(bar_k_full(jj % STAGES), ph, p.timeout_ns);
+                    mbar_wait_drain(bar_v_full(jj % STAGES), ph, p.timeout_ns);
+                }
+            }
+            __syncwarp();
+        } else if (warp == MMA_WARP) {
+            // ==================================================== MMA issuer ===
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
+            constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, STG = STAGE_BYTES >> 4, BOX = BOX_BYTES >> 4;
+            const uint64_t qdesc = desc_kmajor(sq), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
+            auto issue_s = [&](int c, int tile) {
+                const uint64_t a0 = qdesc + (uint64_t)c * BOX;
+                const uint64_t b0 = kdesc + (uint64_t)(tile % STAGES) * STG + (uint64_t)c * BOX;
+                const uint32_t d = tmem + col_s(c);
+    #pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a0 + kk * KSTEP, b0 + kk * KSTEP, idesc_s, kk > 0 ? 1u : 0u);
+                mma_commit_elect(bar_s_full(c));
+            };
+            auto issue_pv = [&](int c, int tile, bool first) {
+                const uint64_t b0 = vdesc + (uint64_t)(tile % STAGES) * STG;
+                const uint32_t d = tmem + col_o(c), a = tmem + col_s(c);
+    #pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, (kk > 0 || !first) ? 1u : 0u);
+            };
+            int tile = 0, items = 0;
+            bool ok = true;
+            for (;;) {
+                const int slot = items % NSLOT;
+                if (!(ok = warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(items / NSLOT) & 1u, ab)))) break;
+                const Item it = ms.work[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_item_empty(slot));
+                if (it.n_kv < 0) break;
+                // S of the item's first tile: the S columns are free (the previous item's last
+                // P V was issued before, and the tensor pipe completes in issue order)
+                if (!(ok = warp_all(mbar_wait(bar_q_full, (uint32_t)items & 1u, ab)))) break;
+                if (!(ok = warp_all(mbar_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
+                tc_fence_after();
+                issue_s(0, tile);
+                issue_s(1, tile);
+                for (int j = 0; j < it.n_kv; ++j, ++tile) {
+                    const int s = tile % STAGES;
+                    const bool has_next = j + 1 < it.n_kv;
+                    const int t1 = tile + 1;
+                    if (!(ok = warp_all(mbar_wait(bar_v_full(s), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
+                    if (j == 0 && !(ok = warp_all(mbar_wait(bar_o_empty, ((uint32_t)items & 1u) ^ 1u, ab)))) break;
+                    if (!(ok = warp_all(mbar_wait(bar_p_ready(0), (uint32_t)tile & 1u, ab)))) break;
+                    tc_fence_after();
+                    issue_pv(0, tile, j == 0);
+                    if (has_next) {
+                        if (!(ok = warp_all(mbar_wait(bar_k_full(t1 % STAGES), (uint32_t)(t1 / STAGES) & 1u, ab)))) break;
+                        issue_s(0, t1);
+                    }
+                    if (!(ok = warp_all(mbar_wait(bar_p_ready(1), (uint32_t)tile & 1u, ab)))) break;
+                    tc_fence_after();
+                    issue_pv(1, tile, j == 0);
+                    mma_commit_elect(bar_kv_empty(s));
+                    if (has_next) issue_s(1, t1);
+                }
+                if (!ok) break;
+                mma_commit_elect(bar_q_empty);  // every MMA reading this item's Q has been issued
+                mma_commit_elect(bar_o_full);
+                ++items;
+            }
+            // every MMA issued has completed before TMEM is released
+            mma_commit_elect(bar_q_empty);
+            mbar_wait_drain(bar_q_empty, (uint32_t)items & 1u, p.timeout_ns);
+            __syncwarp();
         }
     }
 
@@ -510,6 +568,15 @@ cudaError_t launch_fwd_bf16_persistent(const FwdParams& p, const FwdTensorMaps& 
         if (err != cudaSuccess) return err;
         attr_done[dev] = true;
     }
+    // the register split needs the launch to hold REG_LAUNCH registers a thread
+    static int launch_regs = 0;
+    if (launch_regs == 0) {
+        cudaFuncAttributes fa{};
+        err = cudaFuncGetAttributes(&fa, diffattn_fwd_bf16_persistent_kernel);
+        if (err != cudaSuccess) return err;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs * NUM_THREADS < REG_NEED || launch_regs < REG_LAUNCH) return cudaErrorInvalidConfiguration;
     int sms = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;

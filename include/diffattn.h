@@ -108,8 +108,8 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
  * Name of the kernel diffattn_fwd / diffattn_fwd_train launch for `desc`
  * (packed nonzero: with cu_seqlens), or NULL for an unsupported dtype / d.
  * bf16 inputs run "diffattn_fwd_bf16_sm103a_kernel" (one CTA per 128 query rows
- * of one head of one sequence) or, when those items have at most 32 key tiles
- * (max_seqlen <= 4096), number at least two per SM and come from at most 64
+ * of one head of one sequence) or, when those items have at most 64 key tiles
+ * (max_seqlen <= 8192), number at least two per SM and come from at most 64
  * packed sequences, "diffattn_fwd_bf16_persistent_kernel" (one CTA per SM
  * walking the items). The two give the same bits for the same rows. fp32
  * inputs run "diffattn_fwd_f32_kernel".

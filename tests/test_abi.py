@@ -85,7 +85,7 @@ def test_fwd_rejects_on_host(lib, kw, ptrs, want):
 
 
 def test_forward_kernel_choice(lib):
-    # items of at most 32 key tiles, at least two per SM, at most 64 packed
+    # items of at most 64 key tiles, at least two per SM, at most 64 packed
     # sequences: the persistent kernel (the library assumes 152 SMs when no GPU
     # answers; a GB300 has 152)
     def kernel(packed=0, **kw):
@@ -101,7 +101,9 @@ def test_forward_kernel_choice(lib):
                   num_kv_heads=4) == "diffattn_fwd_bf16_sm103a_kernel"
     assert kernel(packed=1, num_seqs=2, max_seqlen=256, total_tokens=356, num_heads=16,
                   num_kv_heads=4) == "diffattn_fwd_bf16_sm103a_kernel"
-    assert kernel(batch=2, seqlen=8192, num_heads=16, num_kv_heads=4) == "diffattn_fwd_bf16_sm103a_kernel"
+    assert kernel(batch=2, seqlen=8192, num_heads=16, num_kv_heads=4) == "diffattn_fwd_bf16_persistent_kernel"
+    assert kernel(batch=1, seqlen=8193, num_heads=16, num_kv_heads=4) == "diffattn_fwd_bf16_sm103a_kernel"
+    assert kernel(batch=1, seqlen=32768, num_heads=16, num_kv_heads=16) == "diffattn_fwd_bf16_sm103a_kernel"
     assert kernel(d=16, dv=32, dtype=_lib.DTYPE_F32) == "diffattn_fwd_f32_kernel"
     assert kernel(d=32, dv=64) is None
 
