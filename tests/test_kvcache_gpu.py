@@ -102,3 +102,19 @@ def test_split_past_the_visible_keys_of_early_rows():
     # key visible to the first new query (position 254): an empty partial
     inp = W.generate_kv(kvw(batch=3, q_len=4), seed=56, lengths=[258, 130, 1000])
     compare(run_gpu_kv(inp, num_splits=4), oracle_kv(inp), "bf16")
+
+
+def test_ragged_lengths_library_splits():
+    # library-planned splits over ragged caches: lengths from one tile to the
+    # whole cache, so most splits of the short sequences hold no key
+    inp = W.generate_kv(kvw(batch=6, capacity=4000, q_len=2), seed=57, lengths=[4000, 10, 2500, 700, 64, 3999])
+    compare(run_gpu_kv(inp), oracle_kv(inp), "bf16")
+
+
+def test_more_groups_than_resident_ctas():
+    # 200 sequences x 4 kv heads: more (sequence, kv head) groups than resident
+    # split CTAs, so the plan takes one split each over more than one wave
+    rng = np.random.default_rng(58)
+    lengths = rng.integers(1, 301, 200).tolist()
+    inp = W.generate_kv(kvw(batch=200, capacity=300), seed=58, lengths=lengths)
+    compare(run_gpu_kv(inp), oracle_kv(inp), "bf16")

@@ -169,24 +169,28 @@ def test_batch_equals_separate_calls_bitwise():
         assert torch.equal(run_gpu(one), full[a:b])
 
 
-def test_persistent_and_per_tile_kernels_agree_bitwise():
-    """An unpacked batch of 3 x 1000 tokens runs on the persistent kernel, each
+# 3 x 1000 tokens, 16 / 4 heads (8 key tiles an item); 3 x 8192 tokens, 2 heads
+# (items of up to 64 key tiles, the longest the persistent kernel takes)
+@pytest.mark.parametrize("T,H,Hkv", [(1000, 16, 4), (8192, 2, 2)])
+def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv):
+    """An unpacked batch of three sequences runs on the persistent kernel, each
     sequence alone on the one-item-per-CTA kernel: the same bits."""
-    inp = W.generate(BF, seed=32, seq_lens=[1000, 1000, 1000])
-    B, T = 3, 1000
+    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv)
+    inp = W.generate(wl, seed=32, seq_lens=[T] * 3)
+    B = 3
     sh = lambda x: x.cuda().view(B, T, *x.shape[1:])  # noqa: E731
     lam = torch.ones(1, dtype=torch.float32, device="cuda")
     assert da.diffattn_fwd_kernel(sh(inp.q), sh(inp.k), sh(inp.v), lam,
                                   inp.subln_w.cuda()) == "diffattn_fwd_bf16_persistent_kernel"
     full = run_gpu(inp, packed=False)
     for s in range(3):
-        one = W.generate(BF, seed=32, seq_lens=[1000, 1000, 1000])
-        a, b = s * 1000, (s + 1) * 1000
+        one = W.generate(wl, seed=32, seq_lens=[T] * 3)
+        a, b = s * T, (s + 1) * T
         one.q, one.k, one.v = one.q[a:b], one.k[a:b], one.v[a:b]
-        one.seq_lens, one.cu_seqlens = [1000], torch.tensor([0, 1000], dtype=torch.int32)
+        one.seq_lens, one.cu_seqlens = [T], torch.tensor([0, T], dtype=torch.int32)
         cu = one.cu_seqlens.cuda()
         assert da.diffattn_fwd_kernel(one.q.cuda(), one.k.cuda(), one.v.cuda(), lam, inp.subln_w.cuda(), cu_seqlens=cu,
-                                      max_seqlen=1000) == "diffattn_fwd_bf16_sm103a_kernel"
+                                      max_seqlen=T) == "diffattn_fwd_bf16_sm103a_kernel"
         assert torch.equal(run_gpu(one), full[a:b])
 
 
