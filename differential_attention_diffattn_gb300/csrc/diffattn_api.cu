@@ -709,6 +709,6 @@ const char* diffattn_status_string(diffattn_status s) {
 
 void diffattn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : kDefaultWaitTimeoutNs; }
 
-void diffattn_set_fault_injection(int mode) { g_inject = mode == 1 ? 1 : 0; }
+void diffattn_set_fault_injection(int mode) { g_inject = (mode == 1 || mode == 2) ? mode : 0; }
 
 }  // extern "C"

@@ -27,8 +27,8 @@
 // holds; each SM sub-partition runs two softmax warps, one epilogue warp and one
 // of warps 12-15: 2 x 168 + 88 + 88 = 512 registers a lane, its whole share).
 // Barriers that advance once per item: item_full / item_empty (a four-slot ring
-// of items), q_full / q_empty (the Q box), stats_full (1/l_c per row from the
-// softmax warps), o_full / o_empty (the O accumulators: an item's first P V
+// of items), q_full / q_empty (the Q box), stats_full[item parity] (1/l_c per
+// row from the softmax warps), o_full / o_empty (the O accumulators: an item's first P V
 // waits until the epilogue of the previous one has read them); once per key
 // tile over all items: the K / V ring, s_full, p_ready. Every wait is bounded;
 // the eight softmax warps decide together, at each item's start and end,
@@ -77,7 +77,7 @@ struct Misc {
     uint64_t q_full, q_empty;
     uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
     uint64_t s_full[2], p_ready[2];
-    uint64_t o_full, o_empty, stats_full;
+    uint64_t o_full, o_empty, stats_full[2];
     uint32_t tmem_base;
     int abort_flag;
     float il[2][2][BM];                 // 1/l_c per row, by item parity and component
@@ -124,7 +124,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
     auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full), bar_o_empty = smem_u32(&ms.o_empty);
-    const uint32_t bar_stats_full = smem_u32(&ms.stats_full);
+    auto bar_stats_full = [&](int i) { return smem_u32(&ms.stats_full[i]); };
     const uint32_t sq = sbase + OFF_Q;
     auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
     auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
@@ -150,7 +150,8 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         }
         mbar_init(bar_o_full, 1);
         mbar_init(bar_o_empty, 128);     // every epilogue thread
-        mbar_init(bar_stats_full, 256);  // every softmax thread
+        mbar_init(bar_stats_full(0), 256);  // every softmax thread, items of even / odd index
+        mbar_init(bar_stats_full(1), 256);
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -286,11 +287,15 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 const volatile Item* iv = &ms.work[slot];
                 p.lse[((size_t)(iv->start + qi) * p.H + iv->h) * 2 + c] = m + __log2f(l);
             }
-            // 1/l_c for the epilogue; the buffer of this parity was read by the epilogue
-            // of item - 2 before it released O for item - 1, whose first P V precedes
-            // every score of this item
+            // 1/l_c for the epilogue, in the buffer and on the barrier of this item's
+            // parity: the epilogue of item - 2 read that buffer and waited on that
+            // barrier before it released O for item - 1, whose first P V precedes every
+            // score of this item. (One barrier for all items could run two phases ahead
+            // of the epilogue: an item of one key tile needs no P V before its scores,
+            // so its stats can follow the previous item's while the epilogue is still on
+            // the one before, and a parity wait cannot tell those phases apart.)
             ms.il[items & 1][c][r] = 1.f / l;
-            mbar_arrive(bar_stats_full);
+            mbar_arrive(bar_stats_full(items & 1));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_item_empty(slot));
             ++items;
@@ -314,8 +319,13 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_item_empty(slot));
             if (it.n_kv < 0) break;
+            if (p.inject == 2) {  // test hook: hold the epilogue back so the softmax warps run ahead
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 20000ull) {
+                }
+            }
             const int par = items & 1;
-            if (!warp_all(mbar_wait(bar_stats_full, (uint32_t)par, ab))) break;
+            if (!warp_all(mbar_wait(bar_stats_full(par), (uint32_t)(items >> 1) & 1u, ab))) break;
             if (!warp_all(mbar_wait(bar_o_full, (uint32_t)par, ab))) break;
             tc_fence_after();
             const int qi = it.qt * BM + r;

@@ -37,7 +37,8 @@ struct FwdParams {
     float scale_log2;         // d^-0.5 * log2(e)
     float scale;              // d^-0.5
     unsigned long long timeout_ns;
-    int inject;               // test hook: 1 = the copy producer issues no loads
+    int inject;               // test hook: 1 = the copy producer issues no loads; 2 = the persistent
+                              // kernel's epilogue pauses ~20 us before each item
     float* lse;               // training outputs (all null, or all set; bf16 kernel only):
     void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
     void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c

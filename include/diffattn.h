@@ -435,8 +435,11 @@ void diffattn_set_wait_timeout_ns(unsigned long long ns);
  * producer of the bf16 forward kernel issues no loads, so the barriers every
  * other role waits on are never armed; each wait runs out after the wait limit,
  * the kernel records DIFFATTN_ERR_TIMEOUT, frees its tensor memory and returns,
- * and diffattn_get_device_status reports it. mode 0 (the default) turns it off.
- * Affects launches made after the call; nothing faults, traps or hangs.
+ * and diffattn_get_device_status reports it. mode 2: the epilogue warpgroup of
+ * the persistent bf16 forward pauses about 20 us (a bounded spin) before each
+ * item, so that the softmax warps run ahead of it; the results and the status
+ * must not change. mode 0 (the default) turns it off. Affects launches made
+ * after the call; nothing faults, traps or hangs.
  */
 void diffattn_set_fault_injection(int mode);
 

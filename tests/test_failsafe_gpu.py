@@ -42,3 +42,26 @@ def test_wait_timeout_reported_and_context_usable(lens, packed):
         da.diffattn_set_wait_timeout_ns(0)
     assert da.diffattn_get_device_status() == 0  # the read cleared it
     compare(run_gpu(inp, packed=packed), oracle_out(inp), "bf16")
+
+
+def test_epilogue_held_back_changes_nothing():
+    """The persistent kernel's epilogue warpgroup paused ~20 us before each item,
+    so that the softmax warps run ahead of it, also through items of one key
+    tile (which need no P V before their scores): the same bits, no timeout.
+    With one 1/l barrier for all items instead of one per item parity, its phase
+    could run two ahead of the epilogue here and the epilogue's wait ran out."""
+    lens = [1000, 90, 700, 128, 40, 1000, 300, 129, 64, 900, 1, 500, 256, 77, 1000, 640]
+    inp = W.generate(W.WORKLOADS["b2_t512_gqa"], seed=72, seq_lens=lens)
+    t = {k: v.cuda() for k, v in (("q", inp.q), ("k", inp.k), ("v", inp.v))}
+    lam = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert da.diffattn_fwd_kernel(t["q"], t["k"], t["v"], lam, inp.subln_w.cuda(), cu_seqlens=inp.cu_seqlens.cuda(),
+                                  max_seqlen=max(lens)) == "diffattn_fwd_bf16_persistent_kernel"
+    ref = run_gpu(inp)
+    da.diffattn_set_wait_timeout_ns(200_000_000)  # 200 ms
+    da.diffattn_set_fault_injection(2)
+    try:
+        got = run_gpu(inp)  # asserts a zero status word
+    finally:
+        da.diffattn_set_fault_injection(0)
+        da.diffattn_set_wait_timeout_ns(0)
+    assert torch.equal(got, ref)
