@@ -60,8 +60,17 @@ def run_case(wl, lens, seed):
 BF = W.WORKLOADS["b2_t512_gqa"]
 
 
-def test_training_outputs_match_oracle():
-    inp, dy, out, lse, o1, o2, *_ = run_case(BF, [300, 129], 81)
+# two packed sequences: the one-item-per-CTA kernel; eight (384 items of up to
+# three key tiles): the persistent kernel, whose epilogue warpgroup writes O1, O2
+@pytest.mark.parametrize("lens,kernel", [([300, 129], "diffattn_fwd_bf16_sm103a_kernel"),
+                                         ([300, 129, 200, 1, 256, 77, 300, 150],
+                                          "diffattn_fwd_bf16_persistent_kernel")])
+def test_training_outputs_match_oracle(lens, kernel):
+    chk = W.generate(BF, seed=81, seq_lens=lens)
+    lam1 = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert da.diffattn_fwd_kernel(chk.q.cuda(), chk.k.cuda(), chk.v.cuda(), lam1, chk.subln_w.cuda(),
+                                  cu_seqlens=chk.cu_seqlens.cuda(), max_seqlen=chk.max_seqlen) == kernel
+    inp, dy, out, lse, o1, o2, *_ = run_case(BF, lens, 81)
     compare(out, oracle_out(inp), "bf16")
     # normalised attention outputs: the oracle with lambda = 0, lambda_init = 0,
     # w = 1 and a huge eps returns O1 / sqrt(eps); swapping components gives O2
