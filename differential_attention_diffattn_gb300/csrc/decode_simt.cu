@@ -15,105 +15,94 @@ namespace {
 
 constexpr int DVD = 128;        // value dim
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-    return x;
-}
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
 
-// One CTA of 256 threads per (batch, query, head). The (m, l) of every split are
-// staged in shared memory by parallel loads and the split weights 2^(m_s - M)
-// computed once; then warp w sums splits w, w + 8, ... for both components
-// (lane = four value columns, float4 loads), the eight warps' sums are added
-// through shared memory, and the first 128 threads (one per value column)
-// normalise and store.
+// One warp per (batch, query, head) row, eight rows a block; lane l owns value
+// columns 4l .. 4l + 3. The splits are merged online, SPLITS_PER_ROUND at a time
+// with all their loads in flight together (no block-wide step: the row's whole
+// merge is one warp's): per component the running maximum M is raised to the
+// round's largest m_s and the running sums rescaled; split s weighs 2^(m_s - M)
+// (an empty split, m_s = -inf, weighs 0). Then O_c = acc_c / l_c, D = O_1 -
+// lambda O_2, the RMSNorm over dv (a warp reduction), the weight and
+// (1 - lambda_init), and four bf16 values per lane.
 constexpr int MAX_COMBINE_SPLITS = 1024;
 constexpr int CWARPS = 8;
+constexpr int SPLITS_PER_ROUND = 4;
 
 __global__ void __launch_bounds__(32 * CWARPS)
 diffattn_decode_combine_kernel(const KvParams p) {
     griddep_wait();  // a programmatic dependent of the split kernel: its partials are complete
-    const int row = blockIdx.x;  // ((b * q_len) + t) * H + h
-    const int h = row % p.H;
-    const int b = row / (p.H * p.q_len);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * CWARPS + (threadIdx.x >> 5);  // ((b * q_len) + t) * H + h
+    if (row >= (long long)p.batch * p.q_len * p.H) return;
+    const int h = (int)(row % p.H);
+    const int b = (int)(row / ((long long)p.H * p.q_len));
     const int L = p.cache_seqlens ? p.cache_seqlens[b] : p.capacity;
     if (L < p.q_len || L > p.capacity) return;  // reported by the split kernel
-    __shared__ float wgt[2][MAX_COMBINE_SPLITS];  // m_s, then 2^(m_s - M)
-    __shared__ float lsm[2][MAX_COMBINE_SPLITS];
-    __shared__ __align__(16) float part[CWARPS][2][DVD];
-    __shared__ float red[DVD / 32];
-    __shared__ float mmax[2], lsum[2];
     const int n = p.num_splits;
-    const float* ml = p.ws_ml + (size_t)row * n * 4;  // [split][component][m, l]
-    for (int i = tid; i < 2 * n; i += 32 * CWARPS) {
-        const int s_ = i >> 1, c = i & 1;
-        wgt[c][s_] = ml[(s_ * 2 + c) * 2];
-        lsm[c][s_] = ml[(s_ * 2 + c) * 2 + 1];
-    }
-    __syncthreads();
-    if (warp < 2) {  // warp 0: max of component 0, warp 1: component 1
-        float m = -INFINITY;
-        for (int s_ = lane; s_ < n; s_ += 32) m = fmaxf(m, wgt[warp][s_]);
-        m = warp_max(m);
-        if (lane == 0) mmax[warp] = m;
-    }
-    __syncthreads();
-    for (int i = tid; i < 2 * n; i += 32 * CWARPS) {
-        const int s_ = i >> 1, c = i & 1;
-        const float ms = wgt[c][s_];
-        wgt[c][s_] = ms == -INFINITY ? 0.f : exp2f(ms - mmax[c]);  // empty splits weigh nothing
-    }
-    __syncthreads();
-    if (warp < 2) {
-        float ls = 0.f;
-        for (int s_ = lane; s_ < n; s_ += 32) ls = fmaf(lsm[warp][s_], wgt[warp][s_], ls);
-        ls = warp_sum(ls);
-        if (lane == 0) lsum[warp] = ls;
-    }
+    const float* ml = p.ws_ml + (size_t)row * n * 4;              // [split][component][m, l]
+    const float4* op = reinterpret_cast<const float4*>(p.ws_o + (size_t)row * n * 2 * DVD) + lane;  // [split][c][dv]
+    float M[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s0 = 0; s0 < n; s0 += SPLITS_PER_ROUND) {
+        float4 mlv[SPLITS_PER_ROUND];  // m_1, l_1, m_2, l_2
+        float4 ov[SPLITS_PER_ROUND][2];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4* op = reinterpret_cast<const float4*>(p.ws_o + ((size_t)row * n * 2 + c) * DVD) + lane;
-#pragma unroll 4
-        for (int s_ = warp; s_ < n; s_ += CWARPS) {
-            const float wv = wgt[c][s_];
-            const float4 o = op[(size_t)s_ * 2 * (DVD / 4)];
-            acc.x = fmaf(o.x, wv, acc.x);
-            acc.y = fmaf(o.y, wv, acc.y);
-            acc.z = fmaf(o.z, wv, acc.z);
-            acc.w = fmaf(o.w, wv, acc.w);
+        for (int u = 0; u < SPLITS_PER_ROUND; ++u) {
+            const int sp = s0 + u;
+            if (sp < n) {
+                mlv[u] = reinterpret_cast<const float4*>(ml)[sp];
+                ov[u][0] = op[(size_t)sp * 2 * (DVD / 4)];
+                ov[u][1] = op[(size_t)sp * 2 * (DVD / 4) + DVD / 4];
+            } else {
+                mlv[u] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+                ov[u][0] = ov[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        reinterpret_cast<float4*>(part[warp][c])[lane] = acc;
-    }
-    __syncthreads();
-    float dval = 0.f;
-    if (tid < DVD) {
-        float o[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            float acc = 0.f;
+            float m = M[c];
 #pragma unroll
-            for (int w = 0; w < CWARPS; ++w) acc += part[w][c][tid];
-            o[c] = acc / lsum[c];
+            for (int u = 0; u < SPLITS_PER_ROUND; ++u) m = fmaxf(m, c ? mlv[u].z : mlv[u].x);
+            if (m == -INFINITY) continue;  // no visible key so far
+            if (M[c] != -INFINITY && M[c] != m) {
+                const float r = exp2f(M[c] - m);
+                lsum[c] *= r;
+                acc[c].x *= r;
+                acc[c].y *= r;
+                acc[c].z *= r;
+                acc[c].w *= r;
+            }
+#pragma unroll
+            for (int u = 0; u < SPLITS_PER_ROUND; ++u) {
+                const float ms = c ? mlv[u].z : mlv[u].x, ls = c ? mlv[u].w : mlv[u].y;
+                const float w = ms == -INFINITY ? 0.f : exp2f(ms - m);  // empty splits weigh nothing
+                lsum[c] = fmaf(ls, w, lsum[c]);
+                acc[c].x = fmaf(ov[u][c].x, w, acc[c].x);
+                acc[c].y = fmaf(ov[u][c].y, w, acc[c].y);
+                acc[c].z = fmaf(ov[u][c].z, w, acc[c].z);
+                acc[c].w = fmaf(ov[u][c].w, w, acc[c].w);
+            }
+            M[c] = m;
         }
-        const float lam = p.lambda[h * p.lambda_stride];
-        dval = o[0] - lam * o[1];
-        const float ss = warp_sum(dval * dval);
-        if (lane == 0) red[warp] = ss;
     }
-    __syncthreads();
-    if (tid < DVD) {
-        const float ss = red[0] + red[1] + red[2] + red[3];
-        const float rinv = 1.f / sqrtf(ss / (float)DVD + p.eps);
-        const float y = dval * rinv * p.subln_w[tid] * (1.f - p.lambda_init);
-        static_cast<__nv_bfloat16*>(p.out)[(size_t)row * DVD + tid] = __float2bfloat16_rn(y);
-    }
+    const float i1 = 1.f / lsum[0], i2 = 1.f / lsum[1];  // every row sees at least one key
+    const float lam = p.lambda[h * p.lambda_stride];
+    const float4 d = make_float4(acc[0].x * i1 - lam * (acc[1].x * i2), acc[0].y * i1 - lam * (acc[1].y * i2),
+                                 acc[0].z * i1 - lam * (acc[1].z * i2), acc[0].w * i1 - lam * (acc[1].w * i2));
+    const float ss = warp_sum(d.x * d.x + d.y * d.y + d.z * d.z + d.w * d.w);
+    const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DVD + p.eps);
+    const float4 w = reinterpret_cast<const float4*>(p.subln_w)[lane];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(d.x * post * w.x, d.y * post * w.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(d.z * post * w.z, d.w * post * w.w);
+    uint2 u2;
+    u2.x = *reinterpret_cast<uint32_t*>(&lo);
+    u2.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)row * DVD)[lane] = u2;
 }
 
 }  // namespace
@@ -128,7 +117,8 @@ cudaError_t launch_decode(const KvParams& p, const KvTensorMaps& maps, cudaStrea
     cudaError_t err = launch_decode_tc(p, maps, stream);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.batch * p.q_len * p.H));
+    const long long rows = (long long)p.batch * p.q_len * p.H;
+    cfg.gridDim = dim3((unsigned)((rows + CWARPS - 1) / CWARPS));
     cfg.blockDim = dim3(32 * CWARPS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
