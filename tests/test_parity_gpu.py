@@ -89,6 +89,18 @@ def test_bf16_packed(lens):
     compare(run_gpu(inp), oracle_out(inp), "bf16")
 
 
+def test_bf16_many_short_packed_sequences():
+    # 2000 packed sequences of 1..48 tokens: the one-item-per-CTA kernel (more than
+    # 64 packed sequences), with the sequences along the grid's slowest dimension.
+    # This seed's lambda is 0.937, so among the 780k rows some nearly cancel
+    # (kappa up to 24): each row's max-abs bound scales with its kappa
+    lens = np.random.default_rng(17).integers(1, 49, 2000).tolist()
+    inp = W.generate(BF, seed=17, seq_lens=lens)
+    lam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2,
+                            orc.lambda_init(inp.wl.depth))
+    compare(run_gpu(inp), oracle_out(inp), "bf16", kappa=row_condition(inp, lam))
+
+
 @pytest.mark.parametrize("T", [1, 100, 300])
 def test_bf16_non_causal(T):
     inp = W.generate(W.with_overrides(BF, causal=False), seed=5, seq_lens=[T, 77])
