@@ -31,7 +31,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Block (x, h): rows t = x * 64 .. x * 64 + 63 of head h; warp w takes 8 of them,
 // lane l owns value columns 4l .. 4l+3. The norm-weight and lambda gradients are
 // summed over the block before one set of atomics.
-__global__ void __launch_bounds__(32 * WARPS)
+__global__ void __launch_bounds__(32 * WARPS, 2)  // two blocks an SM: 16 warps' loads in flight
 diffattn_bwd_pre_kernel(const BwdPreParams p) {
     __shared__ float s_dw[WARPS][DVD];
     __shared__ float s_dl[WARPS];
@@ -44,6 +44,11 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = p.subln_w[4 * lane + i];
     float dy[ROWS_PER_WARP][4], o1[ROWS_PER_WARP][4], o2[ROWS_PER_WARP][4];
+    // lane r < ROWS_PER_WARP fetches row r's (lse_1, lse_2) with the other loads, so
+    // no row waits on a load of its own
+    float2 lse_r = make_float2(0.f, 0.f);
+    if (lane < ROWS_PER_WARP && t0 + lane < p.tokens)
+        lse_r = reinterpret_cast<const float2*>(p.lse)[(size_t)(t0 + lane) * p.H + h];
 #pragma unroll
     for (int r = 0; r < ROWS_PER_WARP; ++r) {
         const int t = t0 + r;
@@ -90,6 +95,7 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
         }
         d1 = warp_sum(d1);
         d2 = warp_sum(d2);
+        const float lse1 = __shfl_sync(0xffffffffu, lse_r.x, r), lse2 = __shfl_sync(0xffffffffu, lse_r.y, r);
         if (t < p.tokens) {
             dlam -= d2;
             const size_t row = (size_t)t * p.H + h;
@@ -99,10 +105,8 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
             st.x = *reinterpret_cast<uint32_t*>(&lo2);
             st.y = *reinterpret_cast<uint32_t*>(&hi2);
             reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
-            if (lane == 0) {
-                const float2 l2 = reinterpret_cast<const float2*>(p.lse)[row];
-                reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(l2.x, l2.y, d1, d2);
-            }
+            if (lane == 0)
+                reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(lse1, lse2, d1, d2);
         }
     }
 #pragma unroll
