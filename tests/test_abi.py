@@ -168,3 +168,21 @@ def test_rope_tables_reject_on_host(lib):
     assert lib.diffattn_rope_tables(10000.0, 8, 63, vp(FAKE), vp(FAKE), None) == 1
     assert lib.diffattn_rope_tables(-1.0, 8, 64, vp(FAKE), vp(FAKE), None) == 1
     assert lib.diffattn_rope_tables(10000.0, 8, 64, None, vp(FAKE), None) == 1
+
+
+def test_cache_forward_split_plan(lib):
+    # The library-planned split count of the cache forward, seen through the
+    # workspace it needs: B q_len H splits (m, l, O of both components) in fp32.
+    # The plan takes the fewest waves of resident split CTAs (2 per SM; the
+    # library assumes 152 SMs when no GPU answers) whose last wave is at least
+    # 80 % full: 8 sequences x 4 kv heads -> 9 splits (288 CTAs of 304 slots);
+    # 16 x 4 -> 4 splits (256 of 304); a forced count is taken as given.
+    def ws(batch, q_len, cap, H=16, Hkv=4, splits=0):
+        d = _lib.DiffAttnKvDesc(batch=batch, q_len=q_len, cache_capacity=cap, num_heads=H, num_kv_heads=Hkv,
+                                d=64, dv=128, dtype=_lib.DTYPE_BF16, eps=1e-5, num_splits=splits)
+        return lib.diffattn_fwd_kvcache_workspace_size(ctypes.byref(d))
+    per_split = lambda batch, q_len, H=16: batch * q_len * H * 2 * (128 + 2) * 4  # noqa: E731
+    assert ws(8, 1, 16384) == 9 * per_split(8, 1)
+    assert ws(16, 4, 8192) == 4 * per_split(16, 4)
+    assert ws(16, 4, 8192, splits=7) == 7 * per_split(16, 4)
+    assert ws(0, 1, 16384) == 0
