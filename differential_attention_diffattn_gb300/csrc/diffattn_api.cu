@@ -4,11 +4,23 @@
 #include <cstdint>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/diffattn.h"
 #include "internal.h"
 
 namespace diffattn {
 namespace {
+
+// An NVTX range over one call of the ABI, so that a profiler's timeline shows each
+// call (and the launches it makes) under the entry point's name; with no tool
+// attached a push or pop is a check of one function pointer.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 // Error bits written by kernels; one word per device (a module variable of
 // this library, so nothing is allocated for it).
@@ -186,6 +198,7 @@ float diffattn_lambda_init(int depth) {
 
 diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int n_sets,
                                 int d, float lambda_init, float* lambda_out, void* stream) {
+    const CallRange nvtx_range("diffattn_lambda");
     if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out) return DIFFATTN_ERR_INVALID_ARG;
     if (n_sets < 1 || d < 1 || d > 1024) return DIFFATTN_ERR_INVALID_ARG;
     if (launch_lambda(lq1, lk1, lq2, lk2, n_sets, d, lambda_init, lambda_out,
@@ -307,6 +320,7 @@ const char* diffattn_fwd_kernel(const diffattn_desc* desc, int packed) {
 diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
                              const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
                              int causal, const int* cu_seqlens, void* out, void* stream) {
+    const CallRange nvtx_range("diffattn_fwd");
     return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
                       nullptr, nullptr, nullptr, stream);
 }
@@ -315,6 +329,7 @@ diffattn_status diffattn_fwd_train(const diffattn_desc* desc, const void* q, con
                                    const float* lambda, int lambda_per_head, float lambda_init,
                                    const float* subln_w, int causal, const int* cu_seqlens, void* out, float* lse,
                                    void* o1, void* o2, void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_train");
     if (!lse || !o1 || !o2) return DIFFATTN_ERR_INVALID_ARG;
     return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out, lse,
                       o1, o2, stream);
@@ -331,6 +346,7 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
                                      int lambda_per_head, float lambda_init, const float* subln_w, int causal,
                                      void* workspace, unsigned long long workspace_bytes, void* out,
                                      void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_kvcache");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_kv_desc& ds = *desc;
     int n_splits = 0, chunk = 0;
@@ -427,6 +443,7 @@ diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const
                                              const void* v_cache, const int* cache_seqlens, const float* lambda,
                                              int lambda_per_head, float lambda_init, const float* subln_w,
                                              int causal, void* out, void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_kvcache_noalloc");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const unsigned long long need = diffattn_fwd_kvcache_workspace_size(desc);
     if (need > DIFFATTN_NOALLOC_SCRATCH_BYTES) return DIFFATTN_ERR_UNSUPPORTED;
@@ -450,6 +467,7 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
                              int causal, const int* cu_seqlens, const void* dout, const float* lse, const void* o1,
                              const void* o2, void* dq, void* dk, void* dv, float* dlambda, float* dsubln_w,
                              void* workspace, unsigned long long workspace_bytes, void* stream) {
+    const CallRange nvtx_range("diffattn_bwd");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_desc& ds = *desc;
     if (ds.num_heads <= 0 || ds.num_kv_heads <= 0 || ds.num_heads % ds.num_kv_heads != 0 || ds.num_heads > 65535)
@@ -545,6 +563,7 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
 diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                     const float* dlambda, int n_sets, int d, float* dlq1, float* dlk1,
                                     float* dlq2, float* dlk2, void* stream) {
+    const CallRange nvtx_range("diffattn_lambda_bwd");
     if (!lq1 || !lk1 || !lq2 || !lk2 || !dlambda || !dlq1 || !dlk1 || !dlq2 || !dlk2) return DIFFATTN_ERR_INVALID_ARG;
     if (n_sets < 1 || d < 1 || d > 1024) return DIFFATTN_ERR_INVALID_ARG;
     return launch_lambda_bwd(lq1, lk1, lq2, lk2, dlambda, n_sets, d, dlq1, dlk1, dlq2, dlk2,
@@ -557,6 +576,7 @@ diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const fl
 
 diffattn_status diffattn_rope_tables(double theta, int n_pos, int rot_dim, float* cos_out, float* sin_out,
                                      void* stream) {
+    const CallRange nvtx_range("diffattn_rope_tables");
     if (!cos_out || !sin_out || n_pos < 1 || rot_dim < 2 || (rot_dim & 1) || !(theta > 0.0) || !std::isfinite(theta))
         return DIFFATTN_ERR_INVALID_ARG;
     return launch_rope_tables(theta, n_pos, rot_dim, cos_out, sin_out, static_cast<cudaStream_t>(stream)) ==
@@ -568,6 +588,7 @@ diffattn_status diffattn_rope_tables(double theta, int n_pos, int rot_dim, float
 diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* positions, const int* cu_seqlens,
                                  const float* cos_table, const float* sin_table, const void* q_in, void* q_out,
                                  const void* k_in, void* k_out, void* stream) {
+    const CallRange nvtx_range("diffattn_rope_qk");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_rope_desc& ds = *desc;
     if (ds.tokens < 0 || ds.num_heads < 1 || ds.num_kv_heads < 0 || ds.d < 4 || (ds.d % 4) != 0 || ds.n_pos < 1)
@@ -621,6 +642,7 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
 
 diffattn_status diffattn_out_proj(const diffattn_out_proj_desc* desc, const void* x, const void* w, void* y,
                                   void* stream) {
+    const CallRange nvtx_range("diffattn_out_proj");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_out_proj_desc& ds = *desc;
     if (ds.tokens < 0 || ds.in_features < 8 || ds.out_features < 8 || (ds.in_features % 8) != 0 ||
@@ -650,6 +672,7 @@ diffattn_status diffattn_out_proj(const diffattn_out_proj_desc* desc, const void
 diffattn_status diffattn_merge_partials(const diffattn_merge_desc* desc, const float* lse, const float* o1,
                                         const float* o2, const float* lambda, int lambda_per_head,
                                         float lambda_init, const float* subln_w, void* out, void* stream) {
+    const CallRange nvtx_range("diffattn_merge_partials");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_merge_desc& ds = *desc;
     if (ds.tokens < 0 || ds.num_heads < 1 || ds.dv < 4 || ds.dv > 512 || (ds.dv % 4) != 0 || ds.n_parts < 1)
