@@ -139,19 +139,37 @@ def test_bf16_large_scores():
 
 # -------------------------------------- persistent kernel (unpacked) ---
 
-@pytest.mark.parametrize("B,T,H,Hkv,causal", [(3, 1000, 16, 4, True), (5, 700, 12, 3, True),
-                                              (4, 2048, 16, 4, False), (12, 256, 16, 16, True)])
-def test_bf16_persistent_kernel(B, T, H, Hkv, causal):
+@pytest.mark.parametrize("B,T,H,Hkv,causal,per_head", [(3, 1000, 16, 4, True, False), (5, 700, 12, 3, True, False),
+                                                       (4, 2048, 16, 4, False, False), (12, 256, 16, 16, True, False),
+                                                       (4, 1000, 16, 4, True, True)])
+def test_bf16_persistent_kernel(B, T, H, Hkv, causal, per_head):
     """Unpacked batches with 2 to 10 (query tile, head, sequence) items per SM run
     on the persistent kernel: ragged last tiles, grouped kv heads, non-causal,
-    many short items."""
-    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, random_subln=True)
+    many short items, a lambda per head."""
+    wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, random_subln=True,
+                          lambda_per_head=per_head)
     inp = W.generate(wl, seed=B * 100 + T, seq_lens=[T] * B)
     sh = lambda x: x.cuda().view(B, T, *x.shape[1:])  # noqa: E731
     lam = torch.ones(1, dtype=torch.float32, device="cuda")
     assert da.diffattn_fwd_kernel(sh(inp.q), sh(inp.k), sh(inp.v), lam,
                                   inp.subln_w.cuda()) == "diffattn_fwd_bf16_persistent_kernel"
     compare(run_gpu(inp, packed=False), oracle_out(inp), "bf16")
+
+
+def test_bf16_persistent_kernel_longest_items_sampled():
+    """2 x 8192 tokens (items of up to 64 key tiles, the longest the persistent
+    kernel takes), 16 / 4 heads, against the oracle on sampled rows."""
+    B, T = 2, 8192
+    wl = W.with_overrides(W.WORKLOADS["llama1b_b4_t2048"], random_subln=True)
+    inp = W.generate(wl, seed=91, seq_lens=[T] * B)
+    sh = lambda x: x.cuda().view(B, T, *x.shape[1:])  # noqa: E731
+    lam = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert da.diffattn_fwd_kernel(sh(inp.q), sh(inp.k), sh(inp.v), lam,
+                                  inp.subln_w.cuda()) == "diffattn_fwd_bf16_persistent_kernel"
+    got = run_gpu(inp, packed=False)
+    assert torch.isfinite(got.float()).all()
+    tt, hh = sample_rows(inp, every=97)
+    compare(got[torch.as_tensor(tt).long(), torch.as_tensor(hh).long()], oracle_out(inp, rows=(tt, hh)), "bf16")
 
 
 @pytest.mark.parametrize("d,lens", [(16, [64, 3]), (32, [100]), (64, [70, 1])])
