@@ -105,11 +105,13 @@ def test_training_outputs_match_oracle(lens, kernel):
                 assert abs(float(lse[t, h, c]) - want) < 1e-3
 
 
+# the last case's training forward runs on the persistent kernel (384 items)
 @pytest.mark.parametrize("lens,H,Hkv,causal,per_head", [
     ([256], 16, 4, True, False),
     ([300, 129, 1], 8, 2, True, True),
     ([200], 4, 4, False, False),
     ([513], 16, 16, True, False),
+    ([300, 129, 200, 1, 256, 77, 300, 150], 16, 4, True, False),
 ])
 def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
     wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, lambda_per_head=per_head,
