@@ -141,7 +141,7 @@ def test_bf16_large_scores():
 
 @pytest.mark.parametrize("B,T,H,Hkv,causal,per_head", [(3, 1000, 16, 4, True, False), (5, 700, 12, 3, True, False),
                                                        (4, 2048, 16, 4, False, False), (12, 256, 16, 16, True, False),
-                                                       (4, 1000, 16, 4, True, True)])
+                                                       (4, 1000, 16, 4, True, True), (64, 130, 16, 4, True, False)])
 def test_bf16_persistent_kernel(B, T, H, Hkv, causal, per_head):
     """Unpacked batches with 2 to 10 (query tile, head, sequence) items per SM run
     on the persistent kernel: ragged last tiles, grouped kv heads, non-causal,
