@@ -110,7 +110,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_status_string.argtypes = [ctypes.c_int]
         lib.diffattn_set_wait_timeout_ns.restype = None
         lib.diffattn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
-        lib.diffattn_set_fault_injection.restype = None
+        lib.diffattn_set_fault_injection.restype = ctypes.c_int
         lib.diffattn_set_fault_injection.argtypes = [ctypes.c_int]
         lib.diffattn_rope_tables.restype = ctypes.c_int
         lib.diffattn_rope_tables.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp, vp]
@@ -477,7 +477,11 @@ def diffattn_set_wait_timeout_ns(ns: int) -> None:
 
 
 def diffattn_set_fault_injection(mode: int) -> None:
-    load_library().diffattn_set_fault_injection(int(mode))
+    """Test hook of the failure-detection tests; the library honours it only in
+    a process whose environment holds DIFFATTN_TEST_HOOKS=1."""
+    st = load_library().diffattn_set_fault_injection(int(mode))
+    if st != 0 and int(mode) != 0:
+        raise DiffAttnError(st, "diffattn_set_fault_injection")
 
 
 # ------------------------------------------------------------- rotary ---

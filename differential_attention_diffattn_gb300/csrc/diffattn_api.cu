@@ -2,6 +2,8 @@
 // the per-device error word, TMA descriptor encoding and kernel dispatch.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include <nvtx3/nvToolsExt.h>
@@ -184,6 +186,24 @@ unsigned long long kv_workspace_bytes(const diffattn_kv_desc& d, int n_splits) {
     return o + rows * 2 * 4;
 }
 
+// The cache forward's checks of the descriptor alone (no pointers): the split
+// plan, sizes and limits (INVALID_ARG), then what the kernels support
+// (UNSUPPORTED). On success the split count and chunk are set.
+diffattn_status kv_check_desc(const diffattn_kv_desc& ds, float lambda_init, int* n_splits, int* chunk) {
+    if (!kv_plan(ds, n_splits, chunk)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.d <= 0 || ds.dv != 2 * ds.d) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
+    if ((long long)ds.batch * ds.cache_capacity * ds.num_kv_heads * ds.dv >= (1LL << 40) ||
+        (long long)ds.batch * ds.cache_capacity > INT32_MAX - 64 ||
+        (long long)ds.batch * ds.q_len * ds.num_heads > INT32_MAX || ds.batch > 65535 || ds.num_kv_heads > 65535)
+        return DIFFATTN_ERR_INVALID_ARG;
+    const int rows = ds.q_len * (ds.num_heads / ds.num_kv_heads);
+    if (ds.dtype != DIFFATTN_DTYPE_BF16 || ds.d != 64 || !decode_rows_supported(rows))
+        return DIFFATTN_ERR_UNSUPPORTED;
+    return DIFFATTN_OK;
+}
+
 }  // namespace
 }  // namespace diffattn
 
@@ -350,17 +370,8 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_kv_desc& ds = *desc;
     int n_splits = 0, chunk = 0;
-    if (!kv_plan(ds, &n_splits, &chunk)) return DIFFATTN_ERR_INVALID_ARG;
-    if (ds.d <= 0 || ds.dv != 2 * ds.d) return DIFFATTN_ERR_INVALID_ARG;
-    if (!(ds.eps >= 0.f) || !std::isfinite(ds.eps) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
-    if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
-    if ((long long)ds.batch * ds.cache_capacity * ds.num_kv_heads * ds.dv >= (1LL << 40) ||
-        (long long)ds.batch * ds.cache_capacity > INT32_MAX - 64 ||
-        (long long)ds.batch * ds.q_len * ds.num_heads > INT32_MAX || ds.batch > 65535 || ds.num_kv_heads > 65535)
-        return DIFFATTN_ERR_INVALID_ARG;
-    const int rows = ds.q_len * (ds.num_heads / ds.num_kv_heads);
-    if (ds.dtype != DIFFATTN_DTYPE_BF16 || ds.d != 64 || !decode_rows_supported(rows))
-        return DIFFATTN_ERR_UNSUPPORTED;
+    const diffattn_status desc_st = kv_check_desc(ds, lambda_init, &n_splits, &chunk);
+    if (desc_st != DIFFATTN_OK) return desc_st;
     if (ds.batch == 0) return DIFFATTN_OK;
     if (!q || !k_cache || !v_cache || !lambda || !subln_w || !out || !workspace) return DIFFATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
@@ -445,13 +456,26 @@ diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const
                                              int causal, void* out, void* stream) {
     const CallRange nvtx_range("diffattn_fwd_kvcache_noalloc");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
-    const unsigned long long need = diffattn_fwd_kvcache_workspace_size(desc);
-    if (need > DIFFATTN_NOALLOC_SCRATCH_BYTES) return DIFFATTN_ERR_UNSUPPORTED;
+    // The descriptor is checked first, so that a bad one gives the same status as
+    // diffattn_fwd_kvcache rather than a size rejection.
+    diffattn_kv_desc ds = *desc;
+    int n_splits = 0, chunk = 0;
+    const diffattn_status desc_st = kv_check_desc(ds, lambda_init, &n_splits, &chunk);
+    if (desc_st != DIFFATTN_OK) return desc_st;
+    // With the automatic plan, fewer key splits are taken when the planned ones'
+    // partials would not fit the array; a forced split count is kept as given.
+    if (ds.num_splits == 0) {
+        for (int n = n_splits; n >= 1 && kv_workspace_bytes(ds, n_splits) > DIFFATTN_NOALLOC_SCRATCH_BYTES; --n) {
+            ds.num_splits = n;
+            if (kv_check_desc(ds, lambda_init, &n_splits, &chunk) != DIFFATTN_OK) return DIFFATTN_ERR_INVALID_ARG;
+        }
+    }
+    if (kv_workspace_bytes(ds, n_splits) > DIFFATTN_NOALLOC_SCRATCH_BYTES) return DIFFATTN_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    if (need > 0 && desc->batch > 0) {
+    if (ds.batch > 0) {
         if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     }
-    return diffattn_fwd_kvcache(desc, q, k_cache, v_cache, cache_seqlens, lambda, lambda_per_head, lambda_init,
+    return diffattn_fwd_kvcache(&ds, q, k_cache, v_cache, cache_seqlens, lambda, lambda_per_head, lambda_init,
                                 subln_w, causal, scratch, DIFFATTN_NOALLOC_SCRATCH_BYTES, out, stream);
 }
 
@@ -732,6 +756,16 @@ const char* diffattn_status_string(diffattn_status s) {
 
 void diffattn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns ? ns : kDefaultWaitTimeoutNs; }
 
-void diffattn_set_fault_injection(int mode) { g_inject = (mode == 1 || mode == 2) ? mode : 0; }
+diffattn_status diffattn_set_fault_injection(int mode) {
+    // A test hook: it takes effect only in a process that asks for test hooks.
+    const char* on = std::getenv("DIFFATTN_TEST_HOOKS");
+    if (on == nullptr || std::strcmp(on, "1") != 0) {
+        g_inject = 0;
+        return DIFFATTN_ERR_UNSUPPORTED;
+    }
+    if (mode < 0 || mode > 2) return DIFFATTN_ERR_INVALID_ARG;
+    g_inject = mode;
+    return DIFFATTN_OK;
+}
 
 }  // extern "C"

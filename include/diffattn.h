@@ -292,10 +292,13 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
  * calls that overlap on the GPU (different streams, or different host threads)
  * race on it and must be serialised by the caller. Nothing in the array has to
  * start at zero: each call writes every partial it later reads.
- * Errors: as diffattn_fwd_kvcache, plus DIFFATTN_ERR_UNSUPPORTED when the shape
- * needs more than DIFFATTN_NOALLOC_SCRATCH_BYTES of partials (see
- * diffattn_fwd_kvcache_workspace_size; fewer key splits need less), and
- * DIFFATTN_ERR_CUDA if the address lookup fails.
+ * With desc->num_splits == 0 the automatic split plan is lowered, one split at
+ * a time, until the partials fit the array; a caller-forced count is kept.
+ * Errors: the descriptor is checked first and gives the statuses of
+ * diffattn_fwd_kvcache; then DIFFATTN_ERR_UNSUPPORTED when even the lowest
+ * split count (or the forced one) needs more than DIFFATTN_NOALLOC_SCRATCH_BYTES
+ * of partials (see diffattn_fwd_kvcache_workspace_size), and DIFFATTN_ERR_CUDA
+ * if the address lookup fails.
  */
 diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
                                              const void* v_cache, const int* cache_seqlens, const float* lambda,
@@ -424,14 +427,16 @@ diffattn_status diffattn_get_device_status(void* stream);
 const char* diffattn_status_string(diffattn_status status);
 
 /*
- * Test hook (no paper counterpart): sets the limit, in nanoseconds, after
+ * Library setting (no paper counterpart): the limit, in nanoseconds, after
  * which a kernel pipeline wait gives up and records DIFFATTN_ERR_TIMEOUT.
  * 0 restores the default (2 s). Affects launches made after the call.
  */
 void diffattn_set_wait_timeout_ns(unsigned long long ns);
 
 /*
- * Test hook (no paper counterpart) for failure detection. mode 1: the copy
+ * TEST ONLY: not part of the library's interface for callers, and off unless
+ * the process environment holds DIFFATTN_TEST_HOOKS=1 when it is called.
+ * Hook (no paper counterpart) for the failure-detection tests. mode 1: the copy
  * producer of the bf16 forward kernel issues no loads, so the barriers every
  * other role waits on are never armed; each wait runs out after the wait limit,
  * the kernel records DIFFATTN_ERR_TIMEOUT, frees its tensor memory and returns,
@@ -440,8 +445,10 @@ void diffattn_set_wait_timeout_ns(unsigned long long ns);
  * item, so that the softmax warps run ahead of it; the results and the status
  * must not change. mode 0 (the default) turns it off. Affects launches made
  * after the call; nothing faults, traps or hangs.
+ * Returns DIFFATTN_OK; DIFFATTN_ERR_UNSUPPORTED (injection left off) when
+ * DIFFATTN_TEST_HOOKS=1 is not set; DIFFATTN_ERR_INVALID_ARG for another mode.
  */
-void diffattn_set_fault_injection(int mode);
+diffattn_status diffattn_set_fault_injection(int mode);
 
 #ifdef __cplusplus
 }

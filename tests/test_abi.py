@@ -186,3 +186,33 @@ def test_cache_forward_split_plan(lib):
     assert ws(16, 4, 8192) == 4 * per_split(16, 4)
     assert ws(16, 4, 8192, splits=7) == 7 * per_split(16, 4)
     assert ws(0, 1, 16384) == 0
+
+
+def test_noalloc_cache_forward_checks_the_descriptor_first(lib):
+    # A descriptor that diffattn_fwd_kvcache rejects as INVALID_ARG gets the same
+    # status from the allocation-free entry, not a size rejection: a negative dv
+    # would otherwise wrap the unsigned partials size to a huge number.
+    vp = ctypes.c_void_p
+
+    def call(**kw):
+        base = dict(batch=4, q_len=1, cache_capacity=4096, num_heads=16, num_kv_heads=4, d=64, dv=128,
+                    dtype=_lib.DTYPE_BF16, eps=1e-5, num_splits=0)
+        base.update(kw)
+        d = _lib.DiffAttnKvDesc(**base)
+        return lib.diffattn_fwd_kvcache_noalloc(ctypes.byref(d), vp(FAKE), vp(FAKE), vp(FAKE), None, vp(FAKE), 0,
+                                                0.2, vp(FAKE), 1, vp(FAKE), None)
+    assert call(dv=-128) == 1
+    assert call(dv=-128, batch=1 << 20) == 1
+    assert call(batch=70000) == 1       # above the batch limit
+    assert call(num_heads=15) == 1      # heads not a multiple of kv heads
+    assert call(d=32, dv=64) == 2       # valid, but no kernel for d = 32
+
+
+def test_fault_injection_hook_is_off_without_the_test_environment(lib, monkeypatch):
+    monkeypatch.delenv("DIFFATTN_TEST_HOOKS", raising=False)
+    assert lib.diffattn_set_fault_injection(1) == 2   # UNSUPPORTED: left off
+    assert lib.diffattn_set_fault_injection(0) == 2
+    monkeypatch.setenv("DIFFATTN_TEST_HOOKS", "1")
+    assert lib.diffattn_set_fault_injection(3) == 1   # no such mode
+    assert lib.diffattn_set_fault_injection(1) == 0
+    assert lib.diffattn_set_fault_injection(0) == 0

@@ -6,6 +6,8 @@ wait limit each CTA gives up, records DIFFATTN_ERR_TIMEOUT, frees its tensor
 memory and returns; the host reads the status, and the next normal call on the
 same context is correct.
 """
+import os
+
 import pytest
 import torch
 
@@ -22,9 +24,15 @@ def _lib():
     da.build()
     da.load_library()
     torch.cuda.set_device(0)
+    prev = os.environ.get("DIFFATTN_TEST_HOOKS")
+    os.environ["DIFFATTN_TEST_HOOKS"] = "1"  # the library honours its test hook only with this set
     yield
     da.diffattn_set_fault_injection(0)
     da.diffattn_set_wait_timeout_ns(0)
+    if prev is None:
+        del os.environ["DIFFATTN_TEST_HOOKS"]
+    else:
+        os.environ["DIFFATTN_TEST_HOOKS"] = prev
 
 
 # packed: the one-item-per-CTA kernel; an unpacked batch of 3 x 1000 tokens

@@ -63,3 +63,18 @@ def test_noalloc_rejects_shapes_beyond_the_array():
                                                         fake, 1, fake, None)
     assert st == 2  # DIFFATTN_ERR_UNSUPPORTED
     del wl
+
+
+def test_noalloc_takes_fewer_splits_when_the_planned_ones_do_not_fit():
+    # 50 sequences x 4 kv heads = 200 split groups: on 152 SMs (two split CTAs
+    # each) the automatic plan takes 3 splits, whose partials (about 20 MB) exceed
+    # the array; the allocation-free entry takes 2 instead of rejecting the shape.
+    wl = W.KvWorkload("n", num_heads=16, num_kv_heads=4, d=64, dv=128, depth=12, batch=50, q_len=8,
+                      capacity=1024)
+    inp = W.generate_kv(wl, seed=63)
+    desc = _lib.kv_desc(inp.q, inp.k_cache, inp.v_cache)
+    if da.diffattn_fwd_kvcache_workspace_size(desc) <= (16 << 20):
+        pytest.skip("on this device the automatic plan already fits the array")
+    for _ in range(2):
+        got, ref = _run_both(inp)
+        compare(got, ref.double().cpu().numpy(), "bf16")
