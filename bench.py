@@ -12,6 +12,12 @@ one rank per GPU under torchrun, each on its own copy of the workload (weak
 scaling, no data-path collective); `value` is all ranks' flop over the
 slowest rank's time. `--impl reference` times the fp64 CPU oracle on bounded
 row samples of the same workload (rank 0 only).
+
+The default run (one GPU, no workload flags) also measures, after the headline
+line's timed region, the other forward workloads (`per_config`) and the rows
+beyond the forward (`next`: cache forward, backward, rotary embedding, o_proj,
+context-parallel merge), each with its own clock record; `--no-extras` skips
+them.
 """
 from __future__ import annotations
 
@@ -173,8 +179,12 @@ def run_ours(args, rank, world, local_rank):
     inp = W.generate(wl, seed=args.seed)
     tokens = inp.tokens
     pairs = causal_pairs(inp.seq_lens, wl.num_heads)
-    flops_step = FLOP_PER_PAIR * pairs
+    flop_per_pair = 4 * (wl.d + wl.dv)  # 768 at d = 64, dv = 128
+    flops_step = flop_per_pair * pairs
     packed = wl.varlen
+    # algorithmic bytes of the forward: q, k, v read once, out written once
+    alg_bytes = (inp.q.numel() + inp.k.numel() + inp.v.numel()) * inp.q.element_size() + \
+        tokens * wl.num_heads * wl.dv * inp.q.element_size()
     li = da.diffattn_lambda_init(wl.depth)
     stream = torch.cuda.current_stream()
 
@@ -405,7 +415,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "batch": len(inp.seq_lens) if not packed else None,
                    "seq_len": inp.max_seqlen, "tokens": tokens, "diff_heads": wl.num_heads,
                    "kv_heads": wl.num_kv_heads, "d": wl.d, "dv": wl.dv, "depth": wl.depth,
-                   "causal": wl.causal, "flop_per_pair": FLOP_PER_PAIR, "flop_per_step": step_flops,
+                   "causal": wl.causal, "flop_per_pair": flop_per_pair, "flop_per_step": step_flops,
                    "l2": (f"L2 flushed before every step (256 MB memset outside the step events; two rotating "
                           f"{set_bytes / 2**20:.0f} MB input/output sets)") if flush is not None else
                          f"inputs larger than L2: two rotating {set_bytes / 2**20:.0f} MB input/output sets",
@@ -419,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
         "other_flop_counts": {
             "tflops_t2_over_2_pairs": round(value * sum(L * L / 2 for L in inp.seq_lens) /
                                             sum(L * (L + 1) / 2 for L in inp.seq_lens), 2),
-            "tflops_512_per_pair": round(value * 512 / FLOP_PER_PAIR, 2)} if not args.out_proj else None,
+            "tflops_512_per_pair": round(value * 512 / flop_per_pair, 2)} if not args.out_proj else None,
         "tokens_per_s": round(tokens * world * args.steps / (elapsed_ms * 1e-3), 1),
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -431,7 +441,10 @@ def run_ours(args, rank, world, local_rank):
                      "frac_of_clock_peak": (round(achieved / clock_peak_tflops(clocks), 4)
                                             if clock_peak_tflops(clocks) else None),
                      "kernel": kernel_name, "launch_ms": round(fwd_ms, 4),
-                     "algorithmic_flop_per_launch": flops_step},
+                     "algorithmic_flop_per_launch": flops_step,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "hbm_gbs": round(alg_bytes / (fwd_ms * 1e-3) / 1e9, 1),
+                     "frac_of_hbm": round(alg_bytes / (fwd_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4)},
         "clocks": clocks,
         **({"warm": warm} if warm is not None else {}),
         "gpu_launches": (2 + (rope is not None) + bool(args.out_proj)) * args.steps,
@@ -863,6 +876,91 @@ def run_ours_kv(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------- every workload in one run (GPU) ---
+
+# The other configurations of the forward (parity workloads of the same method)
+# and the rows beyond it, each measured in the default run so that one command
+# records every figure with its clocks.
+EXTRA_FWD = ("tiny_f32", "b2_t512_gqa", "llama1b_b4_t2048", "varlen_32k")
+
+
+def run_extras(args, local_rank):
+    import torch
+
+    def sub(**over):
+        a = argparse.Namespace(**vars(args))
+        a.steps, a.warmup, a.e2e_steps = args.extra_steps, max(3, min(args.warmup, 5)), 3
+        a.no_cpu_baseline, a.rope, a.out_proj, a.backward, a.cp = True, None, False, False, 0
+        for k, v in over.items():
+            setattr(a, k, v)
+        return a
+
+    def guarded(fn):
+        try:
+            return fn()
+        except Exception as e:  # recorded in the line, not hidden
+            log(f"extra measurement failed: {e!r}")
+            return {"error": repr(e)[:300]}
+        finally:
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+
+    per_config = {}
+    for name in EXTRA_FWD:
+        def one(name=name):
+            ln = run_ours(sub(workload=name), 0, 1, local_rank)
+            rf = ln["roofline"]
+            d = {"kernel": rf["kernel"], "ms_per_step": ln["ms_per_step"], "tflops_per_step": ln["value"],
+                 "tokens_per_s": ln["tokens_per_s"], "launch_ms": rf["launch_ms"], "kernel_tflops": rf["achieved"],
+                 "frac_of_bf16_peak": rf["frac"], "hbm_gbs": rf["hbm_gbs"], "frac_of_hbm": rf["frac_of_hbm"],
+                 "flop_per_step": ln["config"]["flop_per_step"], "l2": ln["config"]["l2"],
+                 "e2e": ln["e2e"], "clocks": ln["clocks"], "steps": ln["steps"]}
+            if "warm" in ln:
+                d["warm"] = ln["warm"]
+            if name == "tiny_f32":
+                d["note"] = "fp32 parity path on the CUDA cores: a latency figure, not a tensor-core rate"
+            if name == "b2_t512_gqa":
+                d["bound"] = "latency (neither roof): HBM GB/s reported"
+            return d
+        per_config[name] = guarded(one)
+
+    nxt = {}
+
+    def kv(name):
+        ln = run_ours_kv(sub(workload=name), 0, 1, local_rank)
+        return {"gbs_per_step": ln["value"], "call_ms": ln["roofline"]["launch_ms"],
+                "call_gbs": ln["roofline"]["achieved"], "frac_of_hbm": ln["roofline"]["frac"],
+                "bytes_per_step": ln["config"]["bytes_per_step"], "e2e": ln["e2e"], "clocks": ln["clocks"]}
+    for name in ("decode_b8_c16384", "decode_b16_q4_ragged"):
+        nxt[name] = guarded(lambda name=name: kv(name))
+
+    def bwd():
+        ln = run_ours_bwd(sub(workload=WORKLOAD), 0, 1, local_rank)
+        rf = ln["roofline"]
+        return {"workload": WORKLOAD, "bwd_ms": rf["launch_ms"], "bwd_tflops": rf["achieved"],
+                "frac_of_bf16_peak": rf["frac"], "train_step_tflops": ln["value"], "fwd_train": ln["fwd_train"],
+                "flop_per_pair": "768 forward + 1280 backward (algorithmic)", "clocks": ln["clocks"]}
+    nxt["backward"] = guarded(bwd)
+
+    def rope(placement):
+        ln = run_ours(sub(workload=WORKLOAD, rope=placement), 0, 1, local_rank)
+        return dict(ln["rope"], step_tflops=ln["value"], attention_launch_ms=ln["roofline"]["launch_ms"],
+                    clocks=ln["clocks"])
+    for pl in sorted(ROPE_PLACEMENTS):
+        nxt[f"rope_{pl}"] = guarded(lambda pl=pl: rope(pl))
+
+    def proj():
+        ln = run_ours(sub(workload=WORKLOAD, out_proj=True), 0, 1, local_rank)
+        return dict(ln["out_proj"], step_tflops=ln["value"], clocks=ln["clocks"])
+    nxt["o_proj"] = guarded(proj)
+
+    def cp2():
+        ln = run_ours_cp(sub(workload=WORKLOAD, cp=2), 0, 1, local_rank)
+        return dict(ln["merge"], step_tflops=ln["value"], cp_ranks=2, emulated_on_one_gpu=True, clocks=ln["clocks"])
+    nxt["cp_merge"] = guarded(cp2)
+    return per_config, nxt
+
+
 # --------------------------------------------------------- CPU / oracle ---
 
 def oracle_sample(inp, positions):
@@ -966,6 +1064,9 @@ def main():
                     help="context-parallel split of one sequence over N ranks (emulated on one GPU when run alone)")
     ap.add_argument("--rope", choices=sorted(ROPE_PLACEMENTS), default=None,
                     help="rotate q, k (pre-rotary inputs) inside each step before the attention")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads and rows that the default run also measures")
+    ap.add_argument("--extra-steps", type=int, default=50, help="timed steps of each extra measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -995,6 +1096,10 @@ def main():
         else:
             runner = run_ours_bwd if args.backward else run_ours
         line = runner(args, rank, world, local_rank)
+        default_run = (runner is run_ours and args.workload == WORKLOAD and args.rope is None and
+                       not args.out_proj)
+        if line is not None and world == 1 and default_run and not args.no_extras:
+            line["per_config"], line["next"] = run_extras(args, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist
