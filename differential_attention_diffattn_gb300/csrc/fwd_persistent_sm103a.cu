@@ -20,19 +20,37 @@
 // 12 TMA producer; warp 13 TMEM allocator and MMA issuer; warps 14-15 idle. With
 // the epilogue in its own warpgroup the softmax warps go on to the next item as
 // soon as their last P is stored, and the epilogue of one item runs under the
-// next item's key tiles; it still has to read O before the next item's first
-// P V overwrites it. Sixteen warps leave 128 registers a thread at launch; the
-// warpgroups then move registers with setmaxnreg: softmax 168, epilogue 88,
-// producer / MMA 88 (8 x 32 x 168 + 4 x 32 x (88 + 88) = the 65,536 the launch
+// next item's key tiles. Sixteen warps leave 128 registers a thread at launch;
+// the warpgroups then move registers with setmaxnreg: softmax 168, epilogue 80,
+// producer / MMA 96 (8 x 32 x 168 + 4 x 32 x (80 + 96) = the 65,536 the launch
 // holds; each SM sub-partition runs two softmax warps, one epilogue warp and one
-// of warps 12-15: 2 x 168 + 88 + 88 = 512 registers a lane, its whole share).
+// of warps 12-15: 2 x 168 + 80 + 96 = 512 registers a lane, its whole share; the
+// MMA warp's one-item lookahead spilled at 88).
+//
+// Shared memory: two Q boxes (Q1 | Q2 of two items, so the next item's Q loads
+// while the current one runs), two K stages (K1 | K2) and two V stages with
+// their own barriers (a K stage is free once both score MMAs of its tile have
+// run, a V stage once both P V MMAs have: two stages each give the loads the
+// slack of a three-stage ring shared by K and V), and 32 KB where the epilogue
+// keeps half of each row's D. The epilogue reads O from tensor memory once: it
+// forms D = O1/l1 - lambda O2/l2, keeps it in shared memory in fp32 (columns
+// 0-63 in the 32 KB area, 64-127 in the item's own Q box, whose score MMAs have
+// all run), sums D^2, and releases O to the next item's first P V; a second
+// pass over the kept D normalises and stores. The item's Q box is released to
+// the producer after that pass.
+//
 // Barriers that advance once per item: item_full / item_empty (a four-slot ring
-// of items), q_full / q_empty (the Q box), stats_full[item parity] (1/l_c per
-// row from the softmax warps), o_full / o_empty (the O accumulators: an item's first P V
-// waits until the epilogue of the previous one has read them); once per key
-// tile over all items: the K / V ring, s_full, p_ready. Every wait is bounded;
-// the eight softmax warps decide together, at each item's start and end,
-// whether to go on, so that none is left waiting at a barrier another has left.
+// of items), q_full / q_empty per Q box, stats_full[item parity] (1/l_c per row
+// from the softmax warps), o_full / o_empty (the O accumulators: an item's first
+// P V waits until the epilogue of the previous one has read them); once per key
+// tile over all items: k_full / k_empty and v_full / v_empty per stage, s_full,
+// p_ready. The MMA warp looks one item ahead: the next item's first scores of
+// component 1 are issued right after the current item's last P V of component 1
+// (when that item's Q and keys have landed), as within an item, and the two
+// softmax warpgroups cross item boundaries each at its own pace (component 1 at
+// most one item and one tile ahead), keeping their stagger on the tensor pipe.
+// Every wait is an mbarrier wait, bounded and watching the CTA's abort flag, so
+// a role that gives up never leaves another waiting at a barrier it has left.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -41,19 +59,23 @@
 namespace diffattn {
 namespace {
 
-constexpr int BM = 128, BN = 128, HD = 64, DV = 128, STAGES = 3;
+constexpr int BM = 128, BN = 128, HD = 64, DV = 128, STAGES = 2, QBUF = 2;
 constexpr int NUM_THREADS = 512, EPI_WARP0 = 8, PRODUCER_WARP = 12, MMA_WARP = 13;
 constexpr int NSLOT = 4;  // item ring
 // registers a thread: at launch (65,536 / 512) and after the split
-constexpr int REG_LAUNCH = 128, REG_SOFTMAX = 168, REG_EPI = 88, REG_COPY = 88;
+constexpr int REG_LAUNCH = 128, REG_SOFTMAX = 168, REG_EPI = 80, REG_COPY = 96;
 constexpr int REG_NEED = 8 * 32 * REG_SOFTMAX + 4 * 32 * REG_EPI + 4 * 32 * REG_COPY;
 static_assert(REG_NEED <= NUM_THREADS * REG_LAUNCH, "the register split exceeds the launch's registers");
 static_assert(2 * REG_SOFTMAX + REG_EPI + REG_COPY <= 4 * REG_LAUNCH, "the split exceeds one sub-partition's share");
 constexpr uint32_t BOX_BYTES = BM * HD * 2;
 constexpr uint32_t Q_BYTES = 2 * BOX_BYTES, K_BYTES = 2 * BOX_BYTES, V_BYTES = 2 * BOX_BYTES;
-constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;
-constexpr uint32_t OFF_Q = 0, OFF_STAGE0 = Q_BYTES;
-constexpr uint32_t OFF_MISC = OFF_STAGE0 + STAGES * STAGE_BYTES;
+constexpr uint32_t D_HALF_BYTES = BM * 64 * 4;  // 64 fp32 values of D per row
+static_assert(D_HALF_BYTES == Q_BYTES, "the second half of D fills one Q box");
+constexpr uint32_t OFF_Q0 = 0;
+constexpr uint32_t OFF_K0 = OFF_Q0 + QBUF * Q_BYTES;
+constexpr uint32_t OFF_V0 = OFF_K0 + STAGES * K_BYTES;
+constexpr uint32_t OFF_D = OFF_V0 + STAGES * V_BYTES;
+constexpr uint32_t OFF_MISC = OFF_D + D_HALF_BYTES;
 constexpr uint32_t MISC_BYTES = 3072;
 // No alignment slack: every byte up to the per-block limit is in use; the
 // kernel checks that its dynamic shared memory starts on a 1024-byte boundary.
@@ -74,10 +96,11 @@ struct Item {
 
 struct Misc {
     uint64_t item_full[NSLOT], item_empty[NSLOT];
-    uint64_t q_full, q_empty;
-    uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
+    uint64_t q_full[QBUF], q_empty[QBUF];
+    uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
     uint64_t s_full[2], p_ready[2];
     uint64_t o_full, o_empty, stats_full[2];
+    uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
     float il[2][2][BM];                 // 1/l_c per row, by item parity and component
@@ -90,17 +113,6 @@ static_assert(sizeof(Misc) <= MISC_BYTES, "misc area too small");
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return smem_desc_sw128(saddr, 16, 1024); }
 __device__ __forceinline__ uint64_t desc_value(uint32_t saddr) { return smem_desc_sw128(saddr, BOX_BYTES, 1024); }
 __device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffffffu, pred); }
-// Named barrier over n threads that also returns the AND of `v` over them.
-__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p, int n_qt) {
@@ -117,17 +129,20 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
     auto bar_item_full = [&](int i) { return smem_u32(&ms.item_full[i]); };
     auto bar_item_empty = [&](int i) { return smem_u32(&ms.item_empty[i]); };
 
-    const uint32_t bar_q_full = smem_u32(&ms.q_full), bar_q_empty = smem_u32(&ms.q_empty);
+    auto bar_q_full = [&](int b) { return smem_u32(&ms.q_full[b]); };
+    auto bar_q_empty = [&](int b) { return smem_u32(&ms.q_empty[b]); };
     auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
+    auto bar_k_empty = [&](int s) { return smem_u32(&ms.k_empty[s]); };
     auto bar_v_full = [&](int s) { return smem_u32(&ms.v_full[s]); };
-    auto bar_kv_empty = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    auto bar_v_empty = [&](int s) { return smem_u32(&ms.v_empty[s]); };
     auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full), bar_o_empty = smem_u32(&ms.o_empty);
+    const uint32_t bar_mma_done = smem_u32(&ms.mma_done);
     auto bar_stats_full = [&](int i) { return smem_u32(&ms.stats_full[i]); };
-    const uint32_t sq = sbase + OFF_Q;
-    auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
-    auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
+    auto sq = [&](int b) { return sbase + OFF_Q0 + (uint32_t)b * Q_BYTES; };
+    auto sk = [&](int s) { return sbase + OFF_K0 + (uint32_t)s * K_BYTES; };
+    auto sv = [&](int s) { return sbase + OFF_V0 + (uint32_t)s * V_BYTES; };
 
     if (warp == PRODUCER_WARP && lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -137,12 +152,15 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
             mbar_init(bar_item_full(i), 1);
             mbar_init(bar_item_empty(i), 13);  // the MMA warp, the eight softmax and four epilogue warps
         }
-        mbar_init(bar_q_full, 1);
-        mbar_init(bar_q_empty, 1);
+        for (int b = 0; b < QBUF; ++b) {
+            mbar_init(bar_q_full(b), 1);
+            mbar_init(bar_q_empty(b), 4);  // one arrive per epilogue warp, after its second pass
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_k_full(s), 1);
+            mbar_init(bar_k_empty(s), 1);
             mbar_init(bar_v_full(s), 1);
-            mbar_init(bar_kv_empty(s), 1);
+            mbar_init(bar_v_empty(s), 1);
         }
         for (int c = 0; c < 2; ++c) {
             mbar_init(bar_s_full(c), 1);
@@ -152,6 +170,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         mbar_init(bar_o_empty, 128);     // every epilogue thread
         mbar_init(bar_stats_full(0), 256);  // every softmax thread, items of even / odd index
         mbar_init(bar_stats_full(1), 256);
+        mbar_init(bar_mma_done, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
     }
@@ -192,8 +211,6 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         for (;;) {
             const int slot = items % NSLOT;
             ok = warp_all(ok && mbar_wait(bar_item_full(slot), (uint32_t)(items / NSLOT) & 1u, ab));
-            // the eight warps go on or stop together
-            ok = named_barrier_and(2, 256, ok);
             if (!ok) break;
             const Item it = ms.work[slot];
             if (it.n_kv < 0) {
@@ -277,7 +294,6 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 tc_fence_before();
                 mbar_arrive(bar_p_ready(c));
             }
-            ok = named_barrier_and(2, 256, ok);
             if (!ok) break;
             // Training outputs: lse_c = m_c + log2(l_c), so that P_c = 2^(S_c scale log2(e) - lse_c).
             // The item's start and head are read again from its slot (the softmax warps
@@ -304,13 +320,21 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         setmaxnreg_dec<REG_EPI>();
         // =================================================== epilogue (warps 8-11) ===
         // One thread per row, all dv values: D = O1/l1 - lambda O2/l2, RMSNorm over dv,
-        // weight, (1 - lambda_init), bf16. O is read twice (the sum of squares, then the
-        // normalised output) so that D is not held in registers. Each half of the row is
-        // summed on its own and the halves added, the order of the one-item-per-CTA
-        // kernel's two warpgroups, so the two kernels give the same bits.
+        // weight, (1 - lambda_init), bf16. O is read once: D goes to shared memory in
+        // fp32 (values 0-63 in the D area, 64-127 in the item's Q box) while the sums
+        // of squares build up, and O is released to the next item's first P V before
+        // the second pass normalises the kept D. Each half of the row is summed on its
+        // own and the halves added, the order of the one-item-per-CTA kernel's two
+        // warpgroups, so the two kernels give the same bits. Row r of a half is 256
+        // bytes at r x 256, its 16-byte chunk i at chunk i ^ (r % 8) (no bank
+        // conflicts: the 8 rows of a store phase hit 8 different chunks).
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t t_o1 = tmem + lane_off + col_o(0), t_o2 = tmem + lane_off + col_o(1);
+        auto d_chunk = [&](int half, int buf, int i) {  // i: 16-byte chunk 0..15 of the half row
+            uint8_t* base = smem + (half == 0 ? OFF_D : OFF_Q0 + (uint32_t)buf * Q_BYTES);
+            return reinterpret_cast<float4*>(base + (uint32_t)r * 256u + (uint32_t)((i & 8) | ((i ^ r) & 7)) * 16u);
+        };
         int items = 0;
         for (;;) {
             const int slot = items % NSLOT;
@@ -324,7 +348,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 while (global_timer_ns() - t0 < 20000ull) {
                 }
             }
-            const int par = items & 1;
+            const int par = items & 1, qb = items & 1;
             if (!warp_all(mbar_wait(bar_stats_full(par), (uint32_t)(items >> 1) & 1u, ab))) break;
             if (!warp_all(mbar_wait(bar_o_full, (uint32_t)par, ab))) break;
             tc_fence_after();
@@ -337,23 +361,22 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
             for (int hf = 0; hf < 2; ++hf) {
                 float ssp = 0.f;
 #pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int ch = hf * 2 + c2;
-                    uint32_t o1[32], o2[32];
-                    tmem_ld32(t_o1 + ch * 32, o1);
-                    tmem_ld32(t_o2 + ch * 32, o2);
+                for (int c4 = 0; c4 < 4; ++c4) {  // 16 values at a time
+                    const int col = hf * 64 + c4 * 16;
+                    uint32_t o1[16], o2[16];
+                    tmem_ld16(t_o1 + col, o1);
+                    tmem_ld16(t_o2 + col, o2);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float d = diff_combine(__uint_as_float(o1[i]), il1, __uint_as_float(o2[i]), il2, lam);
-                        ssp = fmaf(d, d, ssp);
+                    if (col == DV - 16) {  // O has been read: the next item's first P V may overwrite it
+                        tc_fence_before();
+                        mbar_arrive(bar_o_empty);
                     }
                     // Training outputs: the normalised attention output of each component,
                     // kept in fp32 (the lambda gradient sums many cancelling terms of them).
                     if (store && p.o1 != nullptr) {
-                        const size_t base = ((size_t)(it.start + qi) * p.H + it.h) * DV / 4 + ch * 8;
+                        const size_t base = (((size_t)(it.start + qi) * p.H + it.h) * DV + col) / 4;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 4; ++i) {
                             reinterpret_cast<float4*>(p.o1)[base + i] =
                                 make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
                                             __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
@@ -361,6 +384,17 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                                 make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
                                             __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
                         }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float dq[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            dq[e] = diff_combine(__uint_as_float(o1[4 * i + e]), il1, __uint_as_float(o2[4 * i + e]), il2,
+                                                 lam);
+                            ssp = fmaf(dq[e], dq[e], ssp);
+                        }
+                        *d_chunk(hf, qb, c4 * 4 + i) = make_float4(dq[0], dq[1], dq[2], dq[3]);
                     }
                 }
                 ss_half[hf] = ssp;
@@ -371,22 +405,13 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                                                   ((size_t)(it.start + (store ? qi : 0)) * p.H + it.h) * DV);
 #pragma unroll 1
             for (int ch = 0; ch < DV / 32; ++ch) {
-                uint32_t o1[32], o2[32];
-                tmem_ld32(t_o1 + ch * 32, o1);
-                tmem_ld32(t_o2 + ch * 32, o2);
-                tmem_wait_ld();
-                if (ch == DV / 32 - 1) {  // O has been read: the next item's first P V may overwrite it
-                    tc_fence_before();
-                    mbar_arrive(bar_o_empty);
-                }
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int e = ch * 32 + 2 * i;
-                    const float d0 = diff_combine(__uint_as_float(o1[2 * i]), il1, __uint_as_float(o2[2 * i]), il2, lam);
-                    const float d1 =
-                        diff_combine(__uint_as_float(o1[2 * i + 1]), il1, __uint_as_float(o2[2 * i + 1]), il2, lam);
-                    pk[i] = pack_bf16x2(d0 * post * ms.w[e], d1 * post * ms.w[e + 1]);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 dq = *d_chunk(ch >> 1, qb, (ch & 1) * 8 + i);
+                    const int e = ch * 32 + 4 * i;
+                    pk[2 * i] = pack_bf16x2(dq.x * post * ms.w[e], dq.y * post * ms.w[e + 1]);
+                    pk[2 * i + 1] = pack_bf16x2(dq.z * post * ms.w[e + 2], dq.w * post * ms.w[e + 3]);
                 }
                 if (store) {
 #pragma unroll
@@ -394,6 +419,10 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                         dst[ch * 4 + g4] = make_uint4(pk[4 * g4], pk[4 * g4 + 1], pk[4 * g4 + 2], pk[4 * g4 + 3]);
                 }
             }
+            // The item's Q box (the second half of D) goes back to the producer.
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q_empty(qb));
             ++items;
         }
     } else {
@@ -422,6 +451,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 int q = 0, cq = count_rank(0);
                 long long P = 0;
                 int tile = 0, items = 0;
+                int q_issued = 0, k_issued = 0, v_issued = 0;  // loads issued, for the drain below
                 bool ok = true;
                 for (long long r = 0; ok && r * G < n_valid; ++r) {
                     const long long k = r * G + ((r & 1) ? G - 1 - blockIdx.x : blockIdx.x);
@@ -452,21 +482,27 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                         continue;
                     }
                     const int g = h / (p.H / p.Hkv);
-                    if (!(ok = mbar_wait(bar_q_empty, ((uint32_t)items & 1u) ^ 1u, ab))) break;
+                    const int qb = items % QBUF;
+                    if (!(ok = mbar_wait(bar_q_empty(qb), ((uint32_t)(items / QBUF) & 1u) ^ 1u, ab))) break;
                     const int row_q = it.start + it.qt * BM;
-                    mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
-                    tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
-                    tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
+                    mbar_arrive_expect_tx(bar_q_full(qb), Q_BYTES);
+                    tma_load_2d(sq(qb), &tm_q, bar_q_full(qb), h * 2 * HD, row_q, pol_q);
+                    tma_load_2d(sq(qb) + BOX_BYTES, &tm_q, bar_q_full(qb), h * 2 * HD + HD, row_q, pol_q);
+                    ++q_issued;
                     for (int jj = 0; jj < it.n_kv; ++jj, ++tile) {
                         const int s = tile % STAGES;
-                        if (!(ok = mbar_wait(bar_kv_empty(s), ((uint32_t)(tile / STAGES) & 1u) ^ 1u, ab))) break;
+                        const uint32_t ph = ((uint32_t)(tile / STAGES) & 1u) ^ 1u;
                         const int row = it.start + jj * BN;
+                        if (!(ok = mbar_wait(bar_k_empty(s), ph, ab))) break;
                         mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
                         tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
                         tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
+                        ++k_issued;
+                        if (!(ok = mbar_wait(bar_v_empty(s), ph, ab))) break;
                         mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
                         tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
                         tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+                        ++v_issued;
                     }
                     ++items;
                 }
@@ -478,80 +514,112 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                     ms.work[slot] = end;
                     mbar_arrive(bar_item_full(slot));
                 }
-                // Let every copy this CTA started land before shared memory goes away.
-                const int loaded = p.inject == 1 ? 0 : items;
-                if (loaded > 0) mbar_wait_drain(bar_q_full, (uint32_t)(loaded - 1) & 1u, p.timeout_ns);
-                for (int jj = tile > STAGES ? tile - STAGES : 0; jj < tile; ++jj) {
-                    const uint32_t ph = (uint32_t)(jj / STAGES) & 1u;
-                    mbar_wait_drain(bar_k_full(jj % STAGES), ph, p.timeout_ns);
-                    mbar_wait_drain(bar_v_full(jj % STAGES), ph, p.timeout_ns);
-                }
+                // Let every copy this CTA started land before shared memory goes away:
+                // the last Q load of each box and the last K and V load of each stage.
+                for (int k = q_issued > QBUF ? q_issued - QBUF : 0; k < q_issued; ++k)
+                    mbar_wait_drain(bar_q_full(k % QBUF), (uint32_t)(k / QBUF) & 1u, p.timeout_ns);
+                for (int jj = k_issued > STAGES ? k_issued - STAGES : 0; jj < k_issued; ++jj)
+                    mbar_wait_drain(bar_k_full(jj % STAGES), (uint32_t)(jj / STAGES) & 1u, p.timeout_ns);
+                for (int jj = v_issued > STAGES ? v_issued - STAGES : 0; jj < v_issued; ++jj)
+                    mbar_wait_drain(bar_v_full(jj % STAGES), (uint32_t)(jj / STAGES) & 1u, p.timeout_ns);
             }
             __syncwarp();
         } else if (warp == MMA_WARP) {
             // ==================================================== MMA issuer ===
+            // Items are fetched one ahead: at an item's last tile the next item's first
+            // score MMAs of component 1 follow this item's last P V of component 1 when
+            // that item's Q box and keys have already landed (otherwise they follow the
+            // item's last P V of component 2, so that its O is not held back).
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, DV, true);
-            constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, STG = STAGE_BYTES >> 4, BOX = BOX_BYTES >> 4;
-            const uint64_t qdesc = desc_kmajor(sq), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
-            auto issue_s = [&](int c, int tile) {
-                const uint64_t a0 = qdesc + (uint64_t)c * BOX;
-                const uint64_t b0 = kdesc + (uint64_t)(tile % STAGES) * STG + (uint64_t)c * BOX;
+            constexpr uint64_t KSTEP = 32 >> 4, VSTEP = (16 * 128) >> 4, BOX = BOX_BYTES >> 4;
+            constexpr uint64_t QSTG = Q_BYTES >> 4, KSTG = K_BYTES >> 4, VSTG = V_BYTES >> 4;
+            const uint64_t qdesc = desc_kmajor(sq(0)), kdesc = desc_kmajor(sk(0)), vdesc = desc_value(sv(0));
+            auto issue_s = [&](int c, int qb, int tile) {
+                const uint64_t a0 = qdesc + (uint64_t)qb * QSTG + (uint64_t)c * BOX;
+                const uint64_t b0 = kdesc + (uint64_t)(tile % STAGES) * KSTG + (uint64_t)c * BOX;
                 const uint32_t d = tmem + col_s(c);
     #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a0 + kk * KSTEP, b0 + kk * KSTEP, idesc_s, kk > 0 ? 1u : 0u);
                 mma_commit_elect(bar_s_full(c));
+                if (c == 1) mma_commit_elect(bar_k_empty(tile % STAGES));  // both score MMAs of the tile issued
             };
             auto issue_pv = [&](int c, int tile, bool first) {
-                const uint64_t b0 = vdesc + (uint64_t)(tile % STAGES) * STG;
+                const uint64_t b0 = vdesc + (uint64_t)(tile % STAGES) * VSTG;
                 const uint32_t d = tmem + col_o(c), a = tmem + col_s(c);
     #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, (kk > 0 || !first) ? 1u : 0u);
             };
-            int tile = 0, items = 0;
-            bool ok = true;
-            for (;;) {
-                const int slot = items % NSLOT;
-                if (!(ok = warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(items / NSLOT) & 1u, ab)))) break;
-                const Item it = ms.work[slot];
+            auto fetch = [&](int k, int& n_kv) {  // the MMA warp needs only the item's key tile count
+                const int slot = k % NSLOT;
+                if (!warp_all(mbar_wait(bar_item_full(slot), (uint32_t)(k / NSLOT) & 1u, ab))) return false;
+                n_kv = ms.work[slot].n_kv;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_item_empty(slot));
-                if (it.n_kv < 0) break;
-                // S of the item's first tile: the S columns are free (the previous item's last
-                // P V was issued before, and the tensor pipe completes in issue order)
-                if (!(ok = warp_all(mbar_wait(bar_q_full, (uint32_t)items & 1u, ab)))) break;
-                if (!(ok = warp_all(mbar_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
+                return true;
+            };
+            // Q box of item k and the keys of `tile` landed: waiting, or only probing.
+            auto s_ready = [&](int k, int tile) {
+                return warp_all(mbar_wait(bar_q_full(k % QBUF), (uint32_t)(k / QBUF) & 1u, ab)) &&
+                       warp_all(mbar_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u, ab));
+            };
+            auto s_ready_now = [&](int k, int tile) {
+                return warp_all(mbar_try_wait(bar_q_full(k % QBUF), (uint32_t)(k / QBUF) & 1u)) &&
+                       warp_all(mbar_try_wait(bar_k_full(tile % STAGES), (uint32_t)(tile / STAGES) & 1u));
+            };
+            int tile = 0, items = 0, cur_n = -1;
+            bool ok = fetch(0, cur_n);
+            if (ok && cur_n >= 0 && (ok = s_ready(0, 0))) {
                 tc_fence_after();
-                issue_s(0, tile);
-                issue_s(1, tile);
-                for (int j = 0; j < it.n_kv; ++j, ++tile) {
+                issue_s(0, 0, 0);
+                issue_s(1, 0, 0);
+            }
+            while (ok && cur_n >= 0) {
+                const int qb = items % QBUF;
+                int nxt_n = -1;
+                bool next_s1 = false;  // the next item's first component-1 scores are issued
+                for (int j = 0; j < cur_n; ++j, ++tile) {
                     const int s = tile % STAGES;
-                    const bool has_next = j + 1 < it.n_kv;
+                    const bool last = j + 1 == cur_n;
                     const int t1 = tile + 1;
                     if (!(ok = warp_all(mbar_wait(bar_v_full(s), (uint32_t)(tile / STAGES) & 1u, ab)))) break;
                     if (j == 0 && !(ok = warp_all(mbar_wait(bar_o_empty, ((uint32_t)items & 1u) ^ 1u, ab)))) break;
                     if (!(ok = warp_all(mbar_wait(bar_p_ready(0), (uint32_t)tile & 1u, ab)))) break;
                     tc_fence_after();
                     issue_pv(0, tile, j == 0);
-                    if (has_next) {
+                    if (!last) {
                         if (!(ok = warp_all(mbar_wait(bar_k_full(t1 % STAGES), (uint32_t)(t1 / STAGES) & 1u, ab)))) break;
-                        issue_s(0, t1);
+                        issue_s(0, qb, t1);
+                    } else {
+                        if (!(ok = fetch(items + 1, nxt_n))) break;
+                        if (nxt_n >= 0 && s_ready_now(items + 1, t1)) {
+                            tc_fence_after();
+                            issue_s(0, (items + 1) % QBUF, t1);
+                            next_s1 = true;
+                        }
                     }
                     if (!(ok = warp_all(mbar_wait(bar_p_ready(1), (uint32_t)tile & 1u, ab)))) break;
                     tc_fence_after();
                     issue_pv(1, tile, j == 0);
-                    mma_commit_elect(bar_kv_empty(s));
-                    if (has_next) issue_s(1, t1);
+                    mma_commit_elect(bar_v_empty(s));
+                    if (!last) issue_s(1, qb, t1);
                 }
                 if (!ok) break;
-                mma_commit_elect(bar_q_empty);  // every MMA reading this item's Q has been issued
-                mma_commit_elect(bar_o_full);
+                mma_commit_elect(bar_o_full);  // every P V of this item issued
                 ++items;
+                cur_n = nxt_n;
+                if (cur_n < 0) break;
+                if (!next_s1) {
+                    if (!(ok = s_ready(items, tile))) break;
+                    tc_fence_after();
+                    issue_s(0, items % QBUF, tile);
+                }
+                issue_s(1, items % QBUF, tile);
             }
             // every MMA issued has completed before TMEM is released
-            mma_commit_elect(bar_q_empty);
-            mbar_wait_drain(bar_q_empty, (uint32_t)items & 1u, p.timeout_ns);
+            mma_commit_elect(bar_mma_done);
+            mbar_wait_drain(bar_mma_done, 0, p.timeout_ns);
             __syncwarp();
         }
     }
