@@ -112,6 +112,22 @@ bool fwd_use_persistent(bool packed, int max_seqlen, int heads, int num_seqs) {
     return n_qt * heads * num_seqs >= 2LL * sm_count();
 }
 
+// Heads per launch group of the one-item-per-CTA bf16 forward: a whole number of
+// kv-head groups whose K and V (max_seqlen rows of 2d + dv bf16 per kv head) fit in
+// 32 MB, a quarter of the L2. The CTAs in flight (one per SM) then walk the K / V
+// tiles of those heads only, and re-read them from L2 rather than HBM; with every
+// head in one group, 16 heads of T = 16384 keep 128 MB of K / V in flight and the
+// launch read 3.4x its algorithmic bytes from DRAM.
+int fwd_group_heads(int H, int Hkv, int max_seqlen) {
+    const int G = H / Hkv;
+    const double kv_head_bytes = (double)max_seqlen * (2 * 64 + 128) * 2;
+    int kv = (int)((32.0 * (1 << 20)) / (kv_head_bytes > 1.0 ? kv_head_bytes : 1.0));
+    if (kv < 1) kv = 1;
+    if (kv > Hkv) kv = Hkv;
+    while (Hkv % kv != 0) --kv;  // a divisor of Hkv, so that groups tile the heads
+    return kv * G;
+}
+
 // Launch order of a causal backward kernel, whose CTA for tile t of a sequence of n
 // 128-row tiles visits t + 1 (dQ) or n - t (dK/dV) tiles. Sequence-major order keeps
 // the CTAs in flight on one or two sequences, so the operands they stream are shared
@@ -307,6 +323,7 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
     p.lse = lse;
     p.o1 = o1;
     p.o2 = o2;
+    p.group_heads = fwd_group_heads(p.H, p.Hkv, p.max_seqlen);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;

@@ -109,9 +109,16 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.x;
+    // Launch order within a sequence: groups of group_heads heads one after another,
+    // and within a group the query tiles longest first, the group's heads fastest.
+    // The CTAs in flight then stream the K / V of one group, which the host sizes
+    // to stay in L2.
+    const int n_qt = (p.max_seqlen + BM - 1) / BM;
+    const int hg = p.group_heads;
+    const int grp = (int)blockIdx.x / (n_qt * hg), rem = (int)blockIdx.x - grp * (n_qt * hg);
+    const int h = grp * hg + rem % hg;
+    const int qt = n_qt - 1 - rem / hg;  // longest query tiles are scheduled first
     const int seq = blockIdx.z;
-    const int qt = gridDim.y - 1 - blockIdx.y;  // longest query tiles are scheduled first
 
     // ---- sequence bounds; uniform over the CTA -----------------------------
     int start, len;
@@ -465,8 +472,9 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
         attr_done[dev] = true;
     }
     const int n_qt = (p.max_seqlen + BM - 1) / BM;
+    if (p.group_heads < 1 || p.H % p.group_heads != 0 || (long long)n_qt * p.H > INT32_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
+    cfg.gridDim = dim3((unsigned)(n_qt * p.H), 1u, (unsigned)p.num_seqs);
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;

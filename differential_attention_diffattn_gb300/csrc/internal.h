@@ -39,6 +39,7 @@ struct FwdParams {
     unsigned long long timeout_ns;
     int inject;               // test hook: 1 = the copy producer issues no loads; 2 = the persistent
                               // kernel's epilogue pauses ~20 us before each item
+    int group_heads;          // one-item-per-CTA bf16 kernel: heads per launch group (divides H)
     float* lse;               // training outputs (all null, or all set; bf16 kernel only):
     void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
     void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c
