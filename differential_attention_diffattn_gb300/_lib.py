@@ -36,7 +36,8 @@ class DiffAttnDesc(ctypes.Structure):
 class DiffAttnKvDesc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("q_len", ctypes.c_int), ("cache_capacity", ctypes.c_int),
                 ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("d", ctypes.c_int),
-                ("dv", ctypes.c_int), ("dtype", ctypes.c_int), ("eps", ctypes.c_float), ("num_splits", ctypes.c_int)]
+                ("dv", ctypes.c_int), ("dtype", ctypes.c_int), ("eps", ctypes.c_float), ("num_splits", ctypes.c_int),
+                ("host_seqlens", ctypes.c_void_p)]
 
 
 class DiffAttnRopeDesc(ctypes.Structure):
@@ -382,9 +383,11 @@ def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True,
     return out
 
 
-def kv_desc(q, k_cache, v_cache, eps: float = 1e-5, num_splits: int = 0) -> DiffAttnKvDesc:
+def kv_desc(q, k_cache, v_cache, eps: float = 1e-5, num_splits: int = 0, host_seqlens=None) -> DiffAttnKvDesc:
     """Descriptor of a cache forward from tensor shapes (q [B, q_len, H, 2d],
-    k_cache [B, capacity, Hkv, 2d], v_cache [B, capacity, Hkv, dv])."""
+    k_cache [B, capacity, Hkv, 2d], v_cache [B, capacity, Hkv, dv]).
+    host_seqlens: optional host copy of the cache lengths (a sequence of ints or
+    a CPU tensor, [B]), which lets the library plan the key splits from them."""
     import torch
     if q.dim() != 4 or k_cache.dim() != 4 or v_cache.dim() != 4:
         raise ValueError("q, k_cache, v_cache must be 4-D")
@@ -394,6 +397,14 @@ def kv_desc(q, k_cache, v_cache, eps: float = 1e-5, num_splits: int = 0) -> Diff
     d.d, d.dv = q.shape[3] // 2, v_cache.shape[3]
     d.dtype = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_F32
     d.eps, d.num_splits = float(eps), int(num_splits)
+    d.host_seqlens = None
+    if host_seqlens is not None:
+        vals = [int(x) for x in (host_seqlens.tolist() if hasattr(host_seqlens, "tolist") else host_seqlens)]
+        if len(vals) != d.batch:
+            raise ValueError("host_seqlens must hold one length per sequence")
+        arr = (ctypes.c_int * max(1, len(vals)))(*vals)
+        d._host_arr = arr  # kept alive with the descriptor
+        d.host_seqlens = ctypes.cast(arr, ctypes.c_void_p)
     return d
 
 
@@ -403,11 +414,13 @@ def diffattn_fwd_kvcache_workspace_size(desc: DiffAttnKvDesc) -> int:
 
 def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, cache_seqlens=None,
                          causal: bool = True, eps: float = 1e-5, num_splits: int = 0, workspace=None, out=None,
-                         stream=None):
+                         stream=None, host_seqlens=None):
     """New queries q [B, q_len, H, 2d] against a cache (k_cache [B, capacity,
     Hkv, 2d], v_cache [B, capacity, Hkv, dv], cache_seqlens int32 [B] on the
     device or None). The workspace (scratch for the key splits) is a caller
-    buffer; when None the binding allocates one with torch for this call."""
+    buffer; when None the binding allocates one with torch for this call.
+    host_seqlens: optional host copy of cache_seqlens for the split plan (a
+    caller workspace must then be sized with the same lengths)."""
     import torch
     lib = load_library()
     for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (lam, "lambda"), (subln_w, "subln_w")):
@@ -416,7 +429,7 @@ def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, 
         _check_cuda(cache_seqlens, "cache_seqlens")
         if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != q.shape[0]:
             raise ValueError("cache_seqlens must be int32 [batch]")
-    desc = kv_desc(q, k_cache, v_cache, eps, num_splits)
+    desc = kv_desc(q, k_cache, v_cache, eps, num_splits, host_seqlens)
     need = int(lib.diffattn_fwd_kvcache_workspace_size(ctypes.byref(desc)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -437,7 +450,7 @@ def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, 
 
 def diffattn_fwd_kvcache_noalloc(q, k_cache, v_cache, lam, lambda_init: float, subln_w, cache_seqlens=None,
                                  causal: bool = True, eps: float = 1e-5, num_splits: int = 0, out=None,
-                                 stream=None):
+                                 stream=None, host_seqlens=None):
     """diffattn_fwd_kvcache whose key-split scratch is the library's static device
     array instead of a workspace. The C entry point allocates nothing; only the
     output tensor is created here when `out` is None."""
@@ -449,7 +462,7 @@ def diffattn_fwd_kvcache_noalloc(q, k_cache, v_cache, lam, lambda_init: float, s
         _check_cuda(cache_seqlens, "cache_seqlens")
         if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != q.shape[0]:
             raise ValueError("cache_seqlens must be int32 [batch]")
-    desc = kv_desc(q, k_cache, v_cache, eps, num_splits)
+    desc = kv_desc(q, k_cache, v_cache, eps, num_splits, host_seqlens)
     if out is None:
         out = torch.empty(q.shape[:-1] + (v_cache.shape[-1],), dtype=q.dtype, device=q.device)
     _check_cuda(out, "out")

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/diffattn.h: argument validation,
 // the per-device error word, TMA descriptor encoding and kernel dispatch.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -148,6 +149,49 @@ bool bwd_tiles_outermost(int num_seqs, int heads, int max_seqlen) {
     return last_end > 1.1 * avg_end;
 }
 
+// Key-split count of a cache forward from the sequences' actual key counts (a
+// host copy of cache_seqlens): the count whose modelled time is least, fewer
+// splits on a tie. A split CTA streams its keys (512 bytes per key and kv head at
+// d = 64) at t(A) = sqrt(t1^2 + (A * 512 B / BW)^2) per key while A split CTAs
+// stream together: t1 = 10.4 ns is one CTA's own rate (its two-stage pipeline),
+// BW = 5.8 TB/s the device's; the CTAs run in waves of the resident slots, each
+// wave's longest chunk setting its time, plus 2.5 us a wave and the combine's
+// reads (1040 bytes per row and split at ~3 TB/s). Fitted on GB300 to forced
+// split sweeps: 16 ragged caches of 1016..7005 keys (capacity 8192, 4 kv heads,
+// 4 new tokens) measured best at 6-7 splits (34.4 us; the shape-only plan took 4,
+// 38.4 us), 8 full 16k caches at 8-9 (46.8 us).
+template <typename RoundPlan>
+long long kv_plan_from_lengths(const diffattn_kv_desc& d, RoundPlan round_plan) {
+    const long long cap = d.cache_capacity;
+    const int rows = d.q_len * (d.num_heads / d.num_kv_heads);
+    const double slots = (double)sm_count() * (decode_rows_supported(rows) ? decode_ctas_per_sm() : 1);
+    const double t1 = 10.4, per_cta = 512.0 / 5.8e3;  // ns per key; ns per key per streaming CTA
+    auto rate = [&](double a) { return std::sqrt(t1 * t1 + (a * per_cta) * (a * per_cta)); };
+    const double comb_per_split = (double)d.batch * d.q_len * d.num_heads * 1040.0 / 3.0e3;  // ns
+    const long long max_n = std::min<long long>((cap + 255) / 256, decode_max_splits());
+    long long best_n = 1;
+    double best_t = -1.0;
+    for (long long cand = 1; cand <= max_n; ++cand) {
+        long long cc = 0;
+        const long long n = round_plan(cand, &cc);
+        double active = 0.0;
+        for (int b = 0; b < d.batch; ++b) {
+            const long long L = std::min<long long>(std::max(d.host_seqlens[b], 1), cap);
+            active += (double)((L + cc - 1) / cc);
+        }
+        active *= d.num_kv_heads;
+        const double full = std::floor(active / slots), rest = active - full * slots;
+        const double waves = full + (rest > 0.0 ? 1.0 : 0.0);
+        const double t = (double)cc * (full * rate(slots) + (rest > 0.0 ? rate(rest) : 0.0)) + 2500.0 * waves +
+                         (double)n * comb_per_split;
+        if (best_t < 0.0 || t < best_t * 0.995) {
+            best_t = t;
+            best_n = n;
+        }
+    }
+    return best_n;
+}
+
 // Key-split plan of a cache forward: (number of splits, keys per split), with
 // splits of at least 256 keys (64-key multiples). Without a requested count it
 // takes the fewest waves of resident split CTAs on the device's SMs (1 to 4) whose
@@ -167,7 +211,9 @@ bool kv_plan(const diffattn_kv_desc& d, int* n_splits, int* chunk) {
         return (cap + c - 1) / c;
     };
     long long n = d.num_splits, c = 0;
-    if (n == 0) {
+    if (n == 0 && d.host_seqlens != nullptr && d.batch > 0) {
+        n = kv_plan_from_lengths(d, round_plan);
+    } else if (n == 0) {
         const long long ctas = (long long)d.batch * d.num_kv_heads;
         const int rows = d.q_len * (d.num_heads / d.num_kv_heads);
         const long long slots = (long long)sm_count() * (decode_rows_supported(rows) ? decode_ctas_per_sm() : 1);

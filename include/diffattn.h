@@ -215,7 +215,15 @@ diffattn_status diffattn_lambda_bwd(const float* lq1, const float* lk1, const fl
  *  tokens included: they are the last q_len valid rows).
  *  num_heads, num_kv_heads, d, dv, dtype, eps as in diffattn_desc.
  *  num_splits: key splits per (sequence, kv head), at most 1024; 0 lets the
- *  library choose from the shape (the workspace size depends on it).
+ *  library choose (the workspace size depends on it).
+ *  host_seqlens: NULL, or a HOST copy of cache_seqlens (int32 [batch]) for
+ *  callers that have one. With num_splits == 0 the library then plans the
+ *  splits from the sequences' actual key counts (a ragged batch wants more
+ *  splits than its capacity suggests); without it the plan sees only the
+ *  shape. Read during the call, not retained; pass the same descriptor to
+ *  diffattn_fwd_kvcache_workspace_size and to the forward, since the split
+ *  count sizes the workspace. The device cache_seqlens remain the ones the
+ *  kernels use and check.
  */
 typedef struct {
     int batch;
@@ -228,6 +236,7 @@ typedef struct {
     diffattn_dtype dtype;
     float eps;
     int num_splits;
+    const int* host_seqlens;
 } diffattn_kv_desc;
 
 /*

@@ -51,15 +51,17 @@ def oracle_out(inp, rows=None, lam_value=None, lambda_init=None):
                             inp.wl.causal, rows)
 
 
-def run_gpu_kv(inp, dev="cuda", num_splits=0, use_seqlens=True, out=None):
-    """The library's cache forward on `workloads.KvInputs`."""
+def run_gpu_kv(inp, dev="cuda", num_splits=0, use_seqlens=True, out=None, host_seqlens=False):
+    """The library's cache forward on `workloads.KvInputs` (host_seqlens: also
+    hand the library a host copy of the lengths for its split plan)."""
     wl = inp.wl
     li = da.diffattn_lambda_init(wl.depth)
     lam = da.diffattn_lambda(inp.lambda_q1.to(dev), inp.lambda_k1.to(dev), inp.lambda_q2.to(dev),
                              inp.lambda_k2.to(dev), li)
     y = da.diffattn_fwd_kvcache(inp.q.to(dev), inp.k_cache.to(dev), inp.v_cache.to(dev), lam, li,
                                 inp.subln_w.to(dev), cache_seqlens=inp.cache_seqlens.to(dev) if use_seqlens else None,
-                                causal=wl.causal, eps=wl.eps, num_splits=num_splits, out=out)
+                                causal=wl.causal, eps=wl.eps, num_splits=num_splits, out=out,
+                                host_seqlens=inp.cache_seqlens if host_seqlens else None)
     st = da.diffattn_get_device_status()
     assert st == 0, da.diffattn_status_string(st)
     return y

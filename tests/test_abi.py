@@ -216,3 +216,20 @@ def test_fault_injection_hook_is_off_without_the_test_environment(lib, monkeypat
     assert lib.diffattn_set_fault_injection(3) == 1   # no such mode
     assert lib.diffattn_set_fault_injection(1) == 0
     assert lib.diffattn_set_fault_injection(0) == 0
+
+
+def test_cache_forward_split_plan_from_host_lengths(lib):
+    # With a host copy of the lengths the plan models the split CTAs' streaming
+    # time (fitted to GB300 sweeps; 152 SMs assumed without a GPU): the ragged
+    # 16 x 4-token batch takes 7 splits (4 from the shape), the full 8 x 16k one 8.
+    rag = [6638, 4932, 6735, 1706, 6830, 4356, 1178, 6860, 1195, 5839, 1610, 7005, 5464, 6260, 5740, 1016]
+
+    def ws(batch, q_len, cap, lens):
+        d = _lib.DiffAttnKvDesc(batch=batch, q_len=q_len, cache_capacity=cap, num_heads=16, num_kv_heads=4,
+                                d=64, dv=128, dtype=_lib.DTYPE_BF16, eps=1e-5, num_splits=0)
+        arr = (ctypes.c_int * batch)(*lens)
+        d.host_seqlens = ctypes.cast(arr, ctypes.c_void_p)
+        return lib.diffattn_fwd_kvcache_workspace_size(ctypes.byref(d))
+    per_split = lambda batch, q_len: batch * q_len * 16 * 2 * (128 + 2) * 4  # noqa: E731
+    assert ws(16, 4, 8192, rag) == 7 * per_split(16, 4)
+    assert ws(8, 1, 16384, [16384] * 8) == 8 * per_split(8, 1)

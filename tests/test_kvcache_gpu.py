@@ -118,3 +118,22 @@ def test_more_groups_than_resident_ctas():
     lengths = rng.integers(1, 301, 200).tolist()
     inp = W.generate_kv(kvw(batch=200, capacity=300), seed=58, lengths=lengths)
     compare(run_gpu_kv(inp), oracle_kv(inp), "bf16")
+
+
+@pytest.mark.parametrize("name", ["decode_b8_c16384", "decode_b16_q4_ragged"])
+def test_cache_workloads_with_host_lengths(name):
+    """The split plan from a host copy of the lengths (7 splits on the ragged
+    batch, 8 on the uniform one, against 4 and 9 from the shape alone): the same
+    results within the tolerance, on sampled sequences against the oracle."""
+    inp = W.generate_kv(W.KV_WORKLOADS[name], seed=0)
+    got = run_gpu_kv(inp, host_seqlens=True)
+    ref = run_gpu_kv(inp)
+    compare(got, ref.double().cpu().numpy(), "bf16")
+    b_sel = [0, inp.wl.batch // 2, inp.wl.batch - 1]
+    compare(got[b_sel], oracle_kv(inp, b_sel), "bf16")
+
+
+def test_host_lengths_on_mixed_batch():
+    # one long sequence among short ones: the plan spreads the long one over many splits
+    inp = W.generate_kv(kvw(batch=4, capacity=4096), seed=52, lengths=[100, 200, 4096, 30])
+    compare(run_gpu_kv(inp, host_seqlens=True), oracle_kv(inp), "bf16")
