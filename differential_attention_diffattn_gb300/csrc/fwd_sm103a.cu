@@ -79,6 +79,7 @@ struct Misc {  // lives at OFF_MISC
     uint64_t s_full[2];
     uint64_t p_ready[2];
     uint64_t o_full;
+    uint64_t w_full;  // the norm weight and lambda have landed in shared memory
     uint32_t tmem_base;
     int abort_flag;
     float lam;        // lambda of this head, and the norm weight, staged at setup
@@ -147,32 +148,62 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     auto bar_s_full = [&](int c) { return smem_u32(&ms.s_full[c]); };
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full);
+    const uint32_t bar_w_full = smem_u32(&ms.w_full);
     const uint32_t sq = sbase + OFF_Q;
     auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
     auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
 
     // ---- setup --------------------------------------------------------------
-    if (warp == PRODUCER_WARP && lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        mbar_init(bar_q_full, 1);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_k_full(s), 1);
-            mbar_init(bar_v_full(s), 1);
-            mbar_init(bar_kv_empty(s), 1);
-        }
-        for (int c = 0; c < 2; ++c) {
-            mbar_init(bar_s_full(c), 1);
-            mbar_init(bar_p_ready(c), 128);
-        }
-        mbar_init(bar_o_full, 1);
-        ms.abort_flag = 0;
-        fence_barrier_init();
-    }
+    // The producer issues Q and the first STAGES key / value tiles as soon as its
+    // barriers exist, before the CTA-wide barrier, and the norm weight and lambda
+    // come by cp.async on their own barrier (waited for only by the epilogue): on a
+    // cold L2 the plain loads of those had held the first TMA loads back ~2 us.
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();
+    auto load_kv = [&](int j) {
+        const int s = j % STAGES;
+        const int row = start + j * BN;
+        mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
+        tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
+        tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
+        mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
+        tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
+        tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+    };
+    // With the test hook set, no load is issued: the barriers the other roles
+    // wait on are never armed, so their bounded waits run out.
+    const int early = p.inject == 1 ? 0 : min(n_kv, STAGES);  // tiles loaded before the CTA barrier
     if (warp == PRODUCER_WARP) {
-        for (int i = lane; i < DV; i += 32) ms.w[i] = p.subln_w[i];
-        if (lane == 0) ms.lam = p.lambda[h * p.lambda_stride];
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_init(bar_q_full, 1);
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(bar_k_full(s), 1);
+                mbar_init(bar_v_full(s), 1);
+                mbar_init(bar_kv_empty(s), 1);
+            }
+            for (int c = 0; c < 2; ++c) {
+                mbar_init(bar_s_full(c), 1);
+                mbar_init(bar_p_ready(c), 128);
+            }
+            mbar_init(bar_o_full, 1);
+            mbar_init(bar_w_full, 32);  // one cp.async arrive per lane of this warp
+            ms.abort_flag = 0;
+            fence_barrier_init();
+            if (p.inject != 1) {
+                const int row_q = start + qt * BM;
+                mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
+                tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
+                tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
+                for (int j = 0; j < early; ++j) load_kv(j);  // fresh stages: nothing to wait for
+            }
+        }
+        __syncwarp();  // the barriers exist before any lane arrives on them
+        for (int i = lane; i < DV; i += 32) cp_async4(smem_u32(&ms.w[i]), p.subln_w + i);
+        if (lane == 0) cp_async4(smem_u32(&ms.lam), p.lambda + h * p.lambda_stride);
+        cp_async_arrive_noinc(bar_w_full);
     }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
     tc_fence_before();
@@ -183,27 +214,13 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 
     if (warp == PRODUCER_WARP) {
         // ================================================= TMA producer ===
-        // With the test hook set, no load is issued: the barriers the other roles
-        // wait on are never armed, so their bounded waits run out.
         if (lane == 0 && p.inject != 1) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_last();
-            const int row_q = start + qt * BM;
-            mbar_arrive_expect_tx(bar_q_full, Q_BYTES);
-            tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
-            tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
+            int issued = early;
+            for (int j = early; j < n_kv; ++j) {
                 const int s = j % STAGES;
                 const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
                 if (!mbar_wait(bar_kv_empty(s), ph ^ 1u, ab)) break;
-                const int row = start + j * BN;
-                mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
-                tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol_kv);
-                tma_load_2d(sk(s) + BOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol_kv);
-                mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
-                tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol_kv);
-                tma_load_2d(sv(s) + BOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol_kv);
+                load_kv(j);
                 issued = j + 1;
             }
             // Let every copy this CTA started land before shared memory goes away.
@@ -214,6 +231,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 mbar_wait_drain(bar_v_full(j % STAGES), ph, p.timeout_ns);
             }
         }
+        cp_async_wait_all();  // the weight copies have landed, whatever the epilogue did
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ==================================================== MMA issuer ===
@@ -369,6 +387,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         xch[c * BM + r] = 1.f / l;
         named_barrier_sync(1, 256);
         ok = warp_all(ok && mbar_wait(bar_o_full, 0, ab));
+        ok = warp_all(ok && mbar_wait(bar_w_full, 0, ab));
         const bool store = qi < len;
         float D[64];
         float ssp = 0.f;
