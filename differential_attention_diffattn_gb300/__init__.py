@@ -12,10 +12,12 @@ from ._lib import (  # noqa: F401
     DiffAttnMergeDesc,
     DiffAttnOutProjDesc,
     DiffAttnRopeDesc,
+    DiffAttnRopeQ,
     diffattn_bwd,
     diffattn_bwd_workspace_size,
     diffattn_fwd,
     diffattn_fwd_kernel,
+    diffattn_fwd_rope_q,
     diffattn_fwd_train,
     diffattn_fwd_kvcache,
     diffattn_fwd_kvcache_noalloc,
@@ -26,6 +28,7 @@ from ._lib import (  # noqa: F401
     diffattn_lambda_init,
     diffattn_merge_partials,
     diffattn_out_proj,
+    diffattn_rope_k,
     diffattn_rope_qk,
     diffattn_rope_tables,
     diffattn_set_fault_injection,

@@ -23,7 +23,7 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
             "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj",
-            "diffattn_fwd_kernel")
+            "diffattn_fwd_kernel", "diffattn_fwd_rope_q")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -45,6 +45,11 @@ class DiffAttnRopeDesc(ctypes.Structure):
                 ("d", ctypes.c_int), ("dtype", ctypes.c_int), ("rot_dim", ctypes.c_int),
                 ("interleaved", ctypes.c_int), ("n_pos", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("seqlen", ctypes.c_int)]
+
+
+class DiffAttnRopeQ(ctypes.Structure):
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("n_pos", ctypes.c_int), ("rot_dim", ctypes.c_int),
+                ("interleaved", ctypes.c_int)]
 
 
 class DiffAttnMergeDesc(ctypes.Structure):
@@ -84,6 +89,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_lambda.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp]
         lib.diffattn_fwd_kernel.restype = ctypes.c_char_p
         lib.diffattn_fwd_kernel.argtypes = [ctypes.POINTER(DiffAttnDesc), ctypes.c_int]
+        lib.diffattn_fwd_rope_q.restype = ctypes.c_int
+        lib.diffattn_fwd_rope_q.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
+                                            vp, ctypes.c_int, vp, ctypes.POINTER(DiffAttnRopeQ), vp, vp]
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                      vp, ctypes.c_int, vp, vp, vp]
@@ -317,17 +325,10 @@ def diffattn_lambda_bwd(lq1, lk1, lq2, lk2, dlambda, stream=None):
     return tuple(outs)
 
 
-def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,
-                 max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, stream=None):
-    """Differential-attention forward on the GPU.
-
-    q [B, T, H, 2d] with k [B, T, Hkv, 2d], v [B, T, Hkv, dv] (dense), or
-    q [tokens, H, 2d] with k, v token-major and, for packed sequences,
-    cu_seqlens int32 [num_seqs + 1] on the device plus max_seqlen (host int).
-    lam: fp32 [1] (shared) or [H] (per head). Returns out [..., H, dv] in q's dtype.
-    """
+def _fwd_args(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps, out):
+    """Descriptor, head count and output tensor of a forward call (shared by
+    diffattn_fwd and diffattn_fwd_rope_q)."""
     import torch
-    lib = load_library()
     for t, name in ((q, "q"), (k, "k"), (v, "v"), (lam, "lambda"), (subln_w, "subln_w")):
         _check_cuda(t, name)
     if q.dtype == torch.bfloat16:
@@ -346,7 +347,6 @@ def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True,
             raise ValueError("cu_seqlens goes with token-major [tokens, H, 2d] inputs")
         B, T, H, two_d = q.shape
         desc.batch, desc.seqlen = B, T
-        tokens = B * T
     elif q.dim() == 3:
         tokens, H, two_d = q.shape
         if cu_seqlens is None:
@@ -374,12 +374,52 @@ def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True,
     if out is None:
         out = torch.empty(q.shape[:-1] + (dv,), dtype=q.dtype, device=q.device)
     _check_cuda(out, "out")
+    return desc, H, out
+
+
+def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True, cu_seqlens=None,
+                 max_seqlen: Optional[int] = None, eps: float = 1e-5, out=None, stream=None):
+    """Differential-attention forward on the GPU.
+
+    q [B, T, H, 2d] with k [B, T, Hkv, 2d], v [B, T, Hkv, dv] (dense), or
+    q [tokens, H, 2d] with k, v token-major and, for packed sequences,
+    cu_seqlens int32 [num_seqs + 1] on the device plus max_seqlen (host int).
+    lam: fp32 [1] (shared) or [H] (per head). Returns out [..., H, dv] in q's dtype.
+    """
+    lib = load_library()
+    desc, H, out = _fwd_args(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps, out)
     st = lib.diffattn_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
                           1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
                           1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(out),
                           _stream_handle(stream))
     if st != OK:
         raise DiffAttnError(st, "diffattn_fwd")
+    return out
+
+
+def diffattn_fwd_rope_q(q, k, v, lam, lambda_init: float, subln_w, cos, sin, rot_dim: int, interleaved: bool,
+                        causal: bool = True, cu_seqlens=None, max_seqlen: Optional[int] = None, eps: float = 1e-5,
+                        out=None, stream=None):
+    """diffattn_fwd on q BEFORE its rotary embedding (the kernels rotate each
+    query tile in shared memory; position = index inside the sequence); k must
+    already be rotated (diffattn_rope_k). cos, sin: the tables of
+    diffattn_rope_tables."""
+    import torch
+    lib = load_library()
+    desc, H, out = _fwd_args(q, k, v, lam, subln_w, cu_seqlens, max_seqlen, eps, out)
+    for t, name in ((cos, "cos"), (sin, "sin")):
+        _check_cuda(t, name)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be fp32")
+    rope = DiffAttnRopeQ()
+    rope.cos, rope.sin = _ptr(cos), _ptr(sin)
+    rope.n_pos, rope.rot_dim, rope.interleaved = cos.shape[0], int(rot_dim), 1 if interleaved else 0
+    st = lib.diffattn_fwd_rope_q(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(lam),
+                                 1 if (lam.numel() == H and H > 1) else 0, float(lambda_init), _ptr(subln_w),
+                                 1 if causal else 0, _ptr(cu_seqlens) if cu_seqlens is not None else None,
+                                 ctypes.byref(rope), _ptr(out), _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_rope_q")
     return out
 
 
@@ -516,26 +556,29 @@ def diffattn_rope_tables(theta: float, n_pos: int, rot_dim: int, device=None, st
 def diffattn_rope_qk(q, k, cos, sin, rot_dim: int, interleaved: bool, positions=None, cu_seqlens=None,
                      q_out=None, k_out=None, stream=None):
     """Rotate q [tokens, H, 2d] (or [B, T, H, 2d]) and k (same layout with Hkv
-    heads, or None). Positions: `positions` int32 [tokens] if given, else
-    `cu_seqlens` (packed sequences), else the dense layout. Pass q_out=q /
-    k_out=k to rotate in place. Returns (q_out, k_out)."""
+    heads, or None); q may be None to rotate k only. Positions: `positions`
+    int32 [tokens] if given, else `cu_seqlens` (packed sequences), else the
+    dense layout. Pass q_out=q / k_out=k to rotate in place. Returns (q_out, k_out)."""
     import torch
-    _check_cuda(q, "q")
-    if q.dtype == torch.bfloat16:
+    ref = q if q is not None else k
+    if ref is None:
+        raise ValueError("q or k is required")
+    _check_cuda(ref, "q" if q is not None else "k")
+    if ref.dtype == torch.bfloat16:
         dt = DTYPE_BF16
-    elif q.dtype == torch.float32:
+    elif ref.dtype == torch.float32:
         dt = DTYPE_F32
     else:
-        raise ValueError(f"unsupported dtype {q.dtype}")
+        raise ValueError(f"unsupported dtype {ref.dtype}")
     desc = DiffAttnRopeDesc()
-    H, two_d = q.shape[-2], q.shape[-1]
-    desc.tokens = q.numel() // (H * two_d)
-    desc.num_heads, desc.d, desc.dtype = H, two_d // 2, dt
+    two_d = ref.shape[-1]
+    desc.tokens = ref.numel() // (ref.shape[-2] * two_d)
+    desc.num_heads, desc.d, desc.dtype = (q.shape[-2] if q is not None else 0), two_d // 2, dt
     desc.rot_dim, desc.interleaved = int(rot_dim), 1 if interleaved else 0
     desc.n_pos = cos.shape[0]
     if k is not None:
         _check_cuda(k, "k")
-        if k.dtype != q.dtype or k.shape[:-2] != q.shape[:-2] or k.shape[-1] != two_d:
+        if k.dtype != ref.dtype or k.shape[:-2] != ref.shape[:-2] or k.shape[-1] != two_d:
             raise ValueError("k must match q's dtype, token dims and head width")
         desc.num_kv_heads = k.shape[-2]
     for t, name in ((cos, "cos"), (sin, "sin")):
@@ -552,18 +595,27 @@ def diffattn_rope_qk(q, k, cos, sin, rot_dim: int, interleaved: bool, positions=
             raise ValueError("cu_seqlens must be int32")
         desc.num_seqs = cu_seqlens.numel() - 1
     else:
-        desc.seqlen = q.shape[1] if q.dim() == 4 else q.shape[0]
-    if q_out is None:
+        desc.seqlen = ref.shape[1] if ref.dim() == 4 else ref.shape[0]
+    if q is not None and q_out is None:
         q_out = torch.empty_like(q)
     if k is not None and k_out is None:
         k_out = torch.empty_like(k)
     st = load_library().diffattn_rope_qk(ctypes.byref(desc), _ptr(positions) if positions is not None else None,
                                          _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(cos),
-                                         _ptr(sin), _ptr(q), _ptr(q_out), _ptr(k) if k is not None else None,
+                                         _ptr(sin), _ptr(q) if q is not None else None,
+                                         _ptr(q_out) if q is not None else None, _ptr(k) if k is not None else None,
                                          _ptr(k_out) if k is not None else None, _stream_handle(stream))
     if st != OK:
         raise DiffAttnError(st, "diffattn_rope_qk")
     return q_out, k_out
+
+
+def diffattn_rope_k(k, cos, sin, rot_dim: int, interleaved: bool, positions=None, cu_seqlens=None, k_out=None,
+                    stream=None):
+    """The rotary embedding of k alone (diffattn_rope_qk with num_heads = 0), the
+    companion of diffattn_fwd_rope_q. Returns k_out."""
+    return diffattn_rope_qk(None, k, cos, sin, rot_dim, interleaved, positions=positions, cu_seqlens=cu_seqlens,
+                            k_out=k_out, stream=stream)[1]
 
 
 # -------------------------------------------------------------- merge ---

@@ -133,11 +133,19 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // grid (head, query tile, sequence), or with the tiles outermost (head, sequence,
-    // query tile); either way the longest query tiles of a sequence are scheduled first
+    // grid (head group x query tile x head in group, 1, sequence), or with the tiles
+    // outermost (head, sequence, query tile); either way the longest query tiles of a
+    // sequence are scheduled first. A group's K / V (sized by the host) stays in L2
+    // while its CTAs stream it.
     const bool outer = p.dq_tiles_outer != 0;
-    const int h = blockIdx.x, seq = outer ? blockIdx.y : blockIdx.z;
-    const int qt = outer ? gridDim.z - 1 - blockIdx.z : gridDim.y - 1 - blockIdx.y;
+    int h, seq, qt;
+    if (outer) {
+        h = blockIdx.x, seq = blockIdx.y, qt = gridDim.z - 1 - blockIdx.z;
+    } else {
+        const int n_qt = (p.max_seqlen + BM - 1) / BM, hg = p.dq_group_heads;
+        const int grp = (int)blockIdx.x / (n_qt * hg), rem = (int)blockIdx.x - grp * (n_qt * hg);
+        h = grp * hg + rem % hg, seq = blockIdx.z, qt = n_qt - 1 - rem / hg;
+    }
     int start = 0, len = 0;
     if (!seq_bounds(p, seq, &start, &len)) return;
     if (qt * BM >= len) return;
@@ -409,9 +417,17 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     // grid (kv head, key tile, sequence), or with the tiles outermost (kv head,
     // sequence, key tile). Causal: key tile kt is seen by the query blocks from kt on,
     // so the first tiles carry the most work and are scheduled first
+    // (kv head group x key tile x kv head in group, 1, sequence): a group's Q / dD
+    // (sized by the host) stays in L2 while its CTAs stream it
     const bool outer = p.dkv_tiles_outer != 0;
-    const int g = blockIdx.x, seq = outer ? blockIdx.y : blockIdx.z;
-    const int kt = outer ? blockIdx.z : blockIdx.y;
+    int g, seq, kt;
+    if (outer) {
+        g = blockIdx.x, seq = blockIdx.y, kt = blockIdx.z;
+    } else {
+        const int n_kt = (p.max_seqlen + BK - 1) / BK, kg = p.dkv_group_kv;
+        const int grp = (int)blockIdx.x / (n_kt * kg), rem = (int)blockIdx.x - grp * (n_kt * kg);
+        g = grp * kg + rem % kg, seq = blockIdx.z, kt = rem / kg;
+    }
     int start = 0, len = 0;
     if (!seq_bounds(p, seq, &start, &len)) return;
     if (kt * BK >= len) return;
@@ -675,14 +691,16 @@ cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& m, cudaSt
     err = set_smem(diffattn_bwd_dkv_kernel, dkv::SMEM, dkv_done);
     if (err != cudaSuccess) return err;
     const int n_qt = (p.max_seqlen + dq::BM - 1) / dq::BM;
+    if (p.dq_group_heads < 1 || p.H % p.dq_group_heads != 0 || p.dkv_group_kv < 1 || p.Hkv % p.dkv_group_kv != 0)
+        return cudaErrorInvalidValue;
     const dim3 dq_grid = p.dq_tiles_outer ? dim3((unsigned)p.H, (unsigned)p.num_seqs, (unsigned)n_qt)
-                                          : dim3((unsigned)p.H, (unsigned)n_qt, (unsigned)p.num_seqs);
+                                          : dim3((unsigned)(p.H * n_qt), 1u, (unsigned)p.num_seqs);
     diffattn_bwd_dq_kernel<<<dq_grid, NT, dq::SMEM, stream>>>(
         m.q128, m.k128, m.v128, m.dd128, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const int n_kt = (p.max_seqlen + dkv::BK - 1) / dkv::BK;
     const dim3 dkv_grid = p.dkv_tiles_outer ? dim3((unsigned)p.Hkv, (unsigned)p.num_seqs, (unsigned)n_kt)
-                                            : dim3((unsigned)p.Hkv, (unsigned)n_kt, (unsigned)p.num_seqs);
+                                            : dim3((unsigned)(p.Hkv * n_kt), 1u, (unsigned)p.num_seqs);
     diffattn_bwd_dkv_kernel<<<dkv_grid, NT, dkv::SMEM, stream>>>(
         m.q64, m.k128, m.v128, m.dd64, p);
     return cudaGetLastError();

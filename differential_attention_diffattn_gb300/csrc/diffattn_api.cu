@@ -297,7 +297,7 @@ namespace {
 diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void* k, const void* v,
                            const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
                            int causal, const int* cu_seqlens, void* out, float* lse, void* o1, void* o2,
-                           void* stream) {
+                           void* stream, const diffattn_rope_q* rope = nullptr) {
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const bool train = lse != nullptr || o1 != nullptr || o2 != nullptr;
     if (train && (!lse || !o1 || !o2 || !aligned16(o1) || !aligned16(o2) ||
@@ -336,6 +336,13 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
 
     const bool bf16_tc = ds.dtype == DIFFATTN_DTYPE_BF16 && ds.d == 64;
     const bool f32_simt = ds.dtype == DIFFATTN_DTYPE_F32 && (ds.d == 16 || ds.d == 32 || ds.d == 64);
+    if (rope != nullptr) {  // the rotary embedding of q inside the kernels
+        if ((rope->rot_dim != ds.d && rope->rot_dim != 2 * ds.d) || (rope->rot_dim % 8) != 0 || rope->n_pos < 1 ||
+            (rope->interleaved != 0 && rope->interleaved != 1) || !rope->cos || !rope->sin ||
+            !aligned16(rope->cos) || !aligned16(rope->sin))
+            return DIFFATTN_ERR_INVALID_ARG;
+        if (!bf16_tc) return DIFFATTN_ERR_UNSUPPORTED;
+    }
     if (!bf16_tc && !f32_simt) return DIFFATTN_ERR_UNSUPPORTED;
     if (train && !bf16_tc) return DIFFATTN_ERR_UNSUPPORTED;
 
@@ -370,6 +377,13 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
     p.o1 = o1;
     p.o2 = o2;
     p.group_heads = fwd_group_heads(p.H, p.Hkv, p.max_seqlen);
+    if (rope != nullptr) {
+        p.rope_cos = rope->cos;
+        p.rope_sin = rope->sin;
+        p.rope_npos = rope->n_pos;
+        p.rope_dim = rope->rot_dim;
+        p.rope_interleaved = rope->interleaved;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
@@ -380,7 +394,10 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens) ||
         !encode_bf16_rows(&maps.out, out, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
-    const cudaError_t err = fwd_use_persistent(cu_seqlens != nullptr, p.max_seqlen, p.H, p.num_seqs)
+    // The rotary embedding of q is applied by the one-item-per-CTA kernel only: it
+    // stages each tile's cos / sin rows in its last K/V stage, which the persistent
+    // kernel does not have (its shared memory is all in use).
+    const cudaError_t err = (rope == nullptr && fwd_use_persistent(cu_seqlens != nullptr, p.max_seqlen, p.H, p.num_seqs))
                                 ? launch_fwd_bf16_persistent(p, maps, st)
                                 : launch_fwd_bf16_sm103a(p, maps, st);
     return err == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
@@ -406,6 +423,16 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     const CallRange nvtx_range("diffattn_fwd");
     return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
                       nullptr, nullptr, nullptr, stream);
+}
+
+diffattn_status diffattn_fwd_rope_q(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                                    const float* lambda, int lambda_per_head, float lambda_init,
+                                    const float* subln_w, int causal, const int* cu_seqlens,
+                                    const diffattn_rope_q* rope, void* out, void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_rope_q");
+    if (!rope) return DIFFATTN_ERR_INVALID_ARG;
+    return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
+                      nullptr, nullptr, nullptr, stream, rope);
 }
 
 diffattn_status diffattn_fwd_train(const diffattn_desc* desc, const void* q, const void* k, const void* v,
@@ -637,6 +664,18 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     p.timeout_ns = g_timeout_ns;
     p.dq_tiles_outer = causal && bwd_tiles_outermost(num_seqs, p.H, max_seqlen) ? 1 : 0;
     p.dkv_tiles_outer = causal && bwd_tiles_outermost(num_seqs, p.Hkv, max_seqlen) ? 1 : 0;
+    // launch groups whose streamed operands fit in 32 MB of L2: for the dQ kernel the
+    // K / V of its heads (as the forward), for the dK/dV kernel the Q and dD of every
+    // head of its kv heads (2d + dv bf16 and 16 bytes of row statistics per token)
+    p.dq_group_heads = fwd_group_heads(p.H, p.Hkv, max_seqlen);
+    {
+        const int G = p.H / p.Hkv;
+        const double kv_group_bytes = (double)max_seqlen * G * ((2 * 64 + 128) * 2 + 16);
+        int kg = (int)((32.0 * (1 << 20)) / (kv_group_bytes > 1.0 ? kv_group_bytes : 1.0));
+        kg = kg < 1 ? 1 : (kg > p.Hkv ? p.Hkv : kg);
+        while (p.Hkv % kg != 0) --kg;
+        p.dkv_group_kv = kg;
+    }
     BwdTensorMaps m;
     const uint64_t qw = (uint64_t)ds.num_heads * 2 * ds.d, kw = (uint64_t)ds.num_kv_heads * 2 * ds.d;
     const uint64_t vw = (uint64_t)ds.num_kv_heads * ds.dv, dw = (uint64_t)ds.num_heads * ds.dv;
@@ -678,13 +717,14 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
     const CallRange nvtx_range("diffattn_rope_qk");
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_rope_desc& ds = *desc;
-    if (ds.tokens < 0 || ds.num_heads < 1 || ds.num_kv_heads < 0 || ds.d < 4 || (ds.d % 4) != 0 || ds.n_pos < 1)
+    if (ds.tokens < 0 || ds.num_heads < 0 || ds.num_kv_heads < 0 || ds.num_heads + ds.num_kv_heads < 1 || ds.d < 4 ||
+        (ds.d % 4) != 0 || ds.n_pos < 1)
         return DIFFATTN_ERR_INVALID_ARG;
     if (ds.dtype != DIFFATTN_DTYPE_F32 && ds.dtype != DIFFATTN_DTYPE_BF16) return DIFFATTN_ERR_INVALID_ARG;
     if ((ds.rot_dim != ds.d && ds.rot_dim != 2 * ds.d) || (ds.rot_dim % 8) != 0) return DIFFATTN_ERR_INVALID_ARG;
     if (ds.tokens == 0) return DIFFATTN_OK;
-    if (!cos_table || !sin_table || !q_in || !q_out) return DIFFATTN_ERR_INVALID_ARG;
-    if (!aligned16(cos_table) || !aligned16(sin_table) || !aligned16(q_in) || !aligned16(q_out))
+    if (!cos_table || !sin_table || !aligned16(cos_table) || !aligned16(sin_table)) return DIFFATTN_ERR_INVALID_ARG;
+    if (ds.num_heads > 0 && (!q_in || !q_out || !aligned16(q_in) || !aligned16(q_out)))
         return DIFFATTN_ERR_INVALID_ARG;
     if (ds.num_kv_heads > 0 && (!k_in || !k_out || !aligned16(k_in) || !aligned16(k_out)))
         return DIFFATTN_ERR_INVALID_ARG;
@@ -702,8 +742,8 @@ diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* posi
     unsigned int* err_word = nullptr;
     if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
     RopeParams p{};
-    p.q_in = q_in;
-    p.q_out = q_out;
+    p.q_in = ds.num_heads > 0 ? q_in : nullptr;
+    p.q_out = ds.num_heads > 0 ? q_out : nullptr;
     p.k_in = ds.num_kv_heads > 0 ? k_in : nullptr;
     p.k_out = ds.num_kv_heads > 0 ? k_out : nullptr;
     p.positions = positions;

@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "rope_q.cuh"
 #include "sm103a_ptx.cuh"
 
 namespace diffattn {
@@ -80,6 +81,8 @@ struct Misc {  // lives at OFF_MISC
     uint64_t p_ready[2];
     uint64_t o_full;
     uint64_t w_full;  // the norm weight and lambda have landed in shared memory
+    uint64_t q_rot;   // with the rotary embedding: Q rotated in shared memory
+    uint64_t tab_full;  // with the rotary embedding: the tile's cos / sin rows in shared memory
     uint32_t tmem_base;
     int abort_flag;
     float lam;        // lambda of this head, and the norm weight, staged at setup
@@ -149,6 +152,16 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     auto bar_p_ready = [&](int c) { return smem_u32(&ms.p_ready[c]); };
     const uint32_t bar_o_full = smem_u32(&ms.o_full);
     const uint32_t bar_w_full = smem_u32(&ms.w_full);
+    const uint32_t bar_q_rot = smem_u32(&ms.q_rot);
+    const uint32_t bar_tab_full = smem_u32(&ms.tab_full);
+    const bool rope = p.rope_cos != nullptr;
+    // With the rotary embedding the tile's cos / sin rows (one contiguous block per
+    // table) come by bulk copy into the last K/V stage, whose first load waits until
+    // Q has been rotated: read from shared memory, the 64 KB of table entries a
+    // tile needs do not queue ahead of the Q and K loads (as 4096 plain loads a CTA
+    // they had delayed Q by ~4.6 us).
+    const int rope_rows = rope ? max(0, min(BM, p.rope_npos - qt * BM)) : 0;
+    const uint32_t rope_row_bytes = rope ? (uint32_t)(p.rope_dim / 2) * 4u : 0u;
     const uint32_t sq = sbase + OFF_Q;
     auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
     auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
@@ -172,7 +185,9 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     };
     // With the test hook set, no load is issued: the barriers the other roles
     // wait on are never armed, so their bounded waits run out.
-    const int early = p.inject == 1 ? 0 : min(n_kv, STAGES);  // tiles loaded before the CTA barrier
+    // tiles loaded before the CTA barrier (with the rotary embedding the last stage
+    // holds the tables until Q is rotated)
+    const int early = p.inject == 1 ? 0 : min(n_kv, rope ? STAGES - 1 : STAGES);
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -190,6 +205,8 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             }
             mbar_init(bar_o_full, 1);
             mbar_init(bar_w_full, 32);  // one cp.async arrive per lane of this warp
+            mbar_init(bar_q_rot, 256);  // every softmax thread, after rotating its part of Q
+            mbar_init(bar_tab_full, 1);
             ms.abort_flag = 0;
             fence_barrier_init();
             if (p.inject != 1) {
@@ -198,6 +215,15 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 tma_load_2d(sq, &tm_q, bar_q_full, h * 2 * HD, row_q, pol_q);
                 tma_load_2d(sq + BOX_BYTES, &tm_q, bar_q_full, h * 2 * HD + HD, row_q, pol_q);
                 for (int j = 0; j < early; ++j) load_kv(j);  // fresh stages: nothing to wait for
+                if (rope) {
+                    const uint32_t tab = sk(STAGES - 1), bytes = (uint32_t)rope_rows * rope_row_bytes;
+                    mbar_arrive_expect_tx(bar_tab_full, 2u * bytes);
+                    if (bytes > 0) {
+                        const size_t off = (size_t)qt * BM * (p.rope_dim / 2);
+                        bulk_copy_g2s(tab, p.rope_cos + off, bytes, bar_tab_full);
+                        bulk_copy_g2s(tab + 32768u, p.rope_sin + off, bytes, bar_tab_full);
+                    }
+                }
             }
         }
         __syncwarp();  // the barriers exist before any lane arrives on them
@@ -219,12 +245,14 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             for (int j = early; j < n_kv; ++j) {
                 const int s = j % STAGES;
                 const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
+                if (rope && j == STAGES - 1 && !mbar_wait(bar_q_rot, 0, ab)) break;  // the tables are read
                 if (!mbar_wait(bar_kv_empty(s), ph ^ 1u, ab)) break;
                 load_kv(j);
                 issued = j + 1;
             }
             // Let every copy this CTA started land before shared memory goes away.
             mbar_wait_drain(bar_q_full, 0, p.timeout_ns);
+            if (rope) mbar_wait_drain(bar_tab_full, 0, p.timeout_ns);
             for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
                 const uint32_t ph = (uint32_t)(j / STAGES) & 1u;
                 mbar_wait_drain(bar_k_full(j % STAGES), ph, p.timeout_ns);
@@ -259,7 +287,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) mma_ts_elect(d, a + kk * 8, b0 + kk * VSTEP, idesc_pv, kk > 0 ? 1u : acc0);
         };
-        bool ok = warp_all(mbar_wait(bar_q_full, 0, ab)) && warp_all(mbar_wait(bar_k_full(0), 0, ab));
+        bool ok = warp_all(mbar_wait(rope ? bar_q_rot : bar_q_full, 0, ab)) && warp_all(mbar_wait(bar_k_full(0), 0, ab));
         if (ok) { tc_fence_after(); issue_s(0, 0); issue_s(1, 0); }
         for (int j = 0; ok && j < n_kv; ++j) {
             const int s = j % STAGES;
@@ -297,6 +325,27 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         float m = -INFINITY;  // running max of scores * scale * log2(e)
         float l = 0.f;        // running sum of 2^(x - m)
         bool ok = true;
+        if (rope) {
+            // Rotary embedding of the tile's queries before the first score MMA. Thread t
+            // takes unit t % U of rows t / U + (256 / U) m: consecutive threads read
+            // consecutive table entries and distinct Q chunks (no bank conflicts).
+            const int t = threadIdx.x, U = rope_units(p.rope_interleaved), step = 256 / U, u = t % U;
+            ok = warp_all(mbar_wait(bar_q_full, 0, ab)) && warp_all(mbar_wait(bar_tab_full, 0, ab));
+            bool bad = false;
+            if (ok) {
+                const uint32_t tab = sk(STAGES - 1);
+                for (int rr = t / U; rr < BM; rr += step) {
+                    if (rr >= rope_rows) {  // position past the tables: left unrotated
+                        bad |= qt * BM + rr < len;
+                        continue;
+                    }
+                    rope_unit_smem(sq, BOX_BYTES, rr, u, tab, tab + 32768u, p.rope_dim, p.rope_interleaved);
+                }
+            }
+            if (bad) atomicOr(p.error_word, kErrBadPositions);
+            fence_proxy_async_smem();  // the rotated rows, visible to the MMAs
+            mbar_arrive(bar_q_rot);
+        }
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = warp_all(mbar_wait(bar_s_full(c), (uint32_t)j & 1u, ab)))) break;
             tc_fence_after();

@@ -40,6 +40,9 @@ struct FwdParams {
     int inject;               // test hook: 1 = the copy producer issues no loads; 2 = the persistent
                               // kernel's epilogue pauses ~20 us before each item
     int group_heads;          // one-item-per-CTA bf16 kernel: heads per launch group (divides H)
+    const float* rope_cos;    // rotary embedding of q inside the bf16 kernels (null: q is used as given):
+    const float* rope_sin;    //   fp32 [rope_npos][rope_dim / 2] tables; position = index in the sequence
+    int rope_npos, rope_dim, rope_interleaved;
     float* lse;               // training outputs (all null, or all set; bf16 kernel only):
     void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
     void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c
@@ -97,6 +100,8 @@ struct BwdParams {
     unsigned long long timeout_ns;
     int dq_tiles_outer;        // grid order of the dQ kernel: 1 (head, sequence, tile), 0 (head, tile, sequence)
     int dkv_tiles_outer;       // the same for the dK/dV kernel (kv heads)
+    int dq_group_heads;        // (head, tile) order: heads per launch group of the dQ kernel (divides H)
+    int dkv_group_kv;          // kv heads per launch group of the dK/dV kernel (divides Hkv)
 };
 
 // TMA descriptors of the backward kernels: q and dD with 128- and 64-row boxes,

@@ -113,8 +113,9 @@ __device__ __forceinline__ void rotate_rows(const void* src, void* dst, size_t r
         for (int m = 0; m < 4; ++m) {
             // interleaved: pair m = coordinates (2m, 2m+1); half-split: (m, 4 + m) of the two chunks
             const int ia = INTERLEAVED ? 2 * m : m, ib = INTERLEAVED ? 2 * m + 1 : 4 + m;
-            g[ia] = ok ? f[ia] * cc[m] - f[ib] * ss[m] : f[ia];  // outside the tables:
-            g[ib] = ok ? f[ib] * cc[m] + f[ia] * ss[m] : f[ib];  // copied through
+            // the roundings spelled out, as in the forward kernels' own rotation of q
+            g[ia] = ok ? __fmaf_rn(f[ia], cc[m], -__fmul_rn(f[ib], ss[m])) : f[ia];  // outside the tables:
+            g[ib] = ok ? __fmaf_rn(f[ib], cc[m], __fmul_rn(f[ia], ss[m])) : f[ib];   // copied through
         }
         Vec8<T>::store(dst, o, gap, !INTERLEAVED, g);
     }
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(256) diffattn_rope_qk_kernel(const RopeParams 
     } else if (w == 0) {
         atomicOr(p.error_word, kErrBadPositions);
     }
-    rotate_rows<T, INTERLEAVED>(p.q_in, p.q_out, (size_t)t * p.H, p.H, p.width, off, gap, cc, ss, ok);
+    if (p.H > 0) rotate_rows<T, INTERLEAVED>(p.q_in, p.q_out, (size_t)t * p.H, p.H, p.width, off, gap, cc, ss, ok);
     if (p.Hkv > 0)
         rotate_rows<T, INTERLEAVED>(p.k_in, p.k_out, (size_t)t * p.Hkv, p.Hkv, p.width, off, gap, cc, ss, ok);
 }

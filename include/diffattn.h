@@ -331,6 +331,7 @@ typedef struct diffattn_rope_desc {
     long long tokens;   /* rows of q (and of k)                                         */
     int num_heads;      /* H: q is [tokens][H][2d]                                      */
     int num_kv_heads;   /* Hkv: k is [tokens][Hkv][2d]; 0 rotates q only                */
+                        /* (num_heads 0 rotates k only; q_in / q_out are then ignored)  */
     int d;              /* component dim; head rows are 2d wide; d % 4 == 0             */
     int dtype;          /* diffattn_dtype of q and k                                     */
     int rot_dim;        /* d or 2d                                                       */
@@ -365,6 +366,51 @@ diffattn_status diffattn_rope_tables(double theta, int n_pos, int rot_dim, float
 diffattn_status diffattn_rope_qk(const diffattn_rope_desc* desc, const int* positions, const int* cu_seqlens,
                                  const float* cos_table, const float* sin_table, const void* q_in, void* q_out,
                                  const void* k_in, void* k_out, void* stream);
+
+/*
+ * The rotary embedding of q, applied by the forward kernels themselves: each
+ * query tile is rotated in shared memory once its TMA load lands, before the
+ * first score MMA reads it, so q goes through the forward unrotated and is not
+ * written back. Same rule, tables and rounding as diffattn_rope_qk (the two give
+ * the same bits), positions = the query's index inside its sequence (dense
+ * batches and cu_seqlens alike).
+ *  cos, sin   : device fp32 [n_pos][rot_dim / 2] from diffattn_rope_tables,
+ *               16-byte aligned, caller-owned
+ *  rot_dim    : d or 2d, a multiple of 8; interleaved: 0 or 1
+ */
+typedef struct diffattn_rope_q {
+    const float* cos;
+    const float* sin;
+    int n_pos;
+    int rot_dim;
+    int interleaved;
+} diffattn_rope_q;
+
+/*
+ * diffattn_fwd on q before its rotary embedding: the kernels rotate each query
+ * tile as it arrives ("LlamaDiffSdpaAttention.py", forward, "Apply RoPE before
+ * splitting"; "Add an isolated implementation of FlashDiffAttention", test
+ * script, apply_rotary_emb(..., interleaved=True) on the doubled heads). k must
+ * already be rotated, e.g. by diffattn_rope_qk with num_heads = 0 (k only): every
+ * query tile reads every key tile it sees, so keys are rotated once, apart.
+ * Arguments, layouts and results otherwise as diffattn_fwd (the same bits as
+ * diffattn_rope_qk then diffattn_fwd). It runs on the one-item-per-CTA forward
+ * kernel, which stages each tile's cos / sin rows in shared memory: measured on
+ * GB300 it beats the separate q pass on small or launch-bound calls (B = 2,
+ * T = 512: 22.0 against 29.7 us with k's pass) and ties it on long sequences
+ * (T = 16384), but on batches of short sequences, where diffattn_fwd takes the
+ * persistent kernel, diffattn_rope_qk on q and k then diffattn_fwd is faster
+ * (B = 4, T = 2048: 121 against 136 us).
+ * Supported: bf16, d = 64 (UNSUPPORTED otherwise).
+ * Errors: as diffattn_fwd; INVALID_ARG for a null `rope`, null or misaligned
+ * tables, rot_dim not d or 2d or not a multiple of 8, n_pos < 1. A query whose
+ * position is outside [0, n_pos) is left unrotated and
+ * diffattn_get_device_status returns DIFFATTN_ERR_BAD_POSITIONS.
+ */
+diffattn_status diffattn_fwd_rope_q(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                                    const float* lambda, int lambda_per_head, float lambda_init,
+                                    const float* subln_w, int causal, const int* cu_seqlens,
+                                    const diffattn_rope_q* rope, void* out, void* stream);
 
 /*
  * Context-parallel merge. The pages give no context-parallel scheme; it

@@ -233,3 +233,33 @@ def test_cache_forward_split_plan_from_host_lengths(lib):
     per_split = lambda batch, q_len: batch * q_len * 16 * 2 * (128 + 2) * 4  # noqa: E731
     assert ws(16, 4, 8192, rag) == 7 * per_split(16, 4)
     assert ws(8, 1, 16384, [16384] * 8) == 8 * per_split(8, 1)
+
+
+def test_fused_rope_forward_rejects_on_host(lib):
+    vp = ctypes.c_void_p
+
+    def call(rope_kw=None, **desc_kw):
+        base = dict(batch=1, seqlen=256, num_heads=16, num_kv_heads=4, d=64, dv=128, dtype=_lib.DTYPE_BF16, eps=1e-5)
+        base.update(desc_kw)
+        d = _lib.DiffAttnDesc(**base)
+        rope = None
+        if rope_kw is not None:
+            r = dict(cos=FAKE, sin=FAKE, n_pos=1024, rot_dim=128, interleaved=0)
+            r.update(rope_kw)
+            rope = ctypes.byref(_lib.DiffAttnRopeQ(**r))
+        return lib.diffattn_fwd_rope_q(ctypes.byref(d), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0, 0.2, vp(FAKE),
+                                       1, None, rope, vp(FAKE), None)
+    assert call(None) == 1                           # no rotary tables
+    assert call(dict(rot_dim=96)) == 1               # neither d nor 2d
+    assert call(dict(rot_dim=12), d=12, dv=24) == 1  # not a multiple of 8
+    assert call(dict(n_pos=0)) == 1
+    assert call(dict(interleaved=2)) == 1
+    assert call(dict(cos=FAKE + 4)) == 1             # misaligned table
+    assert call(dict(sin=0)) == 1
+    assert call(dict(), dtype=_lib.DTYPE_F32) == 2   # the fp32 path has no fused rotation
+    assert call(dict(), batch=0) == 0                # empty: nothing launched
+
+
+def test_rope_k_only_and_neither_on_host(lib):
+    d = _rope_desc(num_heads=0, num_kv_heads=0)
+    assert _rope(lib, d) == 1

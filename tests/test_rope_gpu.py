@@ -127,3 +127,76 @@ def test_rope_then_attention_matches_oracle(rot, inter):
     olam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, oli)
     want = orc.forward_rows(inp.cu_seqlens, q64, k64, inp.v, olam, oli, inp.subln_w, wl.eps, True)
     compare(y, want, "bf16")
+
+
+def _fused_case(wl, seq_lens, seed, dense):
+    inp = W.generate(wl, seed=seed, seq_lens=seq_lens)
+    B, T = len(inp.seq_lens), inp.seq_lens[0]
+    sh = (lambda x: x.cuda().view(B, T, *x.shape[1:])) if dense else (lambda x: x.cuda())
+    kw = {} if dense else dict(cu_seqlens=inp.cu_seqlens.cuda(), max_seqlen=inp.max_seqlen)
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(*(x.cuda() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)), li)
+    return inp, sh, kw, li, lam
+
+
+# A dense 4 x 1024 batch (its plain forward takes the persistent kernel, the
+# fused one the one-item-per-CTA kernel: the two give the same bits) and three
+# packed sequences (both on the one-item-per-CTA kernel).
+KERNEL_CASES = [("dense_4x1024", [1024] * 4, True), ("packed_3", [700, 129, 195], False)]
+
+
+@pytest.mark.parametrize("rot,inter", PLACEMENTS)
+@pytest.mark.parametrize("case,lens,dense", KERNEL_CASES)
+def test_fused_rotation_equals_separate_pass(rot, inter, case, lens, dense):
+    """q rotated inside the forward kernel against q rotated by the separate
+    pass and then the plain forward: the same bits (the same expressions with the
+    same explicit roundings, the same tables)."""
+    wl = W.with_overrides(W.WORKLOADS["b2_t512_gqa"], random_subln=True)
+    inp, sh, kw, li, lam = _fused_case(wl, lens, 31, dense)
+    q, k, v, w = sh(inp.q), sh(inp.k), sh(inp.v), inp.subln_w.cuda()
+    cos, sin = da.diffattn_rope_tables(10000.0, 2048, rot)
+    cu = kw.get("cu_seqlens")
+    qr, kr = da.diffattn_rope_qk(q, k, cos, sin, rot, inter, cu_seqlens=cu)
+    kr_only = da.diffattn_rope_k(k, cos, sin, rot, inter, cu_seqlens=cu)
+    assert torch.equal(kr_only, kr)
+    ref = da.diffattn_fwd(qr, kr, v, lam, li, w, causal=True, eps=wl.eps, **kw)
+    got = da.diffattn_fwd_rope_q(q, kr_only, v, lam, li, w, cos, sin, rot, inter, causal=True, eps=wl.eps, **kw)
+    assert da.diffattn_get_device_status() == 0
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("rot,inter", [(128, False), (64, True)])
+def test_fused_rope_then_attention_matches_oracle(rot, inter):
+    """The two placements end to end through the fused entry: k rotated by the
+    separate pass, q inside the forward; the oracle rotates in fp64 and runs its
+    own forward."""
+    wl = W.with_overrides(W.WORKLOADS["b2_t512_gqa"], random_subln=True)
+    inp = W.generate(wl, seed=21, seq_lens=[700, 129, 195])
+    theta, n_pos = 10000.0, 1024
+    cos, sin = da.diffattn_rope_tables(theta, n_pos, rot)
+    cu = inp.cu_seqlens.cuda()
+    kr = da.diffattn_rope_k(inp.k.cuda(), cos, sin, rot, inter, cu_seqlens=cu)
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(*(x.cuda() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)), li)
+    y = da.diffattn_fwd_rope_q(inp.q.cuda(), kr, inp.v.cuda(), lam, li, inp.subln_w.cuda(), cos, sin, rot, inter,
+                               causal=True, cu_seqlens=cu, max_seqlen=inp.max_seqlen, eps=wl.eps)
+    assert da.diffattn_get_device_status() == 0
+    wc, ws = orope.tables(theta, n_pos, rot)
+    pos = orope.positions_from_cu_seqlens(inp.cu_seqlens.numpy())
+    q64 = orope.apply(inp.q.double().numpy(), pos, wc, ws, rot, inter)
+    k64 = orope.apply(inp.k.double().numpy(), pos, wc, ws, rot, inter)
+    oli = orc.lambda_init(wl.depth)
+    olam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, oli)
+    want = orc.forward_rows(inp.cu_seqlens, q64, k64, inp.v, olam, oli, inp.subln_w, wl.eps, True)
+    compare(y, want, "bf16")
+
+
+@pytest.mark.parametrize("case,lens,dense", KERNEL_CASES)
+def test_fused_rotation_reports_positions_past_the_tables(case, lens, dense):
+    wl = W.WORKLOADS["b2_t512_gqa"]
+    inp, sh, kw, li, lam = _fused_case(wl, lens, 32, dense)
+    q, k, v, w = sh(inp.q), sh(inp.k), sh(inp.v), inp.subln_w.cuda()
+    cos, sin = da.diffattn_rope_tables(10000.0, 600, 64)  # shorter than the longest sequence
+    da.diffattn_fwd_rope_q(q, k, v, lam, li, w, cos, sin, 64, True, causal=True, eps=wl.eps, **kw)
+    assert da.diffattn_get_device_status() == da._lib.ERR_BAD_POSITIONS
+    assert da.diffattn_get_device_status() == 0
