@@ -890,9 +890,15 @@ EXTRA_FWD = ("tiny_f32", "b2_t512_gqa", "llama1b_b4_t2048", "varlen_32k")
 def run_extras(args, local_rank):
     import torch
 
+    from differential_attention_diffattn_gb300 import workloads as W
+    W_KV = set(W.KV_WORKLOADS)
+
     def sub(**over):
         a = argparse.Namespace(**vars(args))
         a.steps, a.warmup, a.e2e_steps = args.extra_steps, max(3, min(args.warmup, 5)), 3
+        # calls of tens of microseconds get more steps, so that the figure is not a few launches'
+        if over.get("workload") in ("tiny_f32", "b2_t512_gqa") or over.get("workload") in W_KV:
+            a.steps = max(args.extra_steps, 200)
         a.no_cpu_baseline, a.rope, a.out_proj, a.backward, a.cp = True, None, False, False, 0
         for k, v in over.items():
             setattr(a, k, v)

@@ -137,3 +137,21 @@ def test_host_lengths_on_mixed_batch():
     # one long sequence among short ones: the plan spreads the long one over many splits
     inp = W.generate_kv(kvw(batch=4, capacity=4096), seed=52, lengths=[100, 200, 4096, 30])
     compare(run_gpu_kv(inp, host_seqlens=True), oracle_kv(inp), "bf16")
+
+
+@pytest.mark.parametrize("hint", ["capacity", "q_len", "reversed"])
+def test_host_lengths_are_only_a_plan_hint(hint):
+    """Host lengths that disagree with the device's change only the split count:
+    the kernels use the device lengths, so the results stay those of the oracle."""
+    inp = W.generate_kv(kvw(batch=4, capacity=3000, q_len=2), seed=53, lengths=[3000, 40, 1700, 2])
+    wl = inp.wl
+    wrong = {"capacity": [wl.capacity] * 4, "q_len": [wl.q_len] * 4,
+             "reversed": inp.cache_seqlens.flip(0).tolist()}[hint]
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(inp.lambda_q1.cuda(), inp.lambda_k1.cuda(), inp.lambda_q2.cuda(), inp.lambda_k2.cuda(),
+                             li)
+    y = da.diffattn_fwd_kvcache(inp.q.cuda(), inp.k_cache.cuda(), inp.v_cache.cuda(), lam, li, inp.subln_w.cuda(),
+                                cache_seqlens=inp.cache_seqlens.cuda(), causal=wl.causal, eps=wl.eps,
+                                host_seqlens=wrong)
+    assert da.diffattn_get_device_status() == 0
+    compare(y, oracle_kv(inp), "bf16")

@@ -200,3 +200,29 @@ def test_fused_rotation_reports_positions_past_the_tables(case, lens, dense):
     da.diffattn_fwd_rope_q(q, k, v, lam, li, w, cos, sin, 64, True, causal=True, eps=wl.eps, **kw)
     assert da.diffattn_get_device_status() == da._lib.ERR_BAD_POSITIONS
     assert da.diffattn_get_device_status() == 0
+
+
+def test_fused_rotation_non_causal_per_head_lambda_and_k_positions():
+    """The fused entry with a non-causal mask, a lambda per head and a random
+    weight, k rotated by explicit positions (those of the packed layout), against
+    the oracle."""
+    wl = W.with_overrides(W.WORKLOADS["b2_t512_gqa"], causal=False, lambda_per_head=True, random_subln=True)
+    inp = W.generate(wl, seed=33, seq_lens=[300, 77, 129])
+    rot, inter, theta, n_pos = 64, False, 10000.0, 512
+    cos, sin = da.diffattn_rope_tables(theta, n_pos, rot)
+    pos = orope.positions_from_cu_seqlens(inp.cu_seqlens.numpy())
+    kr = da.diffattn_rope_k(inp.k.cuda(), cos, sin, rot, inter,
+                            positions=torch.tensor(pos, dtype=torch.int32).cuda())
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(*(x.cuda() for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)), li)
+    assert lam.numel() == wl.num_heads
+    y = da.diffattn_fwd_rope_q(inp.q.cuda(), kr, inp.v.cuda(), lam, li, inp.subln_w.cuda(), cos, sin, rot, inter,
+                               causal=False, cu_seqlens=inp.cu_seqlens.cuda(), max_seqlen=inp.max_seqlen, eps=wl.eps)
+    assert da.diffattn_get_device_status() == 0
+    wc, ws = orope.tables(theta, n_pos, rot)
+    q64 = orope.apply(inp.q.double().numpy(), pos, wc, ws, rot, inter)
+    k64 = orope.apply(inp.k.double().numpy(), pos, wc, ws, rot, inter)
+    oli = orc.lambda_init(wl.depth)
+    olam = orc.lambda_values(inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2, oli)
+    want = orc.forward_rows(inp.cu_seqlens, q64, k64, inp.v, olam, oli, inp.subln_w, wl.eps, False)
+    compare(y, want, "bf16")

@@ -78,3 +78,23 @@ def test_noalloc_takes_fewer_splits_when_the_planned_ones_do_not_fit():
     for _ in range(2):
         got, ref = _run_both(inp)
         compare(got, ref.double().cpu().numpy(), "bf16")
+
+
+def test_noalloc_with_host_lengths():
+    """The allocation-free entry with a host copy of the lengths (the split plan
+    from them) against the workspace entry given the same lengths."""
+    wl = W.KV_WORKLOADS["decode_b16_q4_ragged"]
+    inp = W.generate_kv(wl, seed=64)
+    dev = "cuda"
+    li = da.diffattn_lambda_init(wl.depth)
+    lam = da.diffattn_lambda(inp.lambda_q1.to(dev), inp.lambda_k1.to(dev), inp.lambda_q2.to(dev),
+                             inp.lambda_k2.to(dev), li)
+    args = (inp.q.to(dev), inp.k_cache.to(dev), inp.v_cache.to(dev), lam, li, inp.subln_w.to(dev))
+    lens = inp.cache_seqlens.to(dev)
+    host = inp.cache_seqlens.tolist()
+    ref = da.diffattn_fwd_kvcache(*args, cache_seqlens=lens, causal=wl.causal, eps=wl.eps, host_seqlens=host)
+    for _ in range(2):
+        got = da.diffattn_fwd_kvcache_noalloc(*args, cache_seqlens=lens, causal=wl.causal, eps=wl.eps,
+                                              host_seqlens=host)
+        assert da.diffattn_get_device_status() == 0
+        compare(got, ref.double().cpu().numpy(), "bf16")
