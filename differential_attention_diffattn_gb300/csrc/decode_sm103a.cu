@@ -133,6 +133,51 @@ diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid
     }
     const int n_tiles = (k1 - k0 + TK - 1) / TK;
 
+    auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
+    auto bar_v_full = [&](int s) { return smem_u32(&ms.v_full[s]); };
+    auto bar_kv_empty = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    auto bar_s_full = [&](int bf) { return smem_u32(&ms.s_full[bf]); };
+    auto bar_p_ready = [&](int bf) { return smem_u32(&ms.p_ready[bf]); };
+    const uint32_t bar_pv_done = smem_u32(&ms.pv_done), bar_o_full = smem_u32(&ms.o_full);
+    auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
+    auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
+
+    // The producer lane initialises the barriers and at once issues the first
+    // STAGES K / V tiles (fresh stages: nothing to wait for), before the query
+    // boxes are filled and the CTA meets at its barrier: the cache rows are in
+    // flight while the queries are gathered.
+    const int row0 = b * p.capacity + k0;
+    const int n_pre = min(n_tiles, STAGES);
+    auto issue_kv = [&](int j, uint64_t pol) {
+        const int s = j % STAGES;
+        const int row = row0 + j * TK;  // rows past the split are masked, past the cache read as zero
+        mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
+        tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol);
+        tma_load_2d(sk(s) + KVBOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol);
+        mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
+        tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol);
+        tma_load_2d(sv(s) + KVBOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol);
+    };
+    if (warp == PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_k_full(s), 1);
+            mbar_init(bar_v_full(s), 1);
+            mbar_init(bar_kv_empty(s), 1);
+        }
+        for (int bf = 0; bf < 2; ++bf) {
+            mbar_init(bar_s_full(bf), 1);
+            mbar_init(bar_p_ready(bf), 32 * SOFTMAX_WARPS);
+        }
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_o_full, 1);
+        ms.abort_flag = 0;
+        fence_barrier_init();
+        const uint64_t pol = l2_policy_evict_first();  // the cache is streamed once
+        for (int j = 0; j < n_pre; ++j) issue_kv(j, pol);
+    }
+
     // ---- stacked query boxes (128-byte swizzle: row x at x * 128 B, 16-byte
     // chunk c of the row at physical chunk c ^ (x % 8)); every other row zero
     {
@@ -152,32 +197,6 @@ diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid
         fence_proxy_async_smem();  // the boxes, visible to the tensor cores
     }
 
-    auto bar_k_full = [&](int s) { return smem_u32(&ms.k_full[s]); };
-    auto bar_v_full = [&](int s) { return smem_u32(&ms.v_full[s]); };
-    auto bar_kv_empty = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
-    auto bar_s_full = [&](int bf) { return smem_u32(&ms.s_full[bf]); };
-    auto bar_p_ready = [&](int bf) { return smem_u32(&ms.p_ready[bf]); };
-    const uint32_t bar_pv_done = smem_u32(&ms.pv_done), bar_o_full = smem_u32(&ms.o_full);
-    auto sk = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES; };
-    auto sv = [&](int s) { return sbase + OFF_STAGE0 + (uint32_t)s * STAGE_BYTES + K_BYTES; };
-
-    if (warp == PRODUCER_WARP && lane == 0) {
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_k_full(s), 1);
-            mbar_init(bar_v_full(s), 1);
-            mbar_init(bar_kv_empty(s), 1);
-        }
-        for (int bf = 0; bf < 2; ++bf) {
-            mbar_init(bar_s_full(bf), 1);
-            mbar_init(bar_p_ready(bf), 32 * SOFTMAX_WARPS);
-        }
-        mbar_init(bar_pv_done, 1);
-        mbar_init(bar_o_full, 1);
-        ms.abort_flag = 0;
-        fence_barrier_init();
-    }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -189,18 +208,10 @@ diffattn_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid
         // ================================================= TMA producer ===
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();  // the cache is streamed once
-            const int row0 = b * p.capacity + k0;
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % STAGES;
-                if (!mbar_wait(bar_kv_empty(s), ((uint32_t)(j / STAGES) & 1u) ^ 1u, ab)) break;
-                const int row = row0 + j * TK;  // rows past the split are masked, past the cache read as zero
-                mbar_arrive_expect_tx(bar_k_full(s), K_BYTES);
-                tma_load_2d(sk(s), &tm_k, bar_k_full(s), g * 2 * HD, row, pol);
-                tma_load_2d(sk(s) + KVBOX_BYTES, &tm_k, bar_k_full(s), g * 2 * HD + HD, row, pol);
-                mbar_arrive_expect_tx(bar_v_full(s), V_BYTES);
-                tma_load_2d(sv(s), &tm_v, bar_v_full(s), g * DV, row, pol);
-                tma_load_2d(sv(s) + KVBOX_BYTES, &tm_v, bar_v_full(s), g * DV + 64, row, pol);
+            int issued = n_pre;  // issued in the prologue
+            for (int j = n_pre; j < n_tiles; ++j) {
+                if (!mbar_wait(bar_kv_empty(j % STAGES), ((uint32_t)(j / STAGES) & 1u) ^ 1u, ab)) break;
+                issue_kv(j, pol);
                 issued = j + 1;
             }
             for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
