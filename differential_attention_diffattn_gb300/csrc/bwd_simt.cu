@@ -105,8 +105,8 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
             st.x = *reinterpret_cast<uint32_t*>(&lo2);
             st.y = *reinterpret_cast<uint32_t*>(&hi2);
             reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
-            if (lane == 0)
-                reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(lse1, lse2, d1, d2);
+            if (lane == 0)  // negated: the backward kernels add them to products
+                reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(-lse1, -lse2, -d1, -d2);
         }
     }
 #pragma unroll

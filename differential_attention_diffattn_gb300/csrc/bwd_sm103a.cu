@@ -83,8 +83,9 @@ template <bool MASK>
 __device__ __forceinline__ void dq_keys32(const uint32_t (&s1)[32], const uint32_t (&s2)[32],
                                           const uint32_t (&dp)[32], const float4 rs, float lam, float sl2, float sc,
                                           int nvis, uint32_t (&d1)[16], uint32_t (&d2)[16]) {
-    const uint64_t sl2p = f2_pack(sl2, sl2), nl1 = f2_pack(-rs.x, -rs.x), nl2 = f2_pack(-rs.y, -rs.y);
-    const uint64_t nd1 = f2_pack(-rs.z, -rs.z), nlam = f2_pack(-lam, -lam), lamd2 = f2_pack(lam * rs.w, lam * rs.w);
+    // rs holds the row's statistics negated: (-lse_1, -lse_2, -delta_1, -delta_2)
+    const uint64_t sl2p = f2_pack(sl2, sl2), nl1 = f2_pack(rs.x, rs.x), nl2 = f2_pack(rs.y, rs.y);
+    const uint64_t nd1 = f2_pack(rs.z, rs.z), nlam = f2_pack(-lam, -lam), lamd2 = f2_pack(-lam * rs.w, -lam * rs.w);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
         const float2 x1 = f2_unpack(ffma2(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])), sl2p, nl1));
@@ -273,7 +274,7 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         const int qi = qt * BM + r;
         const bool row_ok = qi < len;
         const size_t grow = (size_t)(start + (row_ok ? qi : 0));
-        float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);  // lse1, lse2, delta1, delta2
+        float4 rs = make_float4(0.f, 0.f, 0.f, 0.f);  // -lse1, -lse2, -delta1, -delta2
         if (row_ok) rs = reinterpret_cast<const float4*>(p.rowstat)[(size_t)h * p.total_tokens + grow];
         const float lam = p.lambda[h * p.lambda_stride];
         const float sl2 = p.scale_log2, sc = p.scale;
@@ -339,21 +340,50 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 }
 
 // ============================================================== dKV ===
+// CTA = 128 keys of one kv head; walks the heads of its group and the 64-row
+// query blocks that see its keys. Keys are the MMA rows, so S_c^T, dP^T, and the
+// dV, dK_1, dK_2 accumulators live in tensor memory with one key per lane.
+// Per block:
+//   MMA warp : S_c^T = K_c Q_c^T (A = K_c from tensor memory, bf16 pairs) and
+//              dP^T = V dD^T (both operands in shared memory), N = 64 rows;
+//   compute  : warpgroup w takes rows [32 w, 32 w + 32): it loads its columns of
+//              S_1^T, S_2^T, dP^T, releases the score buffer (so the next
+//              block's scores are issued while it computes), forms
+//              P_1 - lambda P_2, dS_1 / s, dS_2 / s as bf16 and writes them into
+//              three [128 keys x 64 rows] K-major tiles in shared memory;
+//   MMA warp : dV += (P_1 - lambda P_2)^T dD, dK_c += dS_c^T Q_c (A = a tile,
+//              B = the block's dD / Q_c rows, MN-major).
+// The tensor pipe runs the block's scores while the compute warps work on the
+// previous block, and the previous block's dV / dK while they wait. Every MMA has
+// N >= 64: below that an MMA with both operands in shared memory is bound by the
+// operand bandwidth (measured 40 cycles at N = 32, 48 at N = 64, 64 at N = 128
+// for M128 K16), and a 64-row block as two 32-row halves took 44 MMAs instead of 28.
 namespace dkv {
-constexpr int BK = 128, BQ = 64, STAGES = 3;
+constexpr int BK = 128, BQ = 64, STAGES = 4;
 constexpr uint32_t KT_COL = 448;                   // K1 | K2 as bf16 pairs: TMEM columns [448, 512)
+constexpr uint32_t COL_DV = 192, COL_DK = 320;     // dV [192, 320), dK1 [320, 384), dK2 [384, 448)
 constexpr uint32_t KBOX = 128 * ROW;               // [128 keys x 64] 16 KB
 constexpr uint32_t QBOX = 64 * ROW;                // [64 rows x 64] 8 KB
-constexpr uint32_t OFF_K = 0;                      // K1 | K2
+// The bf16 operand tiles, [128 keys x 64 rows] K-major each: P_1 - lambda P_2 and
+// dS_1^T reuse the K1 | K2 boxes (read once into tensor memory at the start),
+// dS_2^T has its own 16 KB; that leaves room for four Q / dD stages.
+constexpr uint32_t OPS_TILE = 128 * ROW;
+constexpr uint32_t OFF_K = 0;                      // K1 | K2, then operand tiles 0 and 1
 constexpr uint32_t OFF_V = 2 * KBOX;               // V lo | V hi
 constexpr uint32_t OFF_ST = 4 * KBOX;              // stages: Q1 | Q2 | dD lo | dD hi | row stats
 constexpr uint32_t ST_STAT = 4 * QBOX;
 constexpr uint32_t STAGE = 4 * QBOX + 1024;
-constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
+constexpr uint32_t OFF_OP2 = OFF_ST + STAGES * STAGE;  // operand tile 2
+constexpr uint32_t OFF_MISC = OFF_OP2 + OPS_TILE;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
+static_assert(STAGE % 1024 == 0 && OFF_OP2 % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+__device__ __forceinline__ uint32_t op_tile(uint32_t sb, int i) {
+    return i == 2 ? sb + OFF_OP2 : sb + OFF_K + (uint32_t)i * OPS_TILE;
+}
 struct Misc {
-    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], s_ready[2], ds_ready[2], acc_done, kt_ready;
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], kt_ready, acc_done;
+    uint64_t s_ready, sdp_free, ops_ready, ops_free;
     uint32_t tmem;
     int abort_flag;
 };
@@ -368,40 +398,54 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
 }
 
 // One thread (= one key) and N query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
-// pairs from S_1^T, S_2^T, dP^T and the rows' (lse_1, lse_2, delta_1, delta_2).
+// pairs from S_1^T, S_2^T, dP^T and the rows' statistics, stored negated
+// (-lse_1, -lse_2, -delta_1, -delta_2), on packed fp32 pairs of adjacent rows:
+//   P_c = 2^(S_c s log2(e) - lse_c),  -lambda P_2,  P_1 - lambda P_2,
+//   dS_1 / s = P_1 (dP - delta_1),  dS_2 / s = -lambda P_2 (dP - delta_2).
 // MASK zeroes rows outside [q_min, q_end); without it every row is visible.
 // The exponentials run on every element and masking is a select after the
 // products, so stale statistics of rows past the end never reach the results.
 template <bool MASK, int N>
 __device__ __forceinline__ void dkv_rows(const uint32_t (&s1)[N], const uint32_t (&s2)[N], const uint32_t (&dp)[N],
-                                         uint32_t stat, float lam, float sl2, float sc, int q0, int q_end,
-                                         int q_min, uint32_t (&pc)[N / 2], uint32_t (&d1)[N / 2],
-                                         uint32_t (&d2)[N / 2]) {
+                                         uint32_t stat, float lam, float sl2, int q0, int q_end, int q_min,
+                                         uint32_t (&pc)[N / 2], uint32_t (&d1)[N / 2], uint32_t (&d2)[N / 2]) {
+    const uint64_t sl2p = f2_pack(sl2, sl2), nlam = f2_pack(-lam, -lam);
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
-        float a[2], b1[2], b2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const float4 st = lds_f4(stat + 16u * (uint32_t)(i + u));
-            const float pp = __uint_as_float(dp[i + u]);
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s1[i + u]), sl2, -st.x));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(s2[i + u]), sl2, -st.y));
-            const float q2 = lam * p2;
-            a[u] = p1 - q2;
-            b1[u] = p1 * (pp - st.z);  // dS_1 / s
-            b2[u] = q2 * (st.w - pp);  // dS_2 / s
-            if (MASK) {
-                const int qi = q0 + i + u;
-                const bool vis = (qi < q_end) & (qi >= q_min);
-                a[u] = vis ? a[u] : 0.f;
-                b1[u] = vis ? b1[u] : 0.f;
-                b2[u] = vis ? b2[u] : 0.f;
-            }
+        const float4 ra = lds_f4(stat + 16u * (uint32_t)i), rb = lds_f4(stat + 16u * (uint32_t)(i + 1));
+        const float2 x1 = f2_unpack(ffma2(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])), sl2p,
+                                          f2_pack(ra.x, rb.x)));
+        const float2 x2 = f2_unpack(ffma2(f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])), sl2p,
+                                          f2_pack(ra.y, rb.y)));
+        const uint64_t p1 = f2_pack(ex2_approx(x1.x), ex2_approx(x1.y));
+        const uint64_t q2 = fmul2(f2_pack(ex2_approx(x2.x), ex2_approx(x2.y)), nlam);  // -lambda P_2
+        const uint64_t pp = f2_pack(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1]));
+        float2 a = f2_unpack(fadd2(p1, q2));
+        float2 b1 = f2_unpack(fmul2(p1, fadd2(pp, f2_pack(ra.z, rb.z))));
+        float2 b2 = f2_unpack(fmul2(q2, fadd2(pp, f2_pack(ra.w, rb.w))));
+        if (MASK) {
+            const int qi = q0 + i;
+            const bool v0 = (qi < q_end) & (qi >= q_min), v1 = (qi + 1 < q_end) & (qi + 1 >= q_min);
+            a.x = v0 ? a.x : 0.f;
+            b1.x = v0 ? b1.x : 0.f;
+            b2.x = v0 ? b2.x : 0.f;
+            a.y = v1 ? a.y : 0.f;
+            b1.y = v1 ? b1.y : 0.f;
+            b2.y = v1 ? b2.y : 0.f;
         }
-        pc[i / 2] = pack_bf16x2(a[0], a[1]);
-        d1[i / 2] = pack_bf16x2(b1[0], b1[1]);
-        d2[i / 2] = pack_bf16x2(b2[0], b2[1]);
+        pc[i / 2] = pack_bf16x2(a.x, a.y);
+        d1[i / 2] = pack_bf16x2(b1.x, b1.y);
+        d2[i / 2] = pack_bf16x2(b2.x, b2.y);
     }
+}
+
+// Rows [32 w, 32 w + 32) of key k's row in a [128 keys x 64 rows] K-major tile
+// (128-byte swizzle: 16-byte chunk c of row k at physical chunk c ^ (k % 8)).
+__device__ __forceinline__ void store_op_row(uint32_t tile, int k, int w, const uint32_t (&v)[16]) {
+    const uint32_t row = tile + (uint32_t)k * ROW;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        sts_u4(row + ((uint32_t)((4 * w + j) ^ (k & 7)) << 4), make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -437,8 +481,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const int n_items = G * nqb;                            // (head, query block) items
 
     const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done), b_kt = smem_u32(&ms.kt_ready);
-    auto b_s = [&](int w) { return smem_u32(&ms.s_ready[w]); };
-    auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
+    const uint32_t b_s = smem_u32(&ms.s_ready), b_free = smem_u32(&ms.sdp_free);
+    const uint32_t b_ops = smem_u32(&ms.ops_ready), b_opf = smem_u32(&ms.ops_free);
     auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
     auto b_se = [&](int s) { return smem_u32(&ms.st_empty[s]); };
     auto item_head = [&](int it) { return g * G + it / nqb; };
@@ -450,10 +494,10 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             mbar_init(b_sf(s), 1);
             mbar_init(b_se(s), 1);
         }
-        mbar_init(b_s(0), 1);
-        mbar_init(b_s(1), 1);
-        mbar_init(b_ds(0), 128);
-        mbar_init(b_ds(1), 128);
+        mbar_init(b_s, 1);
+        mbar_init(b_free, 8);  // one arrive per compute warp
+        mbar_init(b_ops, 8);
+        mbar_init(b_opf, 1);
         mbar_init(b_acc, 1);
         ms.abort_flag = 0;
         fence_barrier_init();
@@ -497,79 +541,73 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
-        // Two 32-row halves per query block, pipelined: once warpgroup h has written the
-        // operands of half h, its dV / dK steps go out and then the scores of half h of
-        // the next block, which overwrite only half h's columns (the pipe runs in issue
-        // order, so the dV / dK steps have read them first).
-        constexpr uint32_t id_s = idesc_bf16_f32(128, 32, false);    // S_c^T, dP^T of a half: N = 32 rows
+        // Per block it: the scores of block it (once its rows have landed and the
+        // compute warps have read block it - 1's scores out of the buffer), then dV / dK
+        // of block it - 1 (once its operand tiles are written). The pipe runs in issue
+        // order, so block it's scores fill the tensor pipe while the compute warps work
+        // on block it - 1.
+        constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false);    // S_c^T, dP^T: N = 64 rows, both K-major
         constexpr uint32_t id_v = idesc_bf16_f32(128, 128, true);    // dV: B = dD rows, MN-major (dv)
         constexpr uint32_t id_k = idesc_bf16_f32(128, 64, true);     // dK_c: B = Q_c rows, MN-major (d)
         constexpr uint64_t KS = 32 >> 4, KB = KBOX >> 4, QB = QBOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
-        constexpr uint64_t HQ = (32 * ROW) >> 4;  // 32 query rows of a K-major box
-        const uint64_t d_k = desc_k(sb + OFF_K), d_v = desc_k(sb + OFF_V);
+        const uint64_t d_v = desc_k(sb + OFF_V);
         const uint64_t d_q = desc_k(sb + OFF_ST), d_qm = desc_mn(sb + OFF_ST, QBOX);
-        // S_c^T = K_c Q_c^T and dP^T = V dD^T for query rows [32 h, 32 h + 32) of the block in
-        // stage s. K_c, the same for every block of the CTA, is read from tensor memory (columns
-        // KT_COL + 32 c, bf16 pairs), so these MMAs read only the 1 KB Q_c slice from shared
-        // memory: from shared memory both, an M128 N32 K16 MMA costs 40 cycles of shared-memory
-        // bandwidth instead of its 16 on the tensor pipe.
-        auto issue_sdp = [&](int s, int h) {
-            const uint64_t sq = d_q + (uint64_t)s * SG + (uint64_t)h * HQ;
-            for (int c = 0; c < 2; ++c) {  // K = d
+        const uint64_t d_op[3] = {desc_k(op_tile(sb, 0)), desc_k(op_tile(sb, 1)), desc_k(op_tile(sb, 2))};
+        // S_c^T = K_c Q_c^T: A = K_c from tensor memory (columns KT_COL + 32 c, 8 columns a
+        // 16-wide K step), B = the block's Q_c rows; dP^T = V dD^T: K = dv = 128 over the two
+        // 64-column halves of V and of dD.
+        auto issue_sdp = [&](int it) {
+            const uint64_t sq = d_q + (uint64_t)(it % STAGES) * SG;
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tmem + c * 64 + 32 * h, tmem + KT_COL + 32 * c + 8 * kk, sq + c * QB + kk * KS, id_s,
-                                 kk > 0);
+                    mma_ts_elect(tmem + c * 64, tmem + KT_COL + 32 * c + 8 * kk, sq + c * QB + kk * KS, id_s, kk > 0);
             }
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // K = dv = 128 over the two 64-column halves
-                mma_ss_elect(tmem + 128 + 32 * h, d_v + (kk >> 2) * KB + (kk & 3) * KS,
+            for (int kk = 0; kk < 8; ++kk)
+                mma_ss_elect(tmem + 128, d_v + (kk >> 2) * KB + (kk & 3) * KS,
                              sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS, id_s, kk > 0);
-            mma_commit_elect(b_s(h));
+            mma_commit_elect(b_s);
         };
-        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && warp_all(mbar_wait(b_kt, 0, ab)) &&
-                  (n_items == 0 || warp_all(mbar_wait(b_sf(0), 0, ab)));
-        if (ok && n_items > 0) {
-            tc_fence_after();
-            issue_sdp(0, 0);
-            issue_sdp(0, 1);
-        }
-        for (int it = 0; ok && it < n_items; ++it) {
-            const int s = it % STAGES, s1 = (it + 1) % STAGES;
-            const bool has_next = it + 1 < n_items;
+        // dV += (P_1 - lambda P_2)^T dD and dK_c += dS_c^T Q_c over the block's 64 rows, 16 a
+        // step: A = an operand tile (K-major, rows contiguous per key), B = the rows of dD /
+        // Q_c in the stage (MN-major).
+        auto issue_dvdk = [&](int it) {
+            const int s = it % STAGES;
             const uint64_t sqm = d_qm + (uint64_t)s * SG;
-            // Warpgroup w wrote the bf16 operands of query rows [32 w, 32 w + 32) into its own
-            // columns: 16-row step kk reads columns 32 (kk / 2) + 8 (kk % 2) of each region.
-            for (int w = 0; w < 2; ++w) {
-                if (!(ok = warp_all(mbar_wait(b_ds(w), (uint32_t)it & 1u, ab)))) break;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 2 * w; kk < 2 * w + 2; ++kk) {
-                    const uint32_t acol = 32 * (kk >> 1) + 8 * (kk & 1);
-                    // dV += (P1 - lambda P2)^T-rows dD
-                    mma_ts_elect(tmem + 192, tmem + acol, sqm + 2 * QB + kk * KR, id_v, (it > 0 || kk > 0) ? 1u : 0u);
-                    // dK_c += dS_c^T-rows Q_c
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                mma_ss_elect(tmem + COL_DV, d_op[0] + kk * KS, sqm + 2 * QB + kk * KR, id_v, acc);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        mma_ts_elect(tmem + 320 + c * 64, tmem + 64 + c * 64 + acol, sqm + c * QB + kk * KR, id_k,
-                                     (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                if (has_next) {
-                    if (w == 0 && !(ok = warp_all(mbar_wait(b_sf(s1), (uint32_t)((it + 1) / STAGES) & 1u, ab)))) break;
-                    tc_fence_after();
-                    issue_sdp(s1, w);
-                }
+                for (int c = 0; c < 2; ++c)
+                    mma_ss_elect(tmem + COL_DK + c * 64, d_op[1 + c] + kk * KS, sqm + c * QB + kk * KR, id_k, acc);
             }
-            if (!ok) break;
+            mma_commit_elect(b_opf);    // the operand tiles may be rewritten once these have run
             mma_commit_elect(b_se(s));  // every MMA reading stage s has been issued
+        };
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && warp_all(mbar_wait(b_kt, 0, ab));
+        for (int it = 0; ok && it < n_items; ++it) {
+            if (!(ok = warp_all(mbar_wait(b_sf(it % STAGES), (uint32_t)(it / STAGES) & 1u, ab)))) break;
+            if (it > 0 && !(ok = warp_all(mbar_wait(b_free, (uint32_t)(it - 1) & 1u, ab)))) break;
+            tc_fence_after();
+            issue_sdp(it);
+            if (it > 0) {
+                if (!(ok = warp_all(mbar_wait(b_ops, (uint32_t)(it - 1) & 1u, ab)))) break;
+                tc_fence_after();
+                issue_dvdk(it - 1);
+            }
+        }
+        if (ok && n_items > 0 && (ok = warp_all(mbar_wait(b_ops, (uint32_t)(n_items - 1) & 1u, ab)))) {
+            tc_fence_after();
+            issue_dvdk(n_items - 1);
         }
         mma_commit_elect(b_acc);
         mbar_wait_drain(b_acc, 0, p.timeout_ns);
         __syncwarp();
     } else {
         // ============================================== compute warpgroups ===
-        // Warpgroup w handles query rows [32 w, 32 w + 32) of every block, 16 at a time;
-        // thread = key.
+        // Warpgroup w handles query rows [32 w, 32 w + 32) of every block; thread = key.
         const int w = warp >> 2;
         const int k = (warp & 3) * 32 + lane;  // key in the tile = TMEM lane
         const uint32_t lo = (uint32_t)((warp & 3) * 32) << 16;
@@ -598,40 +636,40 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         tc_fence_before();
         mbar_arrive(b_kt);
         for (int it = 0; ok && it < n_items; ++it) {
-            if (!(ok = warp_all(mbar_wait(b_s(w), (uint32_t)it & 1u, ab)))) break;
+            if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)it & 1u, ab)))) break;
             tc_fence_after();
+            uint32_t s1[32], s2[32], dp[32];
+            tmem_ld32(tmem + lo + 32 * w, s1);
+            tmem_ld32(tmem + lo + 64 + 32 * w, s2);
+            tmem_ld32(tmem + lo + 128 + 32 * w, dp);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_free);  // the next block's scores may overwrite the buffer
             const int s = it % STAGES;
             // row statistics of the block (shared-window address: explicit shared loads)
-            const uint32_t stat = sb + OFF_ST + (uint32_t)s * STAGE + ST_STAT;
+            const uint32_t stat = sb + OFF_ST + (uint32_t)s * STAGE + ST_STAT + 16u * (uint32_t)(32 * w);
             const int hh = item_head(it);
             const float lam = p.lambda[hh * p.lambda_stride];
             const int row0 = item_row0(it);
             // masking only where a row or key passes the sequence end or (causal) a row
             // precedes a key of the tile: the first two blocks and the last one
             const bool need_mask = row0 + BQ > len || kt * BK + BK > len || (p.causal && row0 < kt * BK + BK - 1);
-#pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {  // query rows [q0, q0 + 16) of the block
-                const int q0 = 32 * w + 16 * sub;
-                uint32_t s1[16], s2[16], dp[16];
-                tmem_ld16(tmem + lo + q0, s1);
-                tmem_ld16(tmem + lo + 64 + q0, s2);
-                tmem_ld16(tmem + lo + 128 + q0, dp);
-                tmem_wait_ld();
-                uint32_t pc[8], d1[8], d2[8];
-                if (need_mask)
-                    dkv_rows<true, 16>(s1, s2, dp, stat + 16u * q0, lam, sl2, sc, row0 + q0, q_end, q_min, pc, d1, d2);
-                else
-                    dkv_rows<false, 16>(s1, s2, dp, stat + 16u * q0, lam, sl2, sc, 0, 0, 0, pc, d1, d2);
-                // rows [q0, q0 + 16) -> columns [32 w + 8 sub, + 8) of each region (already read,
-                // and inside this warpgroup's own columns)
-                const uint32_t pcol = 32 * w + 8 * sub;
-                tmem_st8(tmem + lo + pcol, pc);
-                tmem_st8(tmem + lo + 64 + pcol, d1);
-                tmem_st8(tmem + lo + 128 + pcol, d2);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_ds(w));
+            uint32_t pc[16], d1[16], d2[16];
+            if (need_mask)
+                dkv_rows<true, 32>(s1, s2, dp, stat, lam, sl2, row0 + 32 * w, q_end, q_min, pc, d1, d2);
+            else
+                dkv_rows<false, 32>(s1, s2, dp, stat, lam, sl2, 0, 0, 0, pc, d1, d2);
+            // the operand tiles of the previous block have been read by its dV / dK MMAs; the
+            // first block's overwrite the K boxes, which every compute thread has read by then
+            if (!(ok = warp_all(it > 0 ? mbar_wait(b_opf, (uint32_t)(it - 1) & 1u, ab) : mbar_wait(b_kt, 0, ab))))
+                break;
+            store_op_row(op_tile(sb, 0), k, w, pc);
+            store_op_row(op_tile(sb, 1), k, w, d1);
+            store_op_row(op_tile(sb, 2), k, w, d2);
+            fence_proxy_async_smem();  // visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_ops);
         }
         ok = ok && warp_all(mbar_wait(b_acc, 0, ab));
         // ok is warp-uniform; key_ok is not: every lane takes part in the (warp-wide)
@@ -647,7 +685,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lo + 192 + 128 * w + ch * 32, o);
+                tmem_ld32(tmem + lo + COL_DV + 128 * w + ch * 32, o);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll

@@ -92,7 +92,7 @@ struct BwdParams {
     int num_seqs, seqlen, max_seqlen, total_tokens;
     int H, Hkv;
     float scale, scale_log2;
-    const float* rowstat;      // [H][tokens][4]: lse1, lse2, delta1, delta2 (workspace)
+    const float* rowstat;      // [H][tokens][4]: -lse1, -lse2, -delta1, -delta2 (workspace)
     void* dq;                  // [tokens][H][2d]
     void* dk;                  // [tokens][Hkv][2d]
     void* dv;                  // [tokens][Hkv][dv]
@@ -123,7 +123,7 @@ struct BwdPreParams {
     float eps;
     int tokens, H;
     void* dd;                  // out: [tokens][H][dv] bf16, gradient of the pre-norm output
-    float* rowstat;            // out: [H][tokens][4]
+    float* rowstat;            // out: [H][tokens][4], negated
     float* dlambda;            // out (accumulated): [H] or [1]
     float* dsubln_w;           // out (accumulated): [dv]
 };
