@@ -21,10 +21,9 @@
 //               dQ1 [384,448), dQ2 [448,512); dS_c (bf16) over S_c.
 //   dKV kernel: CTA = 128 keys of one kv head; walks the heads of its group and
 //               the 64-row query blocks that see its keys. With keys as the MMA
-//               rows: S_c^T [0,64) [64,128), dP^T [128,192), dV [192,320),
-//               dK1 [320,384), dK2 [384,448), K1 | K2 (bf16 pairs, the A operand
-//               of the score MMAs) [448,512); the bf16 operands P_1 - lambda P_2,
-//               dS_1^T, dS_2^T go over S1^T, S2^T, dP^T.
+//               rows: S_c^T [0,64) [64,128), dP^T [128,192), dS_1^T | dS_2^T
+//               (bf16 pairs) [192,256), dV [256,384), dK1 [384,448), dK2 [448,512);
+//               P_1 - lambda P_2 (bf16) goes through shared memory.
 // Every wait is bounded; on a timeout a CTA records the error, lets its copies
 // and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -344,15 +343,16 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // query blocks that see its keys. Keys are the MMA rows, so S_c^T, dP^T, and the
 // dV, dK_1, dK_2 accumulators live in tensor memory with one key per lane.
 // Per block:
-//   MMA warp : S_c^T = K_c Q_c^T (A = K_c from tensor memory, bf16 pairs) and
-//              dP^T = V dD^T (both operands in shared memory), N = 64 rows;
+//   MMA warp : S_c^T = K_c Q_c^T and dP^T = V dD^T (operands in shared memory),
+//              N = 64 rows;
 //   compute  : warpgroup w takes rows [32 w, 32 w + 32): it loads its columns of
 //              S_1^T, S_2^T, dP^T, releases the score buffer (so the next
 //              block's scores are issued while it computes), forms
-//              P_1 - lambda P_2, dS_1 / s, dS_2 / s as bf16 and writes them into
-//              three [128 keys x 64 rows] K-major tiles in shared memory;
-//   MMA warp : dV += (P_1 - lambda P_2)^T dD, dK_c += dS_c^T Q_c (A = a tile,
-//              B = the block's dD / Q_c rows, MN-major).
+//              P_1 - lambda P_2, dS_1 / s, dS_2 / s as bf16 and writes the first
+//              into a [128 keys x 64 rows] K-major tile in shared memory, the
+//              other two into tensor memory columns of their own;
+//   MMA warp : dV += (P_1 - lambda P_2)^T dD, dK_c += dS_c^T Q_c (B = the
+//              block's dD / Q_c rows, MN-major).
 // The tensor pipe runs the block's scores while the compute warps work on the
 // previous block, and the previous block's dV / dK while they wait. Every MMA has
 // N >= 64: below that an MMA with both operands in shared memory is bound by the
@@ -360,29 +360,22 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // for M128 K16), and a 64-row block as two 32-row halves took 44 MMAs instead of 28.
 namespace dkv {
 constexpr int BK = 128, BQ = 64, STAGES = 4;
-constexpr uint32_t KT_COL = 448;                   // K1 | K2 as bf16 pairs: TMEM columns [448, 512)
-constexpr uint32_t COL_DV = 192, COL_DK = 320;     // dV [192, 320), dK1 [320, 384), dK2 [384, 448)
+constexpr uint32_t COL_DS = 192;                   // dS_1^T [192, 224), dS_2^T [224, 256): bf16 pairs
+constexpr uint32_t COL_DV = 256, COL_DK = 384;     // dV [256, 384), dK1 [384, 448), dK2 [448, 512)
 constexpr uint32_t KBOX = 128 * ROW;               // [128 keys x 64] 16 KB
 constexpr uint32_t QBOX = 64 * ROW;                // [64 rows x 64] 8 KB
-// The bf16 operand tiles, [128 keys x 64 rows] K-major each: P_1 - lambda P_2 and
-// dS_1^T reuse the K1 | K2 boxes (read once into tensor memory at the start),
-// dS_2^T has its own 16 KB; that leaves room for four Q / dD stages.
-constexpr uint32_t OPS_TILE = 128 * ROW;
-constexpr uint32_t OFF_K = 0;                      // K1 | K2, then operand tiles 0 and 1
+constexpr uint32_t OFF_K = 0;                      // K1 | K2
 constexpr uint32_t OFF_V = 2 * KBOX;               // V lo | V hi
 constexpr uint32_t OFF_ST = 4 * KBOX;              // stages: Q1 | Q2 | dD lo | dD hi | row stats
 constexpr uint32_t ST_STAT = 4 * QBOX;
 constexpr uint32_t STAGE = 4 * QBOX + 1024;
-constexpr uint32_t OFF_OP2 = OFF_ST + STAGES * STAGE;  // operand tile 2
-constexpr uint32_t OFF_MISC = OFF_OP2 + OPS_TILE;
+constexpr uint32_t OFF_P = OFF_ST + STAGES * STAGE;  // (P_1 - lambda P_2)^T: [128 keys x 64 rows] bf16, K-major
+constexpr uint32_t OFF_MISC = OFF_P + 128 * ROW;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
-static_assert(STAGE % 1024 == 0 && OFF_OP2 % 1024 == 0, "swizzle atoms are 1024-byte aligned");
-__device__ __forceinline__ uint32_t op_tile(uint32_t sb, int i) {
-    return i == 2 ? sb + OFF_OP2 : sb + OFF_K + (uint32_t)i * OPS_TILE;
-}
+static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 struct Misc {
-    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], kt_ready, acc_done;
+    uint64_t kv_full, st_full[STAGES], st_empty[STAGES], acc_done;
     uint64_t s_ready, sdp_free, ops_ready, ops_free;
     uint32_t tmem;
     int abort_flag;
@@ -480,7 +473,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const int nqb = (len + BQ - 1) / BQ - qb0;             // query blocks per head
     const int n_items = G * nqb;                            // (head, query block) items
 
-    const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done), b_kt = smem_u32(&ms.kt_ready);
+    const uint32_t b_kv = smem_u32(&ms.kv_full), b_acc = smem_u32(&ms.acc_done);
     const uint32_t b_s = smem_u32(&ms.s_ready), b_free = smem_u32(&ms.sdp_free);
     const uint32_t b_ops = smem_u32(&ms.ops_ready), b_opf = smem_u32(&ms.ops_free);
     auto b_sf = [&](int s) { return smem_u32(&ms.st_full[s]); };
@@ -489,7 +482,6 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     auto item_row0 = [&](int it) { return (qb0 + it % nqb) * BQ; };  // first query position of the block
     if (warp == PRODUCER_WARP && lane == 0) {
         mbar_init(b_kv, 1);
-        mbar_init(b_kt, 256);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(b_sf(s), 1);
             mbar_init(b_se(s), 1);
@@ -550,18 +542,16 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         constexpr uint32_t id_v = idesc_bf16_f32(128, 128, true);    // dV: B = dD rows, MN-major (dv)
         constexpr uint32_t id_k = idesc_bf16_f32(128, 64, true);     // dK_c: B = Q_c rows, MN-major (d)
         constexpr uint64_t KS = 32 >> 4, KB = KBOX >> 4, QB = QBOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
-        const uint64_t d_v = desc_k(sb + OFF_V);
+        const uint64_t d_k = desc_k(sb + OFF_K), d_v = desc_k(sb + OFF_V), d_p = desc_k(sb + OFF_P);
         const uint64_t d_q = desc_k(sb + OFF_ST), d_qm = desc_mn(sb + OFF_ST, QBOX);
-        const uint64_t d_op[3] = {desc_k(op_tile(sb, 0)), desc_k(op_tile(sb, 1)), desc_k(op_tile(sb, 2))};
-        // S_c^T = K_c Q_c^T: A = K_c from tensor memory (columns KT_COL + 32 c, 8 columns a
-        // 16-wide K step), B = the block's Q_c rows; dP^T = V dD^T: K = dv = 128 over the two
-        // 64-column halves of V and of dD.
+        // S_c^T = K_c Q_c^T (A = the K_c box, B = the block's Q_c rows) and dP^T = V dD^T (K = dv
+        // = 128 over the two 64-column halves of V and of dD).
         auto issue_sdp = [&](int it) {
             const uint64_t sq = d_q + (uint64_t)(it % STAGES) * SG;
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts_elect(tmem + c * 64, tmem + KT_COL + 32 * c + 8 * kk, sq + c * QB + kk * KS, id_s, kk > 0);
+                    mma_ss_elect(tmem + c * 64, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -570,23 +560,24 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             mma_commit_elect(b_s);
         };
         // dV += (P_1 - lambda P_2)^T dD and dK_c += dS_c^T Q_c over the block's 64 rows, 16 a
-        // step: A = an operand tile (K-major, rows contiguous per key), B = the rows of dD /
-        // Q_c in the stage (MN-major).
+        // step: A = the P tile (shared memory, K-major) or dS_c^T (tensor memory, 8 columns a
+        // step), B = the rows of dD / Q_c in the stage (MN-major).
         auto issue_dvdk = [&](int it) {
             const int s = it % STAGES;
             const uint64_t sqm = d_qm + (uint64_t)s * SG;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                mma_ss_elect(tmem + COL_DV, d_op[0] + kk * KS, sqm + 2 * QB + kk * KR, id_v, acc);
+                mma_ss_elect(tmem + COL_DV, d_p + kk * KS, sqm + 2 * QB + kk * KR, id_v, acc);
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    mma_ss_elect(tmem + COL_DK + c * 64, d_op[1 + c] + kk * KS, sqm + c * QB + kk * KR, id_k, acc);
+                    mma_ts_elect(tmem + COL_DK + c * 64, tmem + COL_DS + 32 * c + 8 * kk, sqm + c * QB + kk * KR, id_k,
+                                 acc);
             }
-            mma_commit_elect(b_opf);    // the operand tiles may be rewritten once these have run
+            mma_commit_elect(b_opf);    // the operands may be rewritten once these have run
             mma_commit_elect(b_se(s));  // every MMA reading stage s has been issued
         };
-        bool ok = warp_all(mbar_wait(b_kv, 0, ab)) && warp_all(mbar_wait(b_kt, 0, ab));
+        bool ok = warp_all(mbar_wait(b_kv, 0, ab));
         for (int it = 0; ok && it < n_items; ++it) {
             if (!(ok = warp_all(mbar_wait(b_sf(it % STAGES), (uint32_t)(it / STAGES) & 1u, ab)))) break;
             if (it > 0 && !(ok = warp_all(mbar_wait(b_free, (uint32_t)(it - 1) & 1u, ab)))) break;
@@ -616,25 +607,7 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const int q_end = key_ok ? len : 0;       // visible query rows of this key: [q_min, q_end)
         const int q_min = p.causal ? kj : 0;
         const float sl2 = p.scale_log2, sc = p.scale;
-        // K_w (this thread's key row, bf16 pairs) into tensor memory columns KT_COL + 32 w: the
-        // A operand of the score MMAs. The row sits in the 128-byte-swizzled TMA box.
-        bool ok = warp_all(mbar_wait(b_kv, 0, ab));
-        if (ok) {
-            const uint32_t row = sb + OFF_K + (uint32_t)w * KBOX + (uint32_t)k * ROW;
-            uint32_t kw[32];
-#pragma unroll
-            for (int jc = 0; jc < 8; ++jc) {
-                const float4 v = lds_f4(row + ((uint32_t)(jc ^ (k & 7)) << 4));
-                kw[4 * jc] = __float_as_uint(v.x);
-                kw[4 * jc + 1] = __float_as_uint(v.y);
-                kw[4 * jc + 2] = __float_as_uint(v.z);
-                kw[4 * jc + 3] = __float_as_uint(v.w);
-            }
-            tmem_st32(tmem + lo + KT_COL + 32 * w, kw);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(b_kt);
+        bool ok = true;
         for (int it = 0; ok && it < n_items; ++it) {
             if (!(ok = warp_all(mbar_wait(b_s, (uint32_t)it & 1u, ab)))) break;
             tc_fence_after();
@@ -660,14 +633,14 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 dkv_rows<true, 32>(s1, s2, dp, stat, lam, sl2, row0 + 32 * w, q_end, q_min, pc, d1, d2);
             else
                 dkv_rows<false, 32>(s1, s2, dp, stat, lam, sl2, 0, 0, 0, pc, d1, d2);
-            // the operand tiles of the previous block have been read by its dV / dK MMAs; the
-            // first block's overwrite the K boxes, which every compute thread has read by then
-            if (!(ok = warp_all(it > 0 ? mbar_wait(b_opf, (uint32_t)(it - 1) & 1u, ab) : mbar_wait(b_kt, 0, ab))))
-                break;
-            store_op_row(op_tile(sb, 0), k, w, pc);
-            store_op_row(op_tile(sb, 1), k, w, d1);
-            store_op_row(op_tile(sb, 2), k, w, d2);
-            fence_proxy_async_smem();  // visible to the tensor cores
+            // the previous block's operands have been read by its dV / dK MMAs
+            if (it > 0 && !(ok = warp_all(mbar_wait(b_opf, (uint32_t)(it - 1) & 1u, ab)))) break;
+            store_op_row(sb + OFF_P, k, w, pc);
+            tmem_st16(tmem + lo + COL_DS + 16 * w, d1);
+            tmem_st16(tmem + lo + COL_DS + 32 + 16 * w, d2);
+            fence_proxy_async_smem();  // the P tile, visible to the tensor cores
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_ops);
         }
