@@ -106,18 +106,23 @@ __device__ __forceinline__ void dq_keys32(const uint32_t (&s1)[32], const uint32
     }
 }
 
+// K and V have rings of their own: a tile's V is free once its dP MMAs have run,
+// its K only after its dQ steps, so three K stages and two V stages give each
+// load about two tiles of lead (one shared two-stage ring left the MMA warp
+// waiting ~0.8 us a tile for the next tile's rows).
 namespace dq {
-constexpr int BM = 128, BN = 128, STAGES = 2;
+constexpr int BM = 128, BN = 128, KSTAGES = 3, VSTAGES = 2;
 constexpr uint32_t BOX = 128 * ROW;                // [128 x 64] bf16 box: 16 KB
 constexpr uint32_t OFF_Q = 0;                      // Q1 | Q2
 constexpr uint32_t OFF_DD = 2 * BOX;               // dD (two 64-column halves)
-constexpr uint32_t OFF_ST = 4 * BOX;               // stages: K1 | K2 | V lo | V hi
-constexpr uint32_t STAGE = 4 * BOX;
-constexpr uint32_t OFF_MISC = OFF_ST + STAGES * STAGE;
+constexpr uint32_t OFF_K = 4 * BOX;                // K stages: K1 | K2
+constexpr uint32_t OFF_V = OFF_K + KSTAGES * 2 * BOX;  // V stages: V lo | V hi
+constexpr uint32_t OFF_MISC = OFF_V + VSTAGES * 2 * BOX;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
 struct Misc {
-    uint64_t q_full, kv_full[STAGES], kv_empty[STAGES], s_ready[2], ds_ready[2], dq_done;
+    uint64_t q_full, k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES], s_ready[2], ds_ready[2],
+        dq_done;
     uint32_t tmem;
     int abort_flag;
 };
@@ -155,13 +160,19 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const uint32_t b_q = smem_u32(&ms.q_full), b_dq = smem_u32(&ms.dq_done);
     auto b_s = [&](int w) { return smem_u32(&ms.s_ready[w]); };
     auto b_ds = [&](int w) { return smem_u32(&ms.ds_ready[w]); };
-    auto b_kf = [&](int s) { return smem_u32(&ms.kv_full[s]); };
-    auto b_ke = [&](int s) { return smem_u32(&ms.kv_empty[s]); };
+    auto b_kf = [&](int s) { return smem_u32(&ms.k_full[s]); };
+    auto b_ke = [&](int s) { return smem_u32(&ms.k_empty[s]); };
+    auto b_vf = [&](int s) { return smem_u32(&ms.v_full[s]); };
+    auto b_ve = [&](int s) { return smem_u32(&ms.v_empty[s]); };
     if (warp == PRODUCER_WARP && lane == 0) {
         mbar_init(b_q, 1);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < KSTAGES; ++s) {
             mbar_init(b_kf(s), 1);
             mbar_init(b_ke(s), 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(b_vf(s), 1);
+            mbar_init(b_ve(s), 1);
         }
         mbar_init(b_s(0), 1);
         mbar_init(b_s(1), 1);
@@ -187,22 +198,28 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tma_load_2d(sb + OFF_Q + BOX, &tm_q, b_q, h * 2 * HD + HD, row_q, pol);
             tma_load_2d(sb + OFF_DD, &tm_dd, b_q, h * DV, row_q, pol);
             tma_load_2d(sb + OFF_DD + BOX, &tm_dd, b_q, h * DV + 64, row_q, pol);
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_kv; ++j) {
-                const int s = j % STAGES;
-                if (!mbar_wait(b_ke(s), ((uint32_t)(j / STAGES) & 1u) ^ 1u, ab)) break;
-                const uint32_t st = sb + OFF_ST + (uint32_t)s * STAGE;
+                const int sk = j % KSTAGES, sv = j % VSTAGES;
                 const int row = start + j * BN;
-                mbar_arrive_expect_tx(b_kf(s), STAGE);
-                tma_load_2d(st, &tm_k, b_kf(s), g * 2 * HD, row, pol);
-                tma_load_2d(st + BOX, &tm_k, b_kf(s), g * 2 * HD + HD, row, pol);
-                tma_load_2d(st + 2 * BOX, &tm_v, b_kf(s), g * DV, row, pol);
-                tma_load_2d(st + 3 * BOX, &tm_v, b_kf(s), g * DV + 64, row, pol);
-                issued = j + 1;
+                if (!mbar_wait(b_ke(sk), ((uint32_t)(j / KSTAGES) & 1u) ^ 1u, ab)) break;
+                const uint32_t kst = sb + OFF_K + (uint32_t)sk * 2 * BOX;
+                mbar_arrive_expect_tx(b_kf(sk), 2 * BOX);
+                tma_load_2d(kst, &tm_k, b_kf(sk), g * 2 * HD, row, pol);
+                tma_load_2d(kst + BOX, &tm_k, b_kf(sk), g * 2 * HD + HD, row, pol);
+                k_issued = j + 1;
+                if (!mbar_wait(b_ve(sv), ((uint32_t)(j / VSTAGES) & 1u) ^ 1u, ab)) break;
+                const uint32_t vst = sb + OFF_V + (uint32_t)sv * 2 * BOX;
+                mbar_arrive_expect_tx(b_vf(sv), 2 * BOX);
+                tma_load_2d(vst, &tm_v, b_vf(sv), g * DV, row, pol);
+                tma_load_2d(vst + BOX, &tm_v, b_vf(sv), g * DV + 64, row, pol);
+                v_issued = j + 1;
             }
             mbar_wait_drain(b_q, 0, p.timeout_ns);
-            for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-                mbar_wait_drain(b_kf(j % STAGES), (uint32_t)(j / STAGES) & 1u, p.timeout_ns);
+            for (int j = k_issued > KSTAGES ? k_issued - KSTAGES : 0; j < k_issued; ++j)
+                mbar_wait_drain(b_kf(j % KSTAGES), (uint32_t)(j / KSTAGES) & 1u, p.timeout_ns);
+            for (int j = v_issued > VSTAGES ? v_issued - VSTAGES : 0; j < v_issued; ++j)
+                mbar_wait_drain(b_vf(j % VSTAGES), (uint32_t)(j / VSTAGES) & 1u, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
@@ -213,12 +230,13 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false);    // S_c, dP of a half: both operands K-major
         constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true);    // dQ_c: B = K_c is MN-major (d contiguous)
         const uint64_t dq_q = desc_k(sb + OFF_Q), dq_dd = desc_k(sb + OFF_DD);
-        const uint64_t dk0 = desc_k(sb + OFF_ST), dkm = desc_mn(sb + OFF_ST, BOX);
-        constexpr uint64_t KS = 32 >> 4, BX = BOX >> 4, SG = STAGE >> 4, KR = (16 * ROW) >> 4;
+        const uint64_t dk0 = desc_k(sb + OFF_K), dkm = desc_mn(sb + OFF_K, BOX), dv0 = desc_k(sb + OFF_V);
+        constexpr uint64_t KS = 32 >> 4, BX = BOX >> 4, KR = (16 * ROW) >> 4, SG2 = (2 * BOX) >> 4;
         constexpr uint64_t HK = (64 * ROW) >> 4;  // 64 key rows of a K-major box
-        // S_c = Q_c K_c^T and dP = dD V^T for keys [64 h, 64 h + 64) of the tile in stage s
-        auto issue_sdp = [&](int s, int h) {
-            const uint64_t st_k = dk0 + (uint64_t)s * SG + (uint64_t)h * HK;
+        // S_c = Q_c K_c^T and dP = dD V^T for keys [64 h, 64 h + 64) of tile t
+        auto issue_sdp = [&](int t, int h) {
+            const uint64_t st_k = dk0 + (uint64_t)(t % KSTAGES) * SG2 + (uint64_t)h * HK;
+            const uint64_t st_v = dv0 + (uint64_t)(t % VSTAGES) * SG2 + (uint64_t)h * HK;
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -228,19 +246,23 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // K = dv = 128 over the two 64-column halves of dD and of V
                 mma_ss_elect(tmem + 256 + 64 * h, dq_dd + (kk >> 2) * BX + (kk & 3) * KS,
-                             st_k + 2 * BX + (kk >> 2) * BX + (kk & 3) * KS, id_s, kk > 0);
+                             st_v + (kk >> 2) * BX + (kk & 3) * KS, id_s, kk > 0);
             mma_commit_elect(b_s(h));
+            if (h == 1) mma_commit_elect(b_ve(t % VSTAGES));  // both dP halves of tile t issued
         };
-        bool ok = warp_all(mbar_wait(b_q, 0, ab)) && warp_all(mbar_wait(b_kf(0), 0, ab));
+        auto kv_ready = [&](int t) {
+            return warp_all(mbar_wait(b_kf(t % KSTAGES), (uint32_t)(t / KSTAGES) & 1u, ab)) &&
+                   warp_all(mbar_wait(b_vf(t % VSTAGES), (uint32_t)(t / VSTAGES) & 1u, ab));
+        };
+        bool ok = warp_all(mbar_wait(b_q, 0, ab)) && kv_ready(0);
         if (ok) {
             tc_fence_after();
             issue_sdp(0, 0);
             issue_sdp(0, 1);
         }
         for (int j = 0; ok && j < n_kv; ++j) {
-            const int s = j % STAGES, s1 = (j + 1) % STAGES;
             const bool has_next = j + 1 < n_kv;
-            const uint64_t st_km = dkm + (uint64_t)s * SG;
+            const uint64_t st_km = dkm + (uint64_t)(j % KSTAGES) * SG2;
             for (int h = 0; h < 2; ++h) {
                 if (!(ok = warp_all(mbar_wait(b_ds(h), (uint32_t)j & 1u, ab)))) break;
                 tc_fence_after();
@@ -253,13 +275,13 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                                      id_dq, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (has_next) {
-                    if (h == 0 && !(ok = warp_all(mbar_wait(b_kf(s1), (uint32_t)((j + 1) / STAGES) & 1u, ab)))) break;
+                    if (h == 0 && !(ok = kv_ready(j + 1))) break;
                     tc_fence_after();
-                    issue_sdp(s1, h);
+                    issue_sdp(j + 1, h);
                 }
             }
             if (!ok) break;
-            mma_commit_elect(b_ke(s));  // every MMA reading stage s has been issued
+            mma_commit_elect(b_ke(j % KSTAGES));  // every MMA reading tile j's K has been issued
         }
         mma_commit_elect(b_dq);
         mbar_wait_drain(b_dq, 0, p.timeout_ns);
