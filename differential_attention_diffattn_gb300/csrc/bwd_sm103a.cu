@@ -202,6 +202,13 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int j = 0; j < n_kv; ++j) {
                 const int sk = j % KSTAGES, sv = j % VSTAGES;
                 const int row = start + j * BN;
+                if (j + 2 < n_kv) {  // two tiles ahead into L2, so that their loads find them there
+                    const int row2 = row + 2 * BN;
+                    tma_prefetch_l2_2d(&tm_k, g * 2 * HD, row2);
+                    tma_prefetch_l2_2d(&tm_k, g * 2 * HD + HD, row2);
+                    tma_prefetch_l2_2d(&tm_v, g * DV, row2);
+                    tma_prefetch_l2_2d(&tm_v, g * DV + 64, row2);
+                }
                 if (!mbar_wait(b_ke(sk), ((uint32_t)(j / KSTAGES) & 1u) ^ 1u, ab)) break;
                 const uint32_t kst = sb + OFF_K + (uint32_t)sk * 2 * BOX;
                 mbar_arrive_expect_tx(b_kf(sk), 2 * BOX);

@@ -107,6 +107,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// 2-D tiled prefetch of one box into L2 (no shared memory, no completion
+// signal); the box must lie within the tensor.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk async group). The source
 // must be made visible to the async proxy first (fence_proxy_async_smem).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
