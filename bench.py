@@ -260,11 +260,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     check_device(da, "during warm-up")
     warm = None
+    graphs = fwd_graphs = None
     if flush is not None:
-        # Warm figure: consecutive steps replayed from CUDA graphs (lambda + forward
-        # captured once per input set), so that host launch overhead does not pace
-        # steps of a few microseconds.
-        graphs = []
+        # Steps of these workloads take a few to a hundred microseconds, about what the
+        # host needs to launch them from Python (argument checks, tensor maps, two
+        # launches): launched one by one, the events would time the host. Each step is
+        # therefore captured once per input set as a CUDA graph (lambda + forward, and
+        # the forward alone for the launch time) and replayed, the L2 flushed before
+        # every replay; the warm figure replays them back to back.
+        graphs, fwd_graphs = [], []
         for b in range(2):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
@@ -272,6 +276,10 @@ def run_ours(args, rank, world, local_rank):
                 da.diffattn_lambda(*lvec, li, out=lam, stream=st)
                 fwd(sets[b], st=st)
             graphs.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fwd(sets[b], st=torch.cuda.current_stream())
+            fwd_graphs.append(g)
         for i in range(3):
             graphs[i % 2].replay()
         torch.cuda.synchronize()
@@ -302,13 +310,23 @@ def run_ours(args, rank, world, local_rank):
         if flush is not None:
             flush.zero_()
         sev[i][0].record(stream)
-        da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
-        ev[i][0].record(stream)
-        fwd(sets[i % 2], i)
-        ev[i][1].record(stream)
+        if graphs is not None:
+            graphs[i % 2].replay()
+        else:
+            da.diffattn_lambda(*lvec, li, out=lam, stream=stream)
+            ev[i][0].record(stream)
+            fwd(sets[i % 2], i)
+            ev[i][1].record(stream)
         sev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    if fwd_graphs is not None:  # the forward launch alone, flushed L2 before each
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd_graphs[i % 2].replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
@@ -421,6 +439,8 @@ def run_ours(args, rank, world, local_rank):
                    "inputs": "seeded N(0,1) q/k/v rounded to bf16, lambda vectors N(0,0.1^2) fp32, subln w = 1"},
         "per_step_ms": {"median": round(statistics.median(step_times), 5), "min": round(min(step_times), 5),
                         "covers": "lambda + forward launches of one step, CUDA events"},
+        **({"launch": "each step a CUDA graph replay (lambda + forward), L2 flushed before it"}
+           if graphs is not None else {}),
         # the same rate under the other counts of the pages' workloads, for information:
         # T^2 / 2 pairs per head instead of T (T + 1) / 2, and the 512 flop per pair of
         # the probability-map form (which one pass cannot run: it needs the row
