@@ -112,6 +112,10 @@ def test_training_outputs_match_oracle(lens, kernel):
     ([200], 4, 4, False, False),
     ([513], 16, 16, True, False),
     ([300, 129, 200, 1, 256, 77, 300, 150], 16, 4, True, False),
+    # 16 query blocks per key tile and 8 key tiles per query tile: the rings of both
+    # kernels wrap several times, and the last blocks run past the sequences' ends
+    ([1000], 16, 4, True, True),
+    ([777, 1000], 8, 8, True, False),
 ])
 def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
     wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, lambda_per_head=per_head,
