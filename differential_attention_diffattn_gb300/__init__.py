@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     diffattn_bwd,
     diffattn_bwd_workspace_size,
     diffattn_fwd,
+    diffattn_fwd_lambda,
     diffattn_fwd_kernel,
     diffattn_fwd_rope_q,
     diffattn_fwd_train,

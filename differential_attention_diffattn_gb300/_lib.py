@@ -23,7 +23,7 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
             "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj",
-            "diffattn_fwd_kernel", "diffattn_fwd_rope_q")
+            "diffattn_fwd_kernel", "diffattn_fwd_rope_q", "diffattn_fwd_lambda")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -92,6 +92,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_fwd_rope_q.restype = ctypes.c_int
         lib.diffattn_fwd_rope_q.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                             vp, ctypes.c_int, vp, ctypes.POINTER(DiffAttnRopeQ), vp, vp]
+        lib.diffattn_fwd_lambda.restype = ctypes.c_int
+        lib.diffattn_fwd_lambda.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_float, vp, vp, ctypes.c_int, vp, vp, vp]
         lib.diffattn_fwd.restype = ctypes.c_int
         lib.diffattn_fwd.argtypes = [ctypes.POINTER(DiffAttnDesc), vp, vp, vp, vp, ctypes.c_int, ctypes.c_float,
                                      vp, ctypes.c_int, vp, vp, vp]
@@ -395,6 +398,36 @@ def diffattn_fwd(q, k, v, lam, lambda_init: float, subln_w, causal: bool = True,
     if st != OK:
         raise DiffAttnError(st, "diffattn_fwd")
     return out
+
+
+def diffattn_fwd_lambda(q, k, v, lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init: float, subln_w,
+                        causal: bool = True, cu_seqlens=None, max_seqlen: Optional[int] = None, eps: float = 1e-5,
+                        lam_out=None, out=None, stream=None):
+    """diffattn_lambda and diffattn_fwd in one call (the forward's loads and first
+    tiles run while the lambda kernel finishes). lambda_q1 .. lambda_k2: fp32 [d]
+    (shared lambda) or [H, d] (per head). Returns (out, lam)."""
+    import torch
+    lib = load_library()
+    vecs = (lambda_q1, lambda_k1, lambda_q2, lambda_k2)
+    for t, name in zip(vecs, ("lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2")):
+        _check_cuda(t, name)
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape != lambda_q1.shape:
+            raise ValueError(f"{name} must be contiguous fp32 of the shape of lambda_q1")
+    H = q.shape[-2]
+    per_head = lambda_q1.dim() == 2 and lambda_q1.shape[0] == H and H > 1
+    n_sets = H if per_head else 1
+    if lam_out is None:
+        lam_out = torch.empty(n_sets, dtype=torch.float32, device=q.device)
+    _check_cuda(lam_out, "lam_out")
+    desc, H, out = _fwd_args(q, k, v, lam_out, subln_w, cu_seqlens, max_seqlen, eps, out)
+    st = lib.diffattn_fwd_lambda(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), *(_ptr(t) for t in vecs),
+                                 1 if per_head else 0, int(lambda_q1.shape[-1]), float(lambda_init), _ptr(lam_out),
+                                 _ptr(subln_w), 1 if causal else 0,
+                                 _ptr(cu_seqlens) if cu_seqlens is not None else None, _ptr(out),
+                                 _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_lambda")
+    return out, lam_out
 
 
 def diffattn_fwd_rope_q(q, k, v, lam, lambda_init: float, subln_w, cos, sin, rot_dim: int, interleaved: bool,

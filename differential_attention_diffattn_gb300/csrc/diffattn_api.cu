@@ -294,10 +294,18 @@ diffattn_status diffattn_lambda(const float* lq1, const float* lk1, const float*
 namespace {
 // Shared body of diffattn_fwd and diffattn_fwd_train; lse, o1, o2 are all null
 // (inference) or all set (training outputs, bf16 tcgen05 kernel only).
+// The lambda kernel a combined call launches just before its forward, writing
+// the `lambda` the forward reads.
+struct LambdaCall {
+    const float *lq1, *lk1, *lq2, *lk2;
+    int n_sets, d;
+};
+
 diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void* k, const void* v,
                            const float* lambda, int lambda_per_head, float lambda_init, const float* subln_w,
                            int causal, const int* cu_seqlens, void* out, float* lse, void* o1, void* o2,
-                           void* stream, const diffattn_rope_q* rope = nullptr) {
+                           void* stream, const diffattn_rope_q* rope = nullptr,
+                           const LambdaCall* lam_call = nullptr) {
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const bool train = lse != nullptr || o1 != nullptr || o2 != nullptr;
     if (train && (!lse || !o1 || !o2 || !aligned16(o1) || !aligned16(o2) ||
@@ -385,8 +393,16 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         p.rope_interleaved = rope->interleaved;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the combined call's lambda kernel goes first, once nothing can fail on the host
+    auto launch_lambda_first = [&]() {
+        return launch_lambda(lam_call->lq1, lam_call->lk1, lam_call->lq2, lam_call->lk2, lam_call->n_sets,
+                             lam_call->d, lambda_init, const_cast<float*>(lambda), st);
+    };
 
-    if (f32_simt) return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+    if (f32_simt) {
+        if (lam_call && launch_lambda_first() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+        return launch_fwd_f32(p, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+    }
 
     FwdTensorMaps maps;
     if (!encode_bf16_rows(&maps.q, q, (uint64_t)ds.num_heads * 2 * ds.d, (uint64_t)p.total_tokens) ||
@@ -394,6 +410,10 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens) ||
         !encode_bf16_rows(&maps.out, out, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
+    if (lam_call) {
+        if (launch_lambda_first() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+        p.lambda_pending = 1;  // the forward's reads of lambda alone wait for that kernel
+    }
     // The rotary embedding of q is applied by the one-item-per-CTA kernel only: it
     // stages each tile's cos / sin rows in its last K/V stage, which the persistent
     // kernel does not have (its shared memory is all in use).
@@ -423,6 +443,20 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
     const CallRange nvtx_range("diffattn_fwd");
     return fwd_common(desc, q, k, v, lambda, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
                       nullptr, nullptr, nullptr, stream);
+}
+
+diffattn_status diffattn_fwd_lambda(const diffattn_desc* desc, const void* q, const void* k, const void* v,
+                                    const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                    int lambda_per_head, int lambda_d, float lambda_init, float* lambda_out,
+                                    const float* subln_w, int causal, const int* cu_seqlens, void* out,
+                                    void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_lambda");
+    if (!desc || !lq1 || !lk1 || !lq2 || !lk2 || !lambda_out) return DIFFATTN_ERR_INVALID_ARG;
+    if (lambda_d < 1 || lambda_d > 1024 || (reinterpret_cast<uintptr_t>(lambda_out) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
+    const LambdaCall lc{lq1, lk1, lq2, lk2, lambda_per_head ? desc->num_heads : 1, lambda_d};
+    if (lc.n_sets < 1) return DIFFATTN_ERR_INVALID_ARG;
+    return fwd_common(desc, q, k, v, lambda_out, lambda_per_head, lambda_init, subln_w, causal, cu_seqlens, out,
+                      nullptr, nullptr, nullptr, stream, nullptr, &lc);
 }
 
 diffattn_status diffattn_fwd_rope_q(const diffattn_desc* desc, const void* q, const void* k, const void* v,

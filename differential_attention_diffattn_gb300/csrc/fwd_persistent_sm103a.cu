@@ -121,7 +121,10 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
         if (threadIdx.x == 0) atomicOr(p.error_word, kErrLayout);
         return;
     }
-    griddep_wait();
+    // A programmatic dependent of the previous kernel on the stream: nothing is
+    // read before it has completed, except with lambda_pending (that kernel writes
+    // lambda alone), where only the epilogue's reads of lambda wait.
+    if (!p.lambda_pending) griddep_wait();
     griddep_launch_dependents();
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
     const uint32_t sbase = smem_u32(smem);
@@ -335,6 +338,7 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
             uint8_t* base = smem + (half == 0 ? OFF_D : OFF_Q0 + (uint32_t)buf * Q_BYTES);
             return reinterpret_cast<float4*>(base + (uint32_t)r * 256u + (uint32_t)((i & 8) | ((i ^ r) & 7)) * 16u);
         };
+        if (p.lambda_pending) griddep_wait();  // lambda comes from the preceding grid
         int items = 0;
         for (;;) {
             const int slot = items % NSLOT;

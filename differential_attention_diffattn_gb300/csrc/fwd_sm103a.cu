@@ -108,8 +108,10 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     const uint32_t sbase = smem_u32(smem);
 
     // Launched as a programmatic dependent of the previous kernel on the stream
-    // (typically the lambda kernel): nothing is read before it has completed.
-    griddep_wait();
+    // (typically the lambda kernel): nothing is read before it has completed,
+    // except with lambda_pending, where that kernel writes lambda alone and only
+    // the producer's read of lambda waits (below).
+    if (!p.lambda_pending) griddep_wait();
     griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -227,6 +229,7 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
             }
         }
         __syncwarp();  // the barriers exist before any lane arrives on them
+        if (p.lambda_pending) griddep_wait();  // lambda comes from the preceding grid
         for (int i = lane; i < DV; i += 32) cp_async4(smem_u32(&ms.w[i]), p.subln_w + i);
         if (lane == 0) cp_async4(smem_u32(&ms.lam), p.lambda + h * p.lambda_stride);
         cp_async_arrive_noinc(bar_w_full);

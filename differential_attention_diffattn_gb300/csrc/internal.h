@@ -43,6 +43,11 @@ struct FwdParams {
     const float* rope_cos;    // rotary embedding of q inside the bf16 kernels (null: q is used as given):
     const float* rope_sin;    //   fp32 [rope_npos][rope_dim / 2] tables; position = index in the sequence
     int rope_npos, rope_dim, rope_interleaved;
+    int lambda_pending;       // bf16 kernels: 1 when the kernel launched just before this one on the stream
+                              // (by the same call) is the lambda kernel, which writes `lambda` and nothing
+                              // else: every other input is complete at launch, so only the reads of lambda
+                              // wait for that grid (the loads and the first tiles run under it); 0: every
+                              // read waits for the preceding grid
     float* lse;               // training outputs (all null, or all set; bf16 kernel only):
     void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
     void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c

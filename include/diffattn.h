@@ -148,6 +148,30 @@ diffattn_status diffattn_fwd(const diffattn_desc* desc, const void* q, const voi
                              const int* cu_seqlens, void* out, void* stream);
 
 /*
+ * The lambda reparameterisation and the forward in one call: diffattn_lambda
+ * into lambda_out, then diffattn_fwd reading it, on the same stream. The two
+ * formulas and their sources are those of the two entry points; the results
+ * are theirs bit for bit. Because this call launches the lambda kernel itself,
+ * right before the forward, the forward's loads, scores and softmax run while
+ * the lambda kernel finishes, and only its epilogue waits for lambda (through
+ * two separate calls every read of the forward waits for the kernel before it).
+ *  lq1, lk1, lq2, lk2: device fp32 [n_sets][lambda_d], n_sets = H when
+ *  lambda_per_head, else 1.
+ *  lambda_out: device fp32 [n_sets], written by this call (4-byte aligned).
+ *  Every other argument as in diffattn_fwd; the inputs must be complete when
+ *  the call is made on the stream, as for any stream-ordered call.
+ * Errors: those of diffattn_lambda (null vectors, lambda_d outside 1..1024)
+ *  and of diffattn_fwd, all checked before anything is launched. An empty
+ *  problem launches nothing (lambda_out is not written).
+ */
+diffattn_status diffattn_fwd_lambda(const diffattn_desc* desc, const void* q, const void* k,
+                                    const void* v, const float* lq1, const float* lk1,
+                                    const float* lq2, const float* lk2, int lambda_per_head,
+                                    int lambda_d, float lambda_init, float* lambda_out,
+                                    const float* subln_w, int causal, const int* cu_seqlens,
+                                    void* out, void* stream);
+
+/*
  * Forward for training: diffattn_fwd (bf16 tcgen05 kernel only) that also
  * saves what the backward pass needs, per (token, head):
  *  lse : device fp32 [tokens][H][2]: for component c, log2 of the softmax

@@ -235,6 +235,27 @@ def test_cache_forward_split_plan_from_host_lengths(lib):
     assert ws(8, 1, 16384, [16384] * 8) == 8 * per_split(8, 1)
 
 
+def test_fwd_lambda_rejects_on_host(lib):
+    """The combined lambda + forward call checks all its arguments before it
+    launches anything (no GPU here: a launch would fail with ERR_CUDA)."""
+    vp = ctypes.c_void_p
+
+    def call(vecs=(FAKE, FAKE, FAKE, FAKE), lam_d=64, lam_out=FAKE, **desc_kw):
+        base = dict(batch=1, seqlen=256, num_heads=16, num_kv_heads=4, d=64, dv=128, dtype=_lib.DTYPE_BF16, eps=1e-5)
+        base.update(desc_kw)
+        d = _lib.DiffAttnDesc(**base)
+        return lib.diffattn_fwd_lambda(ctypes.byref(d), vp(FAKE), vp(FAKE), vp(FAKE), *(vp(x) for x in vecs), 0, lam_d,
+                                       0.2, vp(lam_out), vp(FAKE), 1, None, vp(FAKE), None)
+    assert call(vecs=(FAKE, 0, FAKE, FAKE)) == 1   # a null lambda vector
+    assert call(lam_d=0) == 1
+    assert call(lam_d=2000) == 1
+    assert call(lam_out=0) == 1
+    assert call(lam_out=FAKE + 2) == 1              # misaligned lambda output
+    assert call(num_heads=15) == 1                  # the forward's own checks come first too
+    assert call(d=32, dv=64) == 2                   # no bf16 kernel for d = 32
+    assert call(batch=0) == 0                       # empty: nothing launched
+
+
 def test_fused_rope_forward_rejects_on_host(lib):
     vp = ctypes.c_void_p
 

@@ -224,6 +224,45 @@ def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv):
         assert torch.equal(run_gpu(one), full[a:b])
 
 
+# The combined call (lambda kernel, then the forward whose reads of lambda alone
+# wait for it) against the two calls, on each forward kernel: the one-item-per-CTA
+# bf16 kernel, the persistent one (dense and packed), the fp32 one; lambdas shared
+# and per head.
+@pytest.mark.parametrize("case", ["tile", "persistent", "packed", "per_head", "f32"])
+def test_fwd_lambda_equals_two_calls_bitwise(case):
+    if case == "f32":
+        wl, lens = W.WORKLOADS["tiny_f32"], [64]
+    elif case == "per_head":
+        wl, lens = W.with_overrides(BF, lambda_per_head=True, random_subln=True), [1000, 1000, 1000]
+    else:
+        wl = W.with_overrides(BF, num_heads=16, num_kv_heads=4)
+        lens = {"tile": [700], "persistent": [1000, 1000, 1000], "packed": [1000, 40, 2500, 300]}[case]
+    inp = W.generate(wl, seed=41, seq_lens=lens)
+    t = {n: getattr(inp, n).cuda() for n in ("q", "k", "v", "lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2",
+                                             "subln_w", "cu_seqlens")}
+    li = da.diffattn_lambda_init(wl.depth)
+    vecs = [t["lambda_q1"], t["lambda_k1"], t["lambda_q2"], t["lambda_k2"]]
+    packed = case == "packed"
+    B, T = len(lens), lens[0]
+    sh = (lambda x: x) if packed else (lambda x: x.view(B, T, *x.shape[1:]))  # noqa: E731
+    kw = dict(cu_seqlens=t["cu_seqlens"], max_seqlen=max(lens)) if packed else {}
+    kern = da.diffattn_fwd_kernel(sh(t["q"]), sh(t["k"]), sh(t["v"]), torch.ones(1, device="cuda"), t["subln_w"],
+                                  **kw)
+    want_kernel = {"tile": "diffattn_fwd_bf16_sm103a_kernel", "persistent": "diffattn_fwd_bf16_persistent_kernel",
+                   "packed": "diffattn_fwd_bf16_persistent_kernel", "per_head": "diffattn_fwd_bf16_persistent_kernel",
+                   "f32": "diffattn_fwd_f32_kernel"}[case]
+    assert kern == want_kernel
+    lam = da.diffattn_lambda(*vecs, li)
+    two = da.diffattn_fwd(sh(t["q"]), sh(t["k"]), sh(t["v"]), lam, li, t["subln_w"], causal=wl.causal, eps=wl.eps,
+                          **kw)
+    for _ in range(2):  # twice, the second time over the first call's outputs
+        one, lam1 = da.diffattn_fwd_lambda(sh(t["q"]), sh(t["k"]), sh(t["v"]), *vecs, li, t["subln_w"],
+                                           causal=wl.causal, eps=wl.eps, **kw)
+        assert da.diffattn_get_device_status() == 0
+        assert torch.equal(lam1, lam)
+        assert torch.equal(one, two)
+
+
 def test_gqa_equals_replicated_bitwise():
     inp = W.generate(BF, seed=32, seq_lens=[400])
     a = run_gpu(inp)
