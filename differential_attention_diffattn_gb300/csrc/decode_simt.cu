@@ -35,13 +35,25 @@ constexpr int SPLITS_PER_ROUND = 4;
 
 __global__ void __launch_bounds__(32 * CWARPS)
 diffattn_decode_combine_kernel(const KvParams p) {
-    griddep_wait();  // a programmatic dependent of the split kernel: its partials are complete
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * CWARPS + (threadIdx.x >> 5);  // ((b * q_len) + t) * H + h
-    if (row >= (long long)p.batch * p.q_len * p.H) return;
+    const bool row_ok = row < (long long)p.batch * p.q_len * p.H;
     const int h = (int)(row % p.H);
     const int b = (int)(row / ((long long)p.H * p.q_len));
-    const int L = p.cache_seqlens ? p.cache_seqlens[b] : p.capacity;
+    // The inputs of the call (lengths, weight, lambda) are read before the wait for
+    // the split kernel: this grid is placed only once every split CTA has passed its
+    // own wait for the kernels before it (the lambda kernel among them), so they are
+    // complete; only the partials come from the split kernel.
+    int L = 0;
+    float lam = 0.f;
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok) {  // from L2 (ld.global.cg): no line an earlier grid left in this SM's L1
+        L = p.cache_seqlens ? __ldcg(p.cache_seqlens + b) : p.capacity;
+        lam = __ldcg(p.lambda + h * p.lambda_stride);
+        w = __ldcg(reinterpret_cast<const float4*>(p.subln_w) + lane);
+    }
+    griddep_wait();  // a programmatic dependent of the split kernel: its partials are complete
+    if (!row_ok) return;
     if (L < p.q_len || L > p.capacity) return;  // reported by the split kernel
     const int n = p.num_splits;
     const float* ml = p.ws_ml + (size_t)row * n * 4;              // [split][component][m, l]
@@ -91,12 +103,10 @@ diffattn_decode_combine_kernel(const KvParams p) {
         }
     }
     const float i1 = 1.f / lsum[0], i2 = 1.f / lsum[1];  // every row sees at least one key
-    const float lam = p.lambda[h * p.lambda_stride];
     const float4 d = make_float4(acc[0].x * i1 - lam * (acc[1].x * i2), acc[0].y * i1 - lam * (acc[1].y * i2),
                                  acc[0].z * i1 - lam * (acc[1].z * i2), acc[0].w * i1 - lam * (acc[1].w * i2));
     const float ss = warp_sum(d.x * d.x + d.y * d.y + d.z * d.z + d.w * d.w);
     const float post = (1.f - p.lambda_init) / sqrtf(ss / (float)DVD + p.eps);
-    const float4 w = reinterpret_cast<const float4*>(p.subln_w)[lane];
     __nv_bfloat162 lo = __floats2bfloat162_rn(d.x * post * w.x, d.y * post * w.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(d.z * post * w.z, d.w * post * w.w);
     uint2 u2;
