@@ -105,8 +105,37 @@ diffattn_bwd_pre_kernel(const BwdPreParams p) {
             st.x = *reinterpret_cast<uint32_t*>(&lo2);
             st.y = *reinterpret_cast<uint32_t*>(&hi2);
             reinterpret_cast<uint2*>(p.dd)[row * (DVD / 4) + lane] = st;
-            if (lane == 0)  // negated: the backward kernels add them to products
+            if (lane == 0) {  // negated: the backward kernels add them to products
                 reinterpret_cast<float4*>(p.rowstat)[(size_t)h * p.tokens + t] = make_float4(-lse1, -lse2, -d1, -d2);
+                // the dK/dV kernel's row operand: values split into bf16 terms whose sum
+                // carries about 24 bits (each term rounds the remainder of the ones before)
+                const float u1 = -lse1 / p.scale_log2, u2 = -lse2 / p.scale_log2, e1 = -d1, cd = d1 - d2;
+                alignas(16) __nv_bfloat16 v[16];
+                auto split3 = [&](float x, int at) {
+                    const __nv_bfloat16 a = __float2bfloat16_rn(x);
+                    const float r1 = x - __bfloat162float(a);
+                    const __nv_bfloat16 b = __float2bfloat16_rn(r1);
+                    v[at] = a;
+                    v[at + 1] = b;
+                    v[at + 2] = __float2bfloat16_rn(r1 - __bfloat162float(b));
+                };
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __float2bfloat16_rn(0.f);
+                split3(u1, 0);
+                split3(u2, 3);
+                split3(e1, 6);
+                // delta_1 - delta_2 as two bf16 terms in slots 12-13 of this row and in slots
+                // 14-15 of the row before, so that one 8-byte load gives a row and its successor
+                const __nv_bfloat16 ch = __float2bfloat16_rn(cd);
+                v[12] = ch;
+                v[13] = __float2bfloat16_rn(cd - __bfloat162float(ch));
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.stat_aug) + ((size_t)h * p.tokens + t) * 16;
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&v[0]);
+                *reinterpret_cast<uint2*>(dst + 8) = *reinterpret_cast<const uint2*>(&v[8]);
+                *reinterpret_cast<uint32_t*>(dst + 12) = *reinterpret_cast<const uint32_t*>(&v[12]);
+                if (t > 0) *reinterpret_cast<uint32_t*>(dst - 2) = *reinterpret_cast<const uint32_t*>(&v[12]);
+                if (t == p.tokens - 1) *reinterpret_cast<uint32_t*>(dst + 14) = 0u;  // no successor: finite zeros
+            }
         }
     }
 #pragma unroll

@@ -46,12 +46,6 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t a) { return smem_desc_sw128(
 __device__ __forceinline__ uint64_t desc_mn(uint32_t a, uint32_t box) { return smem_desc_sw128(a, box, 1024); }
 __device__ __forceinline__ bool warp_all(bool p) { return __all_sync(0xffffffffu, p); }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // ---- sequence bounds (uniform over the CTA); false: nothing to do / bad lengths
 __device__ __forceinline__ bool seq_bounds(const BwdParams& p, int seq, int* start, int* len) {
     if (p.cu_seqlens != nullptr) {
@@ -387,22 +381,49 @@ diffattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // N >= 64: below that an MMA with both operands in shared memory is bound by the
 // operand bandwidth (measured 40 cycles at N = 32, 48 at N = 64, 64 at N = 128
 // for M128 K16), and a 64-row block as two 32-row halves took 44 MMAs instead of 28.
+// The row statistics enter the score and dP MMAs as one more 16-wide K step: the
+// row operand holds -lse_c / (s log2 e) and -delta_1 split into three bf16 terms
+// each (slots 0-2, 3-5, 6-8; written by the preprocessing kernel), the key operand
+// is one of three constant tiles with ones in the matching three slots, so
+//   S_c^T' = S_c^T - lse_c / (s log2 e)   ->  P_c = 2^(S_c^T' s log2 e),
+//   dP^T'  = dP^T - delta_1               ->  dS_1 / s = P_1 dP^T',
+// and of the statistics only delta_1 - delta_2 is read, for
+// dS_2 / s = -lambda P_2 (dP^T' + delta_1 - delta_2): slots 12-13 of row r hold it as
+// two bf16 terms and slots 14-15 hold the next row's, one 8-byte load for two rows.
+// The per-row loads of all four statistics (a broadcast 16-byte shared load per row
+// and warp, two wavefronts) had been half of this kernel's shared-memory traffic.
+// The 16-wide operands use the 32-byte swizzle: 32-byte rows, 16-byte chunk c of row
+// r at c ^ ((r / 4) % 2).
 namespace dkv {
 constexpr int BK = 128, BQ = 64, STAGES = 4;
 constexpr uint32_t COL_DS = 192;                   // dS_1^T [192, 224), dS_2^T [224, 256): bf16 pairs
 constexpr uint32_t COL_DV = 256, COL_DK = 384;     // dV [256, 384), dK1 [384, 448), dK2 [448, 512)
 constexpr uint32_t KBOX = 128 * ROW;               // [128 keys x 64] 16 KB
 constexpr uint32_t QBOX = 64 * ROW;                // [64 rows x 64] 8 KB
+constexpr uint32_t AUG_ROW = 32;                   // a 16-wide bf16 row of the extra K step
+constexpr uint32_t ONES = 8 * AUG_ROW;             // one 8-row group, read for all 128 keys
 constexpr uint32_t OFF_K = 0;                      // K1 | K2
 constexpr uint32_t OFF_V = 2 * KBOX;               // V lo | V hi
-constexpr uint32_t OFF_ST = 4 * KBOX;              // stages: Q1 | Q2 | dD lo | dD hi | row stats
-constexpr uint32_t ST_STAT = 4 * QBOX;
-constexpr uint32_t STAGE = 4 * QBOX + 1024;
+constexpr uint32_t OFF_ONES = 4 * KBOX;            // three key-side tiles of the extra K step
+constexpr uint32_t OFF_ST = OFF_ONES + 1024;       // stages: Q1 | Q2 | dD lo | dD hi | row operand
+constexpr uint32_t ST_AUG = 4 * QBOX;              // the stage's row operand, [64 rows x 16]
+constexpr uint32_t STAGE = 4 * QBOX + 2048;        // 2 KB of row operand
 constexpr uint32_t OFF_P = OFF_ST + STAGES * STAGE;  // (P_1 - lambda P_2)^T: [128 keys x 64 rows] bf16, K-major
 constexpr uint32_t OFF_MISC = OFF_P + 128 * ROW;
 constexpr uint32_t SMEM = 1024 + OFF_MISC + 512;
 static_assert(SMEM <= 232448, "smem");
-static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+static_assert(STAGE % 1024 == 0 && OFF_ST % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+// K-major operand of one 16-wide K step in the 32-byte swizzle: 8-row groups sbo bytes apart
+// (256 for a dense tile; 0 repeats one group, every row of the key-side tiles being the same).
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;   // leading byte offset: unused (one atom along K)
+    d |= (uint64_t)(sbo >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)6u << 61;           // layout: 32-byte swizzle
+    return d;
+}
 struct Misc {
     uint64_t kv_full, st_full[STAGES], st_empty[STAGES], acc_done;
     uint64_t s_ready, sdp_free, ops_ready, ops_free;
@@ -411,40 +432,42 @@ struct Misc {
 };
 }  // namespace dkv
 
-// 16-byte load from a shared-window address (the statistics the bulk copy wrote;
-// ordered after the barrier wait that published them).
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
+// delta_1 - delta_2 of block rows r and r + 1 from the stage's row operand: slots 12-15 of
+// row r (two bf16 terms for each of the two rows, chunk 1 of the row under the 32-byte
+// swizzle).
+__device__ __forceinline__ float2 aug_c2(uint32_t aug, int r) {
+    uint32_t a, b;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                 : "=r"(a), "=r"(b)
+                 : "r"(aug + (uint32_t)r * 32u + ((uint32_t)(1 ^ ((r >> 2) & 1)) << 4) + 8u));
+    return make_float2(__uint_as_float(a << 16) + __uint_as_float(a & 0xffff0000u),
+                       __uint_as_float(b << 16) + __uint_as_float(b & 0xffff0000u));
 }
 
-// One thread (= one key) and N query rows: P_1 - lambda P_2, dS_1, dS_2 as bf16
-// pairs from S_1^T, S_2^T, dP^T and the rows' statistics, stored negated
-// (-lse_1, -lse_2, -delta_1, -delta_2), on packed fp32 pairs of adjacent rows:
-//   P_c = 2^(S_c s log2(e) - lse_c),  -lambda P_2,  P_1 - lambda P_2,
-//   dS_1 / s = P_1 (dP - delta_1),  dS_2 / s = -lambda P_2 (dP - delta_2).
+// One thread (= one key) and N query rows r0 + i: P_1 - lambda P_2, dS_1, dS_2 as
+// bf16 pairs from S_1^T', S_2^T', dP^T' (the statistics already subtracted by the
+// extra K step) and delta_1 - delta_2, on packed fp32 pairs of adjacent rows:
+//   P_c = 2^(S_c^T' s log2(e)),  -lambda P_2,  P_1 - lambda P_2,
+//   dS_1 / s = P_1 dP^T',  dS_2 / s = -lambda P_2 (dP^T' + delta_1 - delta_2).
 // MASK zeroes rows outside [q_min, q_end); without it every row is visible.
 // The exponentials run on every element and masking is a select after the
-// products, so stale statistics of rows past the end never reach the results.
+// products, so the operands of rows past the end never reach the results.
 template <bool MASK, int N>
 __device__ __forceinline__ void dkv_rows(const uint32_t (&s1)[N], const uint32_t (&s2)[N], const uint32_t (&dp)[N],
-                                         uint32_t stat, float lam, float sl2, int q0, int q_end, int q_min,
+                                         uint32_t aug, int r0, float lam, float sl2, int q0, int q_end, int q_min,
                                          uint32_t (&pc)[N / 2], uint32_t (&d1)[N / 2], uint32_t (&d2)[N / 2]) {
     const uint64_t sl2p = f2_pack(sl2, sl2), nlam = f2_pack(-lam, -lam);
 #pragma unroll
     for (int i = 0; i < N; i += 2) {
-        const float4 ra = lds_f4(stat + 16u * (uint32_t)i), rb = lds_f4(stat + 16u * (uint32_t)(i + 1));
-        const float2 x1 = f2_unpack(ffma2(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])), sl2p,
-                                          f2_pack(ra.x, rb.x)));
-        const float2 x2 = f2_unpack(ffma2(f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])), sl2p,
-                                          f2_pack(ra.y, rb.y)));
+        const float2 cc = aug_c2(aug, r0 + i);
+        const float2 x1 = f2_unpack(fmul2(f2_pack(__uint_as_float(s1[i]), __uint_as_float(s1[i + 1])), sl2p));
+        const float2 x2 = f2_unpack(fmul2(f2_pack(__uint_as_float(s2[i]), __uint_as_float(s2[i + 1])), sl2p));
         const uint64_t p1 = f2_pack(ex2_approx(x1.x), ex2_approx(x1.y));
         const uint64_t q2 = fmul2(f2_pack(ex2_approx(x2.x), ex2_approx(x2.y)), nlam);  // -lambda P_2
         const uint64_t pp = f2_pack(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1]));
         float2 a = f2_unpack(fadd2(p1, q2));
-        float2 b1 = f2_unpack(fmul2(p1, fadd2(pp, f2_pack(ra.z, rb.z))));
-        float2 b2 = f2_unpack(fmul2(q2, fadd2(pp, f2_pack(ra.w, rb.w))));
+        float2 b1 = f2_unpack(fmul2(p1, pp));
+        float2 b2 = f2_unpack(fmul2(q2, fadd2(pp, f2_pack(cc.x, cc.y))));
         if (MASK) {
             const int qi = q0 + i;
             const bool v0 = (qi < q_end) & (qi >= q_min), v1 = (qi + 1 < q_end) & (qi + 1 >= q_min);
@@ -473,7 +496,7 @@ __device__ __forceinline__ void store_op_row(uint32_t tile, int k, int w, const 
 __global__ void __launch_bounds__(NT, 1)
 diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dd,
-                        const BwdParams p) {
+                        const __grid_constant__ CUtensorMap tm_aug, const BwdParams p) {
     using namespace dkv;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -523,6 +546,26 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         ms.abort_flag = 0;
         fence_barrier_init();
     }
+    if (threadIdx.x < 8) {
+        // the key-side tiles of the extra K step: tile j holds bf16 ones in slots 3j..3j+2
+        // of each of its 8 rows (the MMAs read the group for every 8 keys)
+        const int k = threadIdx.x;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            uint32_t wd[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t lo = (2 * i >= 3 * j && 2 * i < 3 * j + 3) ? 0x3F80u : 0u;
+                const uint32_t hi = (2 * i + 1 >= 3 * j && 2 * i + 1 < 3 * j + 3) ? 0x3F80u : 0u;
+                wd[i] = lo | (hi << 16);
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                sts_u4(sb + OFF_ONES + (uint32_t)j * ONES + (uint32_t)k * AUG_ROW + ((uint32_t)(c ^ ((k >> 2) & 1)) << 4),
+                       make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]));
+        }
+        fence_proxy_async_smem();  // visible to the tensor cores (ordered by the barrier below)
+    }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem), 512);
     tc_fence_before();
     __syncthreads();
@@ -546,14 +589,13 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 const uint32_t st = sb + OFF_ST + (uint32_t)s * STAGE;
                 const int hh = item_head(it);
                 const int t0 = start + item_row0(it);
-                const int nrow = min(BQ, p.total_tokens - t0);  // row stats past the last token are not read
-                const uint32_t stat_bytes = (uint32_t)nrow * 16u;
-                mbar_arrive_expect_tx(b_sf(s), 4 * QBOX + stat_bytes);
+                mbar_arrive_expect_tx(b_sf(s), 4 * QBOX + BQ * AUG_ROW);
                 tma_load_2d(st, &tm_q, b_sf(s), hh * 2 * HD, t0, pol);
                 tma_load_2d(st + QBOX, &tm_q, b_sf(s), hh * 2 * HD + HD, t0, pol);
                 tma_load_2d(st + 2 * QBOX, &tm_dd, b_sf(s), hh * DV, t0, pol);
                 tma_load_2d(st + 3 * QBOX, &tm_dd, b_sf(s), hh * DV + 64, t0, pol);
-                bulk_load(st + ST_STAT, p.rowstat + ((size_t)hh * p.total_tokens + t0) * 4, stat_bytes, b_sf(s));
+                // the rows' operand of the extra K step (rows past the tokens read as zero)
+                tma_load_2d(st + ST_AUG, &tm_aug, b_sf(s), 0, hh * p.total_tokens + t0, pol);
                 issued = it + 1;
             }
             mbar_wait_drain(b_kv, 0, p.timeout_ns);
@@ -577,15 +619,18 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         // = 128 over the two 64-column halves of V and of dD).
         auto issue_sdp = [&](int it) {
             const uint64_t sq = d_q + (uint64_t)(it % STAGES) * SG;
+            const uint64_t sa = desc_sw32(sb + OFF_ST + (uint32_t)(it % STAGES) * STAGE + ST_AUG, 256u);
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ss_elect(tmem + c * 64, d_k + c * KB + kk * KS, sq + c * QB + kk * KS, id_s, kk > 0);
+                mma_ss_elect(tmem + c * 64, desc_sw32(sb + OFF_ONES + (uint32_t)c * ONES, 0u), sa, id_s, 1u);  // - lse_c
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 mma_ss_elect(tmem + 128, d_v + (kk >> 2) * KB + (kk & 3) * KS,
                              sq + 2 * QB + (kk >> 2) * QB + (kk & 3) * KS, id_s, kk > 0);
+            mma_ss_elect(tmem + 128, desc_sw32(sb + OFF_ONES + 2 * ONES, 0u), sa, id_s, 1u);  // - delta_1
             mma_commit_elect(b_s);
         };
         // dV += (P_1 - lambda P_2)^T dD and dK_c += dS_c^T Q_c over the block's 64 rows, 16 a
@@ -649,8 +694,8 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(b_free);  // the next block's scores may overwrite the buffer
             const int s = it % STAGES;
-            // row statistics of the block (shared-window address: explicit shared loads)
-            const uint32_t stat = sb + OFF_ST + (uint32_t)s * STAGE + ST_STAT + 16u * (uint32_t)(32 * w);
+            // the block's row operand (delta_1 - delta_2 per row; shared-window address)
+            const uint32_t aug = sb + OFF_ST + (uint32_t)s * STAGE + ST_AUG;
             const int hh = item_head(it);
             const float lam = p.lambda[hh * p.lambda_stride];
             const int row0 = item_row0(it);
@@ -659,9 +704,9 @@ diffattn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             const bool need_mask = row0 + BQ > len || kt * BK + BK > len || (p.causal && row0 < kt * BK + BK - 1);
             uint32_t pc[16], d1[16], d2[16];
             if (need_mask)
-                dkv_rows<true, 32>(s1, s2, dp, stat, lam, sl2, row0 + 32 * w, q_end, q_min, pc, d1, d2);
+                dkv_rows<true, 32>(s1, s2, dp, aug, 32 * w, lam, sl2, row0 + 32 * w, q_end, q_min, pc, d1, d2);
             else
-                dkv_rows<false, 32>(s1, s2, dp, stat, lam, sl2, 0, 0, 0, pc, d1, d2);
+                dkv_rows<false, 32>(s1, s2, dp, aug, 32 * w, lam, sl2, 0, 0, 0, pc, d1, d2);
             // the previous block's operands have been read by its dV / dK MMAs
             if (it > 0 && !(ok = warp_all(mbar_wait(b_opf, (uint32_t)(it - 1) & 1u, ab)))) break;
             store_op_row(sb + OFF_P, k, w, pc);
@@ -742,7 +787,7 @@ cudaError_t launch_bwd_sm103a(const BwdParams& p, const BwdTensorMaps& m, cudaSt
     const dim3 dkv_grid = p.dkv_tiles_outer ? dim3((unsigned)p.Hkv, (unsigned)p.num_seqs, (unsigned)n_kt)
                                             : dim3((unsigned)(p.Hkv * n_kt), 1u, (unsigned)p.num_seqs);
     diffattn_bwd_dkv_kernel<<<dkv_grid, NT, dkv::SMEM, stream>>>(
-        m.q64, m.k128, m.v128, m.dd64, p);
+        m.q64, m.k128, m.v128, m.dd64, m.aug64, p);
     return cudaGetLastError();
 }
 

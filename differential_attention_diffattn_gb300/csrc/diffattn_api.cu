@@ -84,6 +84,20 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over [rows][16] (32-byte rows): boxes of 16 x 64 rows with the
+// 32-byte swizzle, as K-major MMA operands of one 16-wide K step.
+bool encode_bf16_aug(CUtensorMap* map, const void* base, uint64_t rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {16, rows};
+    const cuuint64_t strides[1] = {32};
+    const cuuint32_t box[2] = {16, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // SM count of the current device (looked up once per device).
@@ -603,11 +617,13 @@ diffattn_status diffattn_fwd_kvcache_noalloc(const diffattn_kv_desc* desc, const
                                 subln_w, causal, scratch, DIFFATTN_NOALLOC_SCRATCH_BYTES, out, stream);
 }
 
+// Backward workspace: dD (bf16 [tokens][H][dv]), the row statistics (16 bytes a row)
+// and the dK/dV kernel's row operand (16 bf16 a row).
 unsigned long long diffattn_bwd_workspace_size(const diffattn_desc* desc) {
     if (!desc || desc->num_heads <= 0 || desc->dv <= 0) return 0;
     long long tokens = desc->batch > 0 && desc->seqlen > 0 ? (long long)desc->batch * desc->seqlen : 0;
     if (desc->total_tokens > 0) tokens = desc->total_tokens > tokens ? desc->total_tokens : tokens;
-    return (unsigned long long)tokens * desc->num_heads * ((unsigned long long)desc->dv * 2 + 16);
+    return (unsigned long long)tokens * desc->num_heads * ((unsigned long long)desc->dv * 2 + 16 + 32);
 }
 
 diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const void* k, const void* v,
@@ -637,7 +653,10 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
         max_seqlen = ds.max_seqlen;
         tokens = ds.total_tokens;
     }
-    if (num_seqs > 65535 || (long long)tokens * ds.num_heads * ds.dv >= (1LL << 40)) return DIFFATTN_ERR_INVALID_ARG;
+    // (the rows of the dK/dV kernel's row operand, H x tokens, are 32-bit TMA coordinates)
+    if (num_seqs > 65535 || (long long)tokens * ds.num_heads * ds.dv >= (1LL << 40) ||
+        (long long)tokens * ds.num_heads > INT32_MAX - 64)
+        return DIFFATTN_ERR_INVALID_ARG;
     if (tokens == 0 || num_seqs == 0 || max_seqlen == 0) return DIFFATTN_OK;
     const void* b16[] = {q, k, v, dout, o1, o2, dq, dk, dv, workspace};
     for (const void* ptr : b16)
@@ -647,7 +666,7 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
         if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
     const unsigned long long dd_bytes = (unsigned long long)tokens * ds.num_heads * ds.dv * 2;
-    if (workspace_bytes < dd_bytes + (unsigned long long)tokens * ds.num_heads * 16) return DIFFATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < dd_bytes + (unsigned long long)tokens * ds.num_heads * (16 + 32)) return DIFFATTN_ERR_INVALID_ARG;
 
     unsigned int* err_word = nullptr;
     if (error_word_ptr(&err_word) != cudaSuccess) return DIFFATTN_ERR_CUDA;
@@ -659,6 +678,7 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
 
     void* dd = workspace;
     float* rowstat = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + dd_bytes);
+    void* stat_aug = static_cast<uint8_t*>(workspace) + dd_bytes + (unsigned long long)tokens * ds.num_heads * 16;
     BwdPreParams pre{};
     pre.dout = dout;
     pre.o1 = o1;
@@ -673,6 +693,8 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     pre.H = ds.num_heads;
     pre.dd = dd;
     pre.rowstat = rowstat;
+    pre.stat_aug = stat_aug;
+    pre.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
     pre.dlambda = dlambda;
     pre.dsubln_w = dsubln_w;
     if (launch_bwd_pre(pre, st) != cudaSuccess) return DIFFATTN_ERR_CUDA;
@@ -691,6 +713,7 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     p.scale = (float)(1.0 / std::sqrt((double)ds.d));
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
     p.rowstat = rowstat;
+    p.stat_aug = stat_aug;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -700,11 +723,11 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     p.dkv_tiles_outer = causal && bwd_tiles_outermost(num_seqs, p.Hkv, max_seqlen) ? 1 : 0;
     // launch groups whose streamed operands fit in 32 MB of L2: for the dQ kernel the
     // K / V of its heads (as the forward), for the dK/dV kernel the Q and dD of every
-    // head of its kv heads (2d + dv bf16 and 16 bytes of row statistics per token)
+    // head of its kv heads (2d + dv bf16 and the 32-byte row operand per token)
     p.dq_group_heads = fwd_group_heads(p.H, p.Hkv, max_seqlen);
     {
         const int G = p.H / p.Hkv;
-        const double kv_group_bytes = (double)max_seqlen * G * ((2 * 64 + 128) * 2 + 16);
+        const double kv_group_bytes = (double)max_seqlen * G * ((2 * 64 + 128) * 2 + 32);
         int kg = (int)((32.0 * (1 << 20)) / (kv_group_bytes > 1.0 ? kv_group_bytes : 1.0));
         kg = kg < 1 ? 1 : (kg > p.Hkv ? p.Hkv : kg);
         while (p.Hkv % kg != 0) --kg;
@@ -715,7 +738,8 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     const uint64_t vw = (uint64_t)ds.num_kv_heads * ds.dv, dw = (uint64_t)ds.num_heads * ds.dv;
     if (!encode_bf16_rows(&m.q128, q, qw, tokens, 128) || !encode_bf16_rows(&m.q64, q, qw, tokens, 64) ||
         !encode_bf16_rows(&m.k128, k, kw, tokens, 128) || !encode_bf16_rows(&m.v128, v, vw, tokens, 128) ||
-        !encode_bf16_rows(&m.dd128, dd, dw, tokens, 128) || !encode_bf16_rows(&m.dd64, dd, dw, tokens, 64))
+        !encode_bf16_rows(&m.dd128, dd, dw, tokens, 128) || !encode_bf16_rows(&m.dd64, dd, dw, tokens, 64) ||
+        !encode_bf16_aug(&m.aug64, stat_aug, (uint64_t)tokens * ds.num_heads))
         return DIFFATTN_ERR_CUDA;
     return launch_bwd_sm103a(p, m, st) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }

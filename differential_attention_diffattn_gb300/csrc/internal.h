@@ -98,6 +98,10 @@ struct BwdParams {
     int H, Hkv;
     float scale, scale_log2;
     const float* rowstat;      // [H][tokens][4]: -lse1, -lse2, -delta1, -delta2 (workspace)
+    // [H][tokens][16] bf16 (workspace), the row operand of the dK/dV kernel's extra K step:
+    // slots 0-2 and 3-5 split -lse_c / scale_log2 into three bf16 terms (c = 1, 2), 6-8 split
+    // -delta_1, 10-11 hold delta_1 - delta_2 as two terms, the rest zero
+    const void* stat_aug;
     void* dq;                  // [tokens][H][2d]
     void* dk;                  // [tokens][Hkv][2d]
     void* dv;                  // [tokens][Hkv][dv]
@@ -113,6 +117,7 @@ struct BwdParams {
 // k and v with 128-row boxes.
 struct BwdTensorMaps {
     CUtensorMap q128, q64, k128, v128, dd128, dd64;
+    CUtensorMap aug64;  // stat_aug as [H * tokens][16], 64-row boxes, 32-byte swizzle
 };
 
 // Per-row preprocessing of the backward (CUDA cores).
@@ -129,6 +134,8 @@ struct BwdPreParams {
     int tokens, H;
     void* dd;                  // out: [tokens][H][dv] bf16, gradient of the pre-norm output
     float* rowstat;            // out: [H][tokens][4], negated
+    void* stat_aug;            // out: [H][tokens][16] bf16 (BwdParams::stat_aug)
+    float scale_log2;          // d^-0.5 * log2(e)
     float* dlambda;            // out (accumulated): [H] or [1]
     float* dsubln_w;           // out (accumulated): [dv]
 };

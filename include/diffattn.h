@@ -191,8 +191,8 @@ diffattn_status diffattn_fwd_train(const diffattn_desc* desc, const void* q, con
 
 /*
  * Bytes of device workspace diffattn_bwd needs for `desc`: tokens x H x
- * (2 dv + 16) (the gradient of the pre-norm output in bf16 and four fp32 row
- * statistics per (token, head)).
+ * (2 dv + 48) (the gradient of the pre-norm output in bf16, four fp32 row
+ * statistics and 16 bf16 of the dK/dV kernel's row operand per (token, head)).
  */
 unsigned long long diffattn_bwd_workspace_size(const diffattn_desc* desc);
 
@@ -208,7 +208,8 @@ unsigned long long diffattn_bwd_workspace_size(const diffattn_desc* desc);
  * statistics of both softmaxes, the lambda and weight gradients), a dQ kernel
  * and a dK/dV kernel (tcgen05; grouped kv heads summed inside the CTA).
  * workspace: device, 16-byte aligned, >= diffattn_bwd_workspace_size(desc).
- * Errors: as diffattn_fwd; UNSUPPORTED for anything but bf16 with d = 64.
+ * Errors: as diffattn_fwd (and INVALID_ARG for tokens x H beyond 2^31 - 64);
+ * UNSUPPORTED for anything but bf16 with d = 64.
  * Use diffattn_lambda_bwd to turn the lambda gradient into the gradients of the
  * four lambda vectors.
  */
