@@ -697,6 +697,8 @@ diffattn_status diffattn_bwd(const diffattn_desc* desc, const void* q, const voi
     pre.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)ds.d));
     pre.dlambda = dlambda;
     pre.dsubln_w = dsubln_w;
+    pre.error_word = err_word;
+    pre.timeout_ns = g_timeout_ns;
     if (launch_bwd_pre(pre, st) != cudaSuccess) return DIFFATTN_ERR_CUDA;
 
     BwdParams p{};

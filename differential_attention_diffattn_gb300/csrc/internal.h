@@ -138,6 +138,8 @@ struct BwdPreParams {
     float scale_log2;          // d^-0.5 * log2(e)
     float* dlambda;            // out (accumulated): [H] or [1]
     float* dsubln_w;           // out (accumulated): [dv]
+    unsigned int* error_word;  // device error bits (a wait that timed out)
+    uint64_t timeout_ns;       // bound of every wait
 };
 
 // Rotary embedding of q [tokens][H][width] and k [tokens][Hkv][width] (width = 2d).

@@ -116,6 +116,10 @@ def test_training_outputs_match_oracle(lens, kernel):
     # kernels wrap several times, and the last blocks run past the sequences' ends
     ([1000], 16, 4, True, True),
     ([777, 1000], 8, 8, True, False),
+    # token x head rows not a multiple of the preprocessing kernel's 4-row chunks (a last
+    # chunk of 3 rows; per-head and shared lambda)
+    ([333], 3, 1, True, True),
+    ([301, 2], 5, 5, True, False),
 ])
 def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
     wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv, causal=causal, lambda_per_head=per_head,
