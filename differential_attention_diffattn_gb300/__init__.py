@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     diffattn_fwd_rope_q,
     diffattn_fwd_train,
     diffattn_fwd_kvcache,
+    diffattn_fwd_kvcache_lambda,
     diffattn_fwd_kvcache_noalloc,
     diffattn_fwd_kvcache_workspace_size,
     diffattn_get_device_status,

@@ -23,7 +23,7 @@ EXPORTED = ("diffattn_lambda_init", "diffattn_lambda", "diffattn_fwd", "diffattn
             "diffattn_fwd_kvcache", "diffattn_fwd_kvcache_noalloc", "diffattn_get_device_status",
             "diffattn_status_string", "diffattn_set_wait_timeout_ns", "diffattn_set_fault_injection",
             "diffattn_rope_tables", "diffattn_rope_qk", "diffattn_merge_partials", "diffattn_out_proj",
-            "diffattn_fwd_kernel", "diffattn_fwd_rope_q", "diffattn_fwd_lambda")
+            "diffattn_fwd_kernel", "diffattn_fwd_rope_q", "diffattn_fwd_lambda", "diffattn_fwd_kvcache_lambda")
 
 
 class DiffAttnDesc(ctypes.Structure):
@@ -113,6 +113,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.diffattn_fwd_kvcache.restype = ctypes.c_int
         lib.diffattn_fwd_kvcache.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, ctypes.c_int,
                                              ctypes.c_float, vp, ctypes.c_int, vp, ctypes.c_ulonglong, vp, vp]
+        lib.diffattn_fwd_kvcache_lambda.restype = ctypes.c_int
+        lib.diffattn_fwd_kvcache_lambda.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, vp, vp, vp,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_float, vp, vp, ctypes.c_int,
+                                                    vp, ctypes.c_ulonglong, vp, vp]
         lib.diffattn_fwd_kvcache_noalloc.restype = ctypes.c_int
         lib.diffattn_fwd_kvcache_noalloc.argtypes = [ctypes.POINTER(DiffAttnKvDesc), vp, vp, vp, vp, vp, ctypes.c_int,
                                                      ctypes.c_float, vp, ctypes.c_int, vp, vp]
@@ -519,6 +523,51 @@ def diffattn_fwd_kvcache(q, k_cache, v_cache, lam, lambda_init: float, subln_w, 
     if st != OK:
         raise DiffAttnError(st, "diffattn_fwd_kvcache")
     return out
+
+
+def diffattn_fwd_kvcache_lambda(q, k_cache, v_cache, lambda_q1, lambda_k1, lambda_q2, lambda_k2, lambda_init: float,
+                                subln_w, cache_seqlens=None, causal: bool = True, eps: float = 1e-5,
+                                num_splits: int = 0, workspace=None, lam_out=None, out=None, stream=None,
+                                host_seqlens=None):
+    """diffattn_lambda and diffattn_fwd_kvcache in one call (the key-split kernel
+    runs while the lambda kernel finishes; the combine kernel reads lambda).
+    lambda_q1 .. lambda_k2: fp32 [d] (shared lambda) or [H, d] (per head).
+    Returns (out, lam)."""
+    import torch
+    lib = load_library()
+    vecs = (lambda_q1, lambda_k1, lambda_q2, lambda_k2)
+    for t, name in zip(vecs, ("lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2")):
+        _check_cuda(t, name)
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape != lambda_q1.shape:
+            raise ValueError(f"{name} must be contiguous fp32 of the shape of lambda_q1")
+    for t, name in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (subln_w, "subln_w")):
+        _check_cuda(t, name)
+    if cache_seqlens is not None:
+        _check_cuda(cache_seqlens, "cache_seqlens")
+        if cache_seqlens.dtype != torch.int32 or cache_seqlens.numel() != q.shape[0]:
+            raise ValueError("cache_seqlens must be int32 [batch]")
+    H = q.shape[2]
+    per_head = lambda_q1.dim() == 2 and lambda_q1.shape[0] == H and H > 1
+    if lam_out is None:
+        lam_out = torch.empty(H if per_head else 1, dtype=torch.float32, device=q.device)
+    _check_cuda(lam_out, "lam_out")
+    desc = kv_desc(q, k_cache, v_cache, eps, num_splits, host_seqlens)
+    need = int(lib.diffattn_fwd_kvcache_workspace_size(ctypes.byref(desc)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda(workspace, "workspace")
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v_cache.shape[-1],), dtype=q.dtype, device=q.device)
+    _check_cuda(out, "out")
+    st = lib.diffattn_fwd_kvcache_lambda(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(cache_seqlens) if cache_seqlens is not None else None,
+                                         *(_ptr(t) for t in vecs), 1 if per_head else 0, int(lambda_q1.shape[-1]),
+                                         float(lambda_init), _ptr(lam_out), _ptr(subln_w), 1 if causal else 0,
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+                                         _stream_handle(stream))
+    if st != OK:
+        raise DiffAttnError(st, "diffattn_fwd_kvcache_lambda")
+    return out, lam_out
 
 
 def diffattn_fwd_kvcache_noalloc(q, k_cache, v_cache, lam, lambda_init: float, subln_w, cache_seqlens=None,

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "lambda_warp.cuh"
 #include "sm103a_ptx.cuh"
 
 namespace diffattn {
@@ -43,13 +44,22 @@ diffattn_decode_combine_kernel(const KvParams p) {
     // The inputs of the call (lengths, weight, lambda) are read before the wait for
     // the split kernel: this grid is placed only once every split CTA has passed its
     // own wait for the kernels before it (the lambda kernel among them), so they are
-    // complete; only the partials come from the split kernel.
+    // complete; only the partials come from the split kernel. In a combined call each
+    // row's warp forms its head's lambda from the parameter vectors, and the warps of
+    // the first query's rows write it out.
     int L = 0;
     float lam = 0.f;
     float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.lq1 != nullptr) {  // warp-uniform; rows past the end form a valid set's lambda too
+        const int set = p.lambda_stride ? h : 0;
+        const size_t base = (size_t)set * p.lambda_d;
+        lam = lambda_value_warp(p.lq1 + base, p.lk1 + base, p.lq2 + base, p.lk2 + base, p.lambda_d, p.lambda_init,
+                                lane);
+        if (lane == 0 && row == set) p.lambda_out[set] = lam;  // row (b = 0, t = 0, h = set)
+    }
     if (row_ok) {  // from L2 (ld.global.cg): no line an earlier grid left in this SM's L1
         L = p.cache_seqlens ? __ldcg(p.cache_seqlens + b) : p.capacity;
-        lam = __ldcg(p.lambda + h * p.lambda_stride);
+        if (p.lq1 == nullptr) lam = __ldcg(p.lambda + h * p.lambda_stride);
         w = __ldcg(reinterpret_cast<const float4*>(p.subln_w) + lane);
     }
     griddep_wait();  // a programmatic dependent of the split kernel: its partials are complete

@@ -499,12 +499,16 @@ unsigned long long diffattn_fwd_kvcache_workspace_size(const diffattn_kv_desc* d
     return kv_workspace_bytes(*desc, n);
 }
 
-diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
-                                     const void* v_cache, const int* cache_seqlens, const float* lambda,
-                                     int lambda_per_head, float lambda_init, const float* subln_w, int causal,
-                                     void* workspace, unsigned long long workspace_bytes, void* out,
-                                     void* stream) {
-    const CallRange nvtx_range("diffattn_fwd_kvcache");
+}  // extern "C"
+
+namespace {
+// Shared body of diffattn_fwd_kvcache and diffattn_fwd_kvcache_lambda (which
+// passes the lambda parameter vectors: the combine kernel forms lambda from them
+// and writes it to `lambda`).
+diffattn_status kv_common(const diffattn_kv_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                          const int* cache_seqlens, const float* lambda, int lambda_per_head, float lambda_init,
+                          const float* subln_w, int causal, void* workspace, unsigned long long workspace_bytes,
+                          void* out, void* stream, const LambdaCall* lam_call) {
     if (!desc) return DIFFATTN_ERR_INVALID_ARG;
     const diffattn_kv_desc& ds = *desc;
     int n_splits = 0, chunk = 0;
@@ -551,7 +555,43 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
     if (!encode_bf16_rows(&maps.k, k_cache, (uint64_t)ds.num_kv_heads * 2 * ds.d, cache_rows, 64) ||
         !encode_bf16_rows(&maps.v, v_cache, (uint64_t)ds.num_kv_heads * ds.dv, cache_rows, 64))
         return DIFFATTN_ERR_CUDA;
+    if (lam_call) {  // the combine kernel forms lambda itself
+        p.lq1 = lam_call->lq1;
+        p.lk1 = lam_call->lk1;
+        p.lq2 = lam_call->lq2;
+        p.lk2 = lam_call->lk2;
+        p.lambda_d = lam_call->d;
+        p.lambda_out = const_cast<float*>(lambda);
+    }
     return launch_decode(p, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                     const void* v_cache, const int* cache_seqlens, const float* lambda,
+                                     int lambda_per_head, float lambda_init, const float* subln_w, int causal,
+                                     void* workspace, unsigned long long workspace_bytes, void* out,
+                                     void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_kvcache");
+    return kv_common(desc, q, k_cache, v_cache, cache_seqlens, lambda, lambda_per_head, lambda_init, subln_w, causal,
+                     workspace, workspace_bytes, out, stream, nullptr);
+}
+
+diffattn_status diffattn_fwd_kvcache_lambda(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                            const void* v_cache, const int* cache_seqlens, const float* lq1,
+                                            const float* lk1, const float* lq2, const float* lk2,
+                                            int lambda_per_head, int lambda_d, float lambda_init, float* lambda_out,
+                                            const float* subln_w, int causal, void* workspace,
+                                            unsigned long long workspace_bytes, void* out, void* stream) {
+    const CallRange nvtx_range("diffattn_fwd_kvcache_lambda");
+    if (!desc || !lq1 || !lk1 || !lq2 || !lk2 || !lambda_out) return DIFFATTN_ERR_INVALID_ARG;
+    if (lambda_d < 1 || lambda_d > 1024 || (reinterpret_cast<uintptr_t>(lambda_out) & 3u)) return DIFFATTN_ERR_INVALID_ARG;
+    const LambdaCall lc{lq1, lk1, lq2, lk2, lambda_per_head ? desc->num_heads : 1, lambda_d};
+    if (lc.n_sets < 1) return DIFFATTN_ERR_INVALID_ARG;
+    return kv_common(desc, q, k_cache, v_cache, cache_seqlens, lambda_out, lambda_per_head, lambda_init, subln_w,
+                     causal, workspace, workspace_bytes, out, stream, &lc);
 }
 
 }  // extern "C"

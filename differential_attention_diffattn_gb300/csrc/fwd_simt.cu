@@ -5,6 +5,7 @@
 // sqrtf as compiled without fast-math) because its acceptance bound is 1e-5
 // max-abs, below what tf32 tensor cores reach.
 #include "internal.h"
+#include "lambda_warp.cuh"
 #include "sm103a_ptx.cuh"
 
 namespace diffattn {
@@ -34,14 +35,8 @@ __global__ void diffattn_lambda_kernel(const float* __restrict__ lq1, const floa
     const int lane = threadIdx.x & 31;
     if (set >= n_sets) return;
     const size_t base = (size_t)set * d;
-    float a = 0.f, b = 0.f;
-    for (int e = lane; e < d; e += 32) {
-        a = fmaf(lq1[base + e], lk1[base + e], a);
-        b = fmaf(lq2[base + e], lk2[base + e], b);
-    }
-    a = warp_sum(a);
-    b = warp_sum(b);
-    if (lane == 0) out[set] = expf(a) - expf(b) + lambda_init;
+    const float lam = lambda_value_warp(lq1 + base, lk1 + base, lq2 + base, lk2 + base, d, lambda_init, lane);
+    if (lane == 0) out[set] = lam;
 }
 
 constexpr int ROWS_PER_BLOCK = 4;  // one warp per (query row, head)

@@ -80,6 +80,11 @@ struct KvParams {
     float eps;
     float scale;               // d^-0.5
     unsigned long long timeout_ns;
+    // set: the combine kernel forms lambda from these [sets][lambda_d] vectors
+    // (lambda unused) and writes it to lambda_out
+    const float *lq1, *lk1, *lq2, *lk2;
+    int lambda_d;
+    float* lambda_out;
 };
 
 // TMA descriptors of the caches: [batch * capacity][Hkv * 2d] and

@@ -304,6 +304,30 @@ diffattn_status diffattn_fwd_kvcache(const diffattn_kv_desc* desc, const void* q
                                      void* out, void* stream);
 
 /*
+ * The lambda reparameterisation and the cache forward in one call: the results
+ * of diffattn_lambda into lambda_out and of diffattn_fwd_kvcache reading it, bit
+ * for bit, from two launches instead of three. Only the combine kernel uses
+ * lambda, so it forms lambda itself (each row's warp for its head, with the
+ * lambda kernel's arithmetic) and the warps of the first query of the first
+ * sequence write lambda_out.
+ *  lq1, lk1, lq2, lk2: device fp32 [n_sets][lambda_d], n_sets = H when
+ *  lambda_per_head, else 1.
+ *  lambda_out: device fp32 [n_sets], written by this call (4-byte aligned).
+ *  Every other argument as in diffattn_fwd_kvcache; the inputs must be
+ *  complete when the call is made on the stream, as for any stream-ordered call.
+ * Errors: those of diffattn_lambda (null vectors, lambda_d outside 1..1024)
+ *  and of diffattn_fwd_kvcache, all checked before anything is launched. An
+ *  empty batch launches nothing (lambda_out is not written).
+ */
+diffattn_status diffattn_fwd_kvcache_lambda(const diffattn_kv_desc* desc, const void* q, const void* k_cache,
+                                            const void* v_cache, const int* cache_seqlens, const float* lq1,
+                                            const float* lk1, const float* lq2, const float* lk2,
+                                            int lambda_per_head, int lambda_d, float lambda_init,
+                                            float* lambda_out, const float* subln_w, int causal,
+                                            void* workspace, unsigned long long workspace_bytes, void* out,
+                                            void* stream);
+
+/*
  * Size of the scratch array behind diffattn_fwd_kvcache_noalloc: 16 MiB of
  * device memory per GPU that loads the library, held until the process exits.
  */

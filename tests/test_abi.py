@@ -256,6 +256,30 @@ def test_fwd_lambda_rejects_on_host(lib):
     assert call(batch=0) == 0                       # empty: nothing launched
 
 
+def test_kvcache_lambda_rejects_on_host(lib):
+    """The combined lambda + cache forward call checks all its arguments before it
+    launches anything (no GPU here: a launch would fail with ERR_CUDA)."""
+    vp = ctypes.c_void_p
+
+    def call(vecs=(FAKE, FAKE, FAKE, FAKE), lam_d=64, lam_out=FAKE, ws_bytes=1 << 30, **desc_kw):
+        base = dict(batch=4, q_len=1, cache_capacity=4096, num_heads=16, num_kv_heads=4, d=64, dv=128,
+                    dtype=_lib.DTYPE_BF16, eps=1e-5, num_splits=0)
+        base.update(desc_kw)
+        d = _lib.DiffAttnKvDesc(**base)
+        return lib.diffattn_fwd_kvcache_lambda(ctypes.byref(d), vp(FAKE), vp(FAKE), vp(FAKE), None,
+                                               *(vp(x) for x in vecs), 0, lam_d, 0.2, vp(lam_out), vp(FAKE), 1,
+                                               vp(FAKE), ws_bytes, vp(FAKE), None)
+    assert call(vecs=(FAKE, FAKE, 0, FAKE)) == 1   # a null lambda vector
+    assert call(lam_d=0) == 1
+    assert call(lam_d=2000) == 1
+    assert call(lam_out=0) == 1
+    assert call(lam_out=FAKE + 2) == 1              # misaligned lambda output
+    assert call(num_heads=15) == 1                  # the cache forward's own checks come first too
+    assert call(ws_bytes=16) == 1                   # workspace too small
+    assert call(d=32, dv=64) == 2                   # no kernel for d = 32
+    assert call(batch=0) == 0                       # empty: nothing launched
+
+
 def test_fused_rope_forward_rejects_on_host(lib):
     vp = ctypes.c_void_p
 

@@ -155,3 +155,33 @@ def test_host_lengths_are_only_a_plan_hint(hint):
                                 host_seqlens=wrong)
     assert da.diffattn_get_device_status() == 0
     compare(y, oracle_kv(inp), "bf16")
+
+
+# diffattn_fwd_kvcache_lambda against diffattn_lambda + diffattn_fwd_kvcache: the
+# same bits for lambda and for the output (shared and per-head lambda, a forced
+# split count and the library's plan, both cache workloads' shapes).
+@pytest.mark.parametrize("case", ["shared", "per_head", "splits3", "decode_b8_c16384", "decode_b16_q4_ragged"])
+def test_kvcache_lambda_equals_two_calls_bitwise(case):
+    if case in W.KV_WORKLOADS:
+        inp = W.generate_kv(W.KV_WORKLOADS[case], seed=61)
+        splits = 0
+    else:
+        wl = kvw(q_len=2, lambda_per_head=case == "per_head", random_subln=True)
+        inp = W.generate_kv(wl, seed=60, lengths=[1000, 517, 2])
+        splits = 3 if case == "splits3" else 0
+    wl = inp.wl
+    dev = "cuda"
+    li = da.diffattn_lambda_init(wl.depth)
+    vecs = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
+    args = (inp.q.to(dev), inp.k_cache.to(dev), inp.v_cache.to(dev))
+    lens = inp.cache_seqlens.to(dev)
+    w = inp.subln_w.to(dev)
+    lam = da.diffattn_lambda(*vecs, li)
+    two = da.diffattn_fwd_kvcache(*args, lam, li, w, cache_seqlens=lens, causal=wl.causal, eps=wl.eps,
+                                  num_splits=splits)
+    for _ in range(2):  # twice, the second time over the first call's outputs
+        one, lam1 = da.diffattn_fwd_kvcache_lambda(*args, *vecs, li, w, cache_seqlens=lens, causal=wl.causal,
+                                                   eps=wl.eps, num_splits=splits)
+        assert da.diffattn_get_device_status() == 0
+        assert torch.equal(lam1, lam)
+        assert torch.equal(one, two)
