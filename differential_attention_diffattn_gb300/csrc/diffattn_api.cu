@@ -84,6 +84,20 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t row_elems, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over a [rows][row_elems] row-major tensor; box = 32 elements (128 bytes,
+// 128-byte swizzle) x 128 rows.
+bool encode_f32_rows(CUtensorMap* map, const void* base, uint64_t row_elems, uint64_t rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {row_elems, rows};
+    const cuuint64_t strides[1] = {row_elems * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 map over [rows][16] (32-byte rows): boxes of 16 x 64 rows with the
 // 32-byte swizzle, as K-major MMA operands of one 16-wide K step.
 bool encode_bf16_aug(CUtensorMap* map, const void* base, uint64_t rows) {
@@ -424,6 +438,14 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         !encode_bf16_rows(&maps.v, v, (uint64_t)ds.num_kv_heads * ds.dv, (uint64_t)p.total_tokens) ||
         !encode_bf16_rows(&maps.out, out, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
         return DIFFATTN_ERR_CUDA;
+    if (train) {
+        if (!encode_f32_rows(&maps.o1, o1, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens) ||
+            !encode_f32_rows(&maps.o2, o2, (uint64_t)ds.num_heads * ds.dv, (uint64_t)p.total_tokens))
+            return DIFFATTN_ERR_CUDA;
+    } else {
+        maps.o1 = maps.out;  // not read without training outputs
+        maps.o2 = maps.out;
+    }
     if (lam_call) {
         if (launch_lambda_first() != cudaSuccess) return DIFFATTN_ERR_CUDA;
         p.lambda_pending = 1;  // the forward's reads of lambda alone wait for that kernel

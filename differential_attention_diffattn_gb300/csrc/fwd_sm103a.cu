@@ -60,6 +60,12 @@ constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_STAGE0 = Q_BYTES;
 constexpr uint32_t OFF_MISC = OFF_STAGE0 + STAGES * STAGE_BYTES;
+// Epilogue staging in the K / V stages (every load consumed by then): the bf16 output
+// in the first 32 KB, the training outputs O1 / l1 and O2 / l2 (fp32) after it, each as
+// four [128 rows x 32] boxes of 16 KB with the 128-byte swizzle.
+constexpr uint32_t O_BOX = BM * 32 * 4;
+constexpr uint32_t OFF_OSTAGE = OFF_STAGE0 + 2 * BOX_BYTES;
+static_assert(OFF_OSTAGE + 8 * O_BOX <= OFF_MISC, "training-output staging fits the stages");
 constexpr uint32_t MISC_BYTES = 1024;
 constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 232448, "exceeds the per-block shared memory limit");
@@ -98,10 +104,13 @@ __device__ __forceinline__ uint64_t desc_value(uint32_t saddr) { return smem_des
 // True on every lane iff `pred` holds on every lane of the warp.
 __device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffffffu, pred); }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
-                                const FwdParams p) {
+// The kernel body; TRAIN: the training form (O1 / l1 and O2 / l2 of full tiles staged in
+// shared memory for bulk tensor stores), a kernel of its own so that the inference form
+// keeps its register allocation.
+template <bool TRAIN>
+__device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                              const CUtensorMap& tm_out, const CUtensorMap& tm_o1,
+                                              const CUtensorMap& tm_o2, const FwdParams& p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc& ms = *reinterpret_cast<Misc*>(smem + OFF_MISC);
@@ -441,6 +450,8 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
         ok = warp_all(ok && mbar_wait(bar_o_full, 0, ab));
         ok = warp_all(ok && mbar_wait(bar_w_full, 0, ab));
         const bool store = qi < len;
+        // training outputs of a tile wholly inside its sequence: staged for bulk tensor stores
+        const bool stage_o = TRAIN && qt * BM + BM <= len;
         float D[64];
         float ssp = 0.f;
         if (ok) {
@@ -462,7 +473,21 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 }
                 // Training outputs: the normalised attention output of each component,
                 // kept in fp32 (the lambda gradient sums many cancelling terms of them).
-                if (store && p.o1 != nullptr) {
+                if (stage_o && p.o1 != nullptr) {
+                    // box 2c + ch of each: row r at r * 128 bytes, 16-byte chunk i at (i ^ (r % 8))
+                    uint8_t* row1 = smem + OFF_OSTAGE + (uint32_t)(2 * c + ch) * O_BOX + (uint32_t)r * 128u;
+                    uint8_t* row2 = row1 + 4 * O_BOX;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t off = (uint32_t)((i ^ (r & 7)) << 4);
+                        *reinterpret_cast<float4*>(row1 + off) =
+                            make_float4(__uint_as_float(o1[4 * i]) * il1, __uint_as_float(o1[4 * i + 1]) * il1,
+                                        __uint_as_float(o1[4 * i + 2]) * il1, __uint_as_float(o1[4 * i + 3]) * il1);
+                        *reinterpret_cast<float4*>(row2 + off) =
+                            make_float4(__uint_as_float(o2[4 * i]) * il2, __uint_as_float(o2[4 * i + 1]) * il2,
+                                        __uint_as_float(o2[4 * i + 2]) * il2, __uint_as_float(o2[4 * i + 3]) * il2);
+                    }
+                } else if (store && p.o1 != nullptr) {
                     const size_t base = ((size_t)(start + qi) * p.H + h) * DV / 4 + c * 16 + ch * 8;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -514,6 +539,14 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
                 const uint32_t src = sbase + OFF_STAGE0;
                 tma_store_2d(&tm_out, src, h * DV, start + qt * BM);
                 tma_store_2d(&tm_out, src + BOX_BYTES, h * DV + 64, start + qt * BM);
+                if (TRAIN && p.o1 != nullptr) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        tma_store_2d(&tm_o1, sbase + OFF_OSTAGE + (uint32_t)b * O_BOX, h * DV + 32 * b, start + qt * BM);
+                        tma_store_2d(&tm_o2, sbase + OFF_OSTAGE + (uint32_t)(4 + b) * O_BOX, h * DV + 32 * b,
+                                     start + qt * BM);
+                    }
+                }
                 bulk_commit_group();
                 bulk_wait_group_read0();  // shared memory stays until the copy has read it
             }
@@ -529,6 +562,23 @@ diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const 
     }
 }
 
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                                const FwdParams p) {
+    fwd_bf16_body<false>(tm_q, tm_k, tm_v, tm_out, tm_out, tm_out, p);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_bf16_sm103a_train_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                      const __grid_constant__ CUtensorMap tm_k,
+                                      const __grid_constant__ CUtensorMap tm_v,
+                                      const __grid_constant__ CUtensorMap tm_out,
+                                      const __grid_constant__ CUtensorMap tm_o1,
+                                      const __grid_constant__ CUtensorMap tm_o2, const FwdParams p) {
+    fwd_bf16_body<true>(tm_q, tm_k, tm_v, tm_out, tm_o1, tm_o2, p);
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps, cudaStream_t stream) {
@@ -539,6 +589,9 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
     if (dev < 64 && !attr_done[dev]) {
         err = cudaFuncSetAttribute(diffattn_fwd_bf16_sm103a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(diffattn_fwd_bf16_sm103a_train_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (err != cudaSuccess) return err;
         attr_done[dev] = true;
     }
@@ -554,6 +607,9 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.o1 != nullptr)
+        return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_train_kernel, maps.q, maps.k, maps.v, maps.out,
+                                  maps.o1, maps.o2, p);
     return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_kernel, maps.q, maps.k, maps.v, maps.out, p);
 }
 

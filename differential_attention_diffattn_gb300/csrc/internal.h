@@ -56,6 +56,7 @@ struct FwdParams {
 // TMA descriptors of the bf16 operands, built on the host per call.
 struct FwdTensorMaps {
     CUtensorMap q, k, v, out;  // out: [tokens][H * dv] bf16, 64 x 128 boxes (bulk tensor stores)
+    CUtensorMap o1, o2;        // training outputs: [tokens][H * dv] fp32, 32 x 128 boxes (bulk tensor stores)
 };
 
 // One forward against a key/value cache (decode / short query blocks).
