@@ -38,8 +38,12 @@ def grad_close(got, want, name):
     assert rel <= TOL_REL_L1 and mx <= TOL_MAX_REL, (name, rel, mx)
 
 
-def run_case(wl, lens, seed):
+def run_case(wl, lens, seed, one_lambda_set=False):
     inp = W.generate(wl, seed=seed, seq_lens=lens)
+    if one_lambda_set:  # per-head layout, every head given head 0's vectors
+        for n in ("lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2"):
+            t = getattr(inp, n)
+            setattr(inp, n, t[:1].expand_as(t).contiguous())
     dev = "cuda"
     li = da.diffattn_lambda_init(wl.depth)
     lv = [x.to(dev) for x in (inp.lambda_q1, inp.lambda_k1, inp.lambda_q2, inp.lambda_k2)]
@@ -129,6 +133,27 @@ def test_backward_matches_oracle(lens, H, Hkv, causal, per_head):
     want = ob.gradients(inp.cu_seqlens.tolist(), inp.q.double(), inp.k.double(), inp.v.double(),
                         inp.lambda_q1.double(), inp.lambda_k1.double(), inp.lambda_q2.double(),
                         inp.lambda_k2.double(), inp.subln_w.double(), li, wl.eps, causal, dy.double())
+    grad_close(dq, want["q"], "dq")
+    grad_close(dk, want["k"], "dk")
+    grad_close(dv, want["v"], "dv")
+    grad_close(dw, want["w"], "dw")
+    for got, name in zip(dl, ("lq1", "lk1", "lq2", "lk2")):
+        grad_close(got, want[name], name)
+
+
+# More heads than the preprocessing kernel sums per head in shared memory (1024): the
+# per-head lambda gradients accumulate in global memory instead. Every head gets the same
+# lambda vectors (random ones per head would, over a thousand heads, include heads whose
+# two maps nearly cancel, where the bf16 bound of the forward itself does not hold).
+def test_backward_many_heads_per_head_lambda():
+    wl = W.with_overrides(BF, num_heads=1030, num_kv_heads=1030, causal=True, lambda_per_head=True,
+                          random_subln=True)
+    lens = [200, 7]
+    inp, dy, out, lse, o1, o2, dq, dk, dv, dlam, dw, dl = run_case(wl, lens, 97, one_lambda_set=True)
+    li = orc.lambda_init(wl.depth)
+    want = ob.gradients(inp.cu_seqlens.tolist(), inp.q.double(), inp.k.double(), inp.v.double(),
+                        inp.lambda_q1.double(), inp.lambda_k1.double(), inp.lambda_q2.double(),
+                        inp.lambda_k2.double(), inp.subln_w.double(), li, wl.eps, True, dy.double())
     grad_close(dq, want["q"], "dq")
     grad_close(dk, want["k"], "dk")
     grad_close(dv, want["v"], "dv")
