@@ -446,16 +446,27 @@ diffattn_status fwd_common(const diffattn_desc* desc, const void* q, const void*
         maps.o1 = maps.out;  // not read without training outputs
         maps.o2 = maps.out;
     }
-    if (lam_call) {
-        if (launch_lambda_first() != cudaSuccess) return DIFFATTN_ERR_CUDA;
-        p.lambda_pending = 1;  // the forward's reads of lambda alone wait for that kernel
-    }
     // The rotary embedding of q is applied by the one-item-per-CTA kernel only: it
     // stages each tile's cos / sin rows in its last K/V stage, which the persistent
     // kernel does not have (its shared memory is all in use).
-    const cudaError_t err = (rope == nullptr && fwd_use_persistent(cu_seqlens != nullptr, p.max_seqlen, p.H, p.num_seqs))
-                                ? launch_fwd_bf16_persistent(p, maps, st)
-                                : launch_fwd_bf16_sm103a(p, maps, st);
+    const bool persistent = rope == nullptr && fwd_use_persistent(cu_seqlens != nullptr, p.max_seqlen, p.H, p.num_seqs);
+    // A combined call whose one-item-per-CTA grid fits one wave forms lambda in that
+    // kernel (one launch: the step is a latency chain, 2 x 512 tokens 19.0 -> 16.9 us a
+    // flushed step); longer grids launch the lambda kernel first, which runs under the
+    // forward's start (in-kernel there measured 0.3 % slower at 16384 tokens).
+    const long long grid_ctas = (long long)((p.max_seqlen + 127) / 128) * p.H * p.num_seqs;
+    if (lam_call && (persistent || grid_ctas > sm_count())) {
+        if (launch_lambda_first() != cudaSuccess) return DIFFATTN_ERR_CUDA;
+        p.lambda_pending = 1;  // the forward's reads of lambda alone wait for that kernel
+    } else if (lam_call) {
+        p.lq1 = lam_call->lq1;
+        p.lk1 = lam_call->lk1;
+        p.lq2 = lam_call->lq2;
+        p.lk2 = lam_call->lk2;
+        p.lambda_d = lam_call->d;
+        p.lambda_out = const_cast<float*>(lambda);
+    }
+    const cudaError_t err = persistent ? launch_fwd_bf16_persistent(p, maps, st) : launch_fwd_bf16_sm103a(p, maps, st);
     return err == cudaSuccess ? DIFFATTN_OK : DIFFATTN_ERR_CUDA;
 }
 }  // namespace

@@ -39,6 +39,7 @@
 
 #include "internal.h"
 #include "rope_q.cuh"
+#include "lambda_warp.cuh"
 #include "sm103a_ptx.cuh"
 
 namespace diffattn {
@@ -105,9 +106,10 @@ __device__ __forceinline__ uint64_t desc_value(uint32_t saddr) { return smem_des
 __device__ __forceinline__ bool warp_all(bool pred) { return __all_sync(0xffffffffu, pred); }
 
 // The kernel body; TRAIN: the training form (O1 / l1 and O2 / l2 of full tiles staged in
-// shared memory for bulk tensor stores), a kernel of its own so that the inference form
-// keeps its register allocation.
-template <bool TRAIN>
+// shared memory for bulk tensor stores); LAMBDA: lambda formed from its parameter vectors
+// by the producer warp once its copies have landed (only the epilogue reads it). Each
+// form is a kernel of its own, so that the plain inference form keeps its code.
+template <bool TRAIN, bool LAMBDA>
 __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                               const CUtensorMap& tm_out, const CUtensorMap& tm_o1,
                                               const CUtensorMap& tm_o2, const FwdParams& p) {
@@ -215,7 +217,7 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
                 mbar_init(bar_p_ready(c), 128);
             }
             mbar_init(bar_o_full, 1);
-            mbar_init(bar_w_full, 32);  // one cp.async arrive per lane of this warp
+            mbar_init(bar_w_full, LAMBDA ? 33 : 32);  // one cp.async arrive per lane, and lambda's
             mbar_init(bar_q_rot, 256);  // every softmax thread, after rotating its part of Q
             mbar_init(bar_tab_full, 1);
             ms.abort_flag = 0;
@@ -240,7 +242,7 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
         __syncwarp();  // the barriers exist before any lane arrives on them
         if (p.lambda_pending) griddep_wait();  // lambda comes from the preceding grid
         for (int i = lane; i < DV; i += 32) cp_async4(smem_u32(&ms.w[i]), p.subln_w + i);
-        if (lane == 0) cp_async4(smem_u32(&ms.lam), p.lambda + h * p.lambda_stride);
+        if (lane == 0 && !LAMBDA) cp_async4(smem_u32(&ms.lam), p.lambda + h * p.lambda_stride);
         cp_async_arrive_noinc(bar_w_full);
     }
     if (warp == MMA_WARP) tmem_alloc(smem_u32(&ms.tmem_base), TMEM_COLS);
@@ -273,6 +275,18 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
         }
         cp_async_wait_all();  // the weight copies have landed, whatever the epilogue did
         __syncwarp();
+        if (LAMBDA) {
+            // the CTAs of the first query tile write lambda out (all of them, for a shared one)
+            const int set = p.lambda_stride ? h : 0;
+            const size_t base = (size_t)set * p.lambda_d;
+            const float lam = lambda_value_warp(p.lq1 + base, p.lk1 + base, p.lq2 + base, p.lk2 + base, p.lambda_d,
+                                                p.lambda_init, lane);
+            if (lane == 0) {
+                ms.lam = lam;
+                if (qt == 0) atomicExch(p.lambda_out + set, lam);
+                mbar_arrive(bar_w_full);  // releases the store above to the epilogue's wait
+            }
+        }
     } else if (warp == MMA_WARP) {
         // ==================================================== MMA issuer ===
         // The whole warp walks the loop with warp-uniform values; one elected
@@ -566,7 +580,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 diffattn_fwd_bf16_sm103a_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
                                 const FwdParams p) {
-    fwd_bf16_body<false>(tm_q, tm_k, tm_v, tm_out, tm_out, tm_out, p);
+    fwd_bf16_body<false, false>(tm_q, tm_k, tm_v, tm_out, tm_out, tm_out, p);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+diffattn_fwd_bf16_sm103a_lambda_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                       const __grid_constant__ CUtensorMap tm_k,
+                                       const __grid_constant__ CUtensorMap tm_v,
+                                       const __grid_constant__ CUtensorMap tm_out, const FwdParams p) {
+    fwd_bf16_body<false, true>(tm_q, tm_k, tm_v, tm_out, tm_out, tm_out, p);
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -576,7 +598,7 @@ diffattn_fwd_bf16_sm103a_train_kernel(const __grid_constant__ CUtensorMap tm_q,
                                       const __grid_constant__ CUtensorMap tm_out,
                                       const __grid_constant__ CUtensorMap tm_o1,
                                       const __grid_constant__ CUtensorMap tm_o2, const FwdParams p) {
-    fwd_bf16_body<true>(tm_q, tm_k, tm_v, tm_out, tm_o1, tm_o2, p);
+    fwd_bf16_body<true, false>(tm_q, tm_k, tm_v, tm_out, tm_o1, tm_o2, p);
 }
 
 }  // namespace
@@ -591,6 +613,9 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
                                    (int)SMEM_BYTES);
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(diffattn_fwd_bf16_sm103a_train_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(diffattn_fwd_bf16_sm103a_lambda_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (err != cudaSuccess) return err;
         attr_done[dev] = true;
@@ -610,6 +635,8 @@ cudaError_t launch_fwd_bf16_sm103a(const FwdParams& p, const FwdTensorMaps& maps
     if (p.o1 != nullptr)
         return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_train_kernel, maps.q, maps.k, maps.v, maps.out,
                                   maps.o1, maps.o2, p);
+    if (p.lq1 != nullptr)
+        return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_lambda_kernel, maps.q, maps.k, maps.v, maps.out, p);
     return cudaLaunchKernelEx(&cfg, diffattn_fwd_bf16_sm103a_kernel, maps.q, maps.k, maps.v, maps.out, p);
 }
 

@@ -51,6 +51,11 @@ struct FwdParams {
     float* lse;               // training outputs (all null, or all set; bf16 kernel only):
     void* o1;                 //   lse [tokens][H][2] fp32 (log2 domain of the scaled scores),
     void* o2;                 //   o1, o2 [tokens][H][dv] fp32 = O_c / l_c
+    // set (one-item-per-CTA bf16 kernel): lambda is formed in the kernel from these
+    // [sets][lambda_d] vectors (the `lambda` read is skipped) and written to lambda_out
+    const float *lq1, *lk1, *lq2, *lk2;
+    int lambda_d;
+    float* lambda_out;
 };
 
 // TMA descriptors of the bf16 operands, built on the host per call.

@@ -228,15 +228,20 @@ def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv):
 # wait for it) against the two calls, on each forward kernel: the one-item-per-CTA
 # bf16 kernel, the persistent one (dense and packed), the fp32 one; lambdas shared
 # and per head.
-@pytest.mark.parametrize("case", ["tile", "persistent", "packed", "per_head", "f32"])
+# "tile" and "tile_per_head" fit one wave of CTAs, where the one-item-per-CTA kernel
+# forms lambda itself; "tile_waves" (288 CTAs) launches the lambda kernel first.
+@pytest.mark.parametrize("case", ["tile", "tile_per_head", "tile_waves", "persistent", "packed", "per_head", "f32"])
 def test_fwd_lambda_equals_two_calls_bitwise(case):
     if case == "f32":
         wl, lens = W.WORKLOADS["tiny_f32"], [64]
     elif case == "per_head":
         wl, lens = W.with_overrides(BF, lambda_per_head=True, random_subln=True), [1000, 1000, 1000]
+    elif case == "tile_per_head":
+        wl, lens = W.with_overrides(BF, num_heads=16, num_kv_heads=4, lambda_per_head=True, random_subln=True), [700]
     else:
         wl = W.with_overrides(BF, num_heads=16, num_kv_heads=4)
-        lens = {"tile": [700], "persistent": [1000, 1000, 1000], "packed": [1000, 40, 2500, 300]}[case]
+        lens = {"tile": [700], "tile_waves": [2300], "persistent": [1000, 1000, 1000],
+                "packed": [1000, 40, 2500, 300]}[case]
     inp = W.generate(wl, seed=41, seq_lens=lens)
     t = {n: getattr(inp, n).cuda() for n in ("q", "k", "v", "lambda_q1", "lambda_k1", "lambda_q2", "lambda_k2",
                                              "subln_w", "cu_seqlens")}
@@ -248,7 +253,8 @@ def test_fwd_lambda_equals_two_calls_bitwise(case):
     kw = dict(cu_seqlens=t["cu_seqlens"], max_seqlen=max(lens)) if packed else {}
     kern = da.diffattn_fwd_kernel(sh(t["q"]), sh(t["k"]), sh(t["v"]), torch.ones(1, device="cuda"), t["subln_w"],
                                   **kw)
-    want_kernel = {"tile": "diffattn_fwd_bf16_sm103a_kernel", "persistent": "diffattn_fwd_bf16_persistent_kernel",
+    want_kernel = {"tile": "diffattn_fwd_bf16_sm103a_kernel", "tile_per_head": "diffattn_fwd_bf16_sm103a_kernel",
+                   "tile_waves": "diffattn_fwd_bf16_sm103a_kernel", "persistent": "diffattn_fwd_bf16_persistent_kernel",
                    "packed": "diffattn_fwd_bf16_persistent_kernel", "per_head": "diffattn_fwd_bf16_persistent_kernel",
                    "f32": "diffattn_fwd_f32_kernel"}[case]
     assert kern == want_kernel
