@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libdiffattn.so")
 INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 SOURCES = ["diffattn_api.cu", "fwd_simt.cu", "fwd_sm103a.cu", "fwd_persistent_sm103a.cu", "decode_simt.cu",
            "decode_sm103a.cu", "bwd_simt.cu", "bwd_sm103a.cu", "rope_simt.cu", "merge_simt.cu", "gemm_sm103a.cu"]
-HEADERS = ["internal.h", "sm103a_ptx.cuh", "rope_q.cuh", "lambda_warp.cuh"]
+HEADERS = ["internal.h", "sm103a_ptx.cuh", "rope_q.cuh", "lambda_warp.cuh", "softmax_exact.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -55,6 +55,7 @@
 
 #include "internal.h"
 #include "sm103a_ptx.cuh"
+#include "softmax_exact.cuh"
 
 namespace diffattn {
 namespace {
@@ -85,6 +86,9 @@ constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ uint32_t col_s(int c) { return (uint32_t)c * 128u; }
 __device__ __forceinline__ uint32_t col_o(int c) { return 256u + (uint32_t)c * 128u; }
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// Past an item's first tile, the row sum of a tile above which the warp takes it
+// maximum-first (the steps of the one-item-per-CTA kernel).
+constexpr float EXACT_SUM = 4294967296.0f;  // 2^32
 constexpr int MAX_PACKED_SEQS = 64;
 
 // One work item: 128 query rows of one diff head of one sequence (n_kv < 0: no
@@ -222,6 +226,9 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                 break;
             }
             const int qi = it.qt * BM + r;
+            // the softmax steps of the one-item-per-CTA kernel: the item's first tile
+            // maximum-first, later ones exponentiated with that reference at once, the
+            // rare tile whose row sum passes 2^32 taken again maximum-first (softmax_exact.cuh)
             float m = -INFINITY, l = 0.f;
             for (int j = 0; ok && j < it.n_kv; ++j, ++tile) {
                 if (!(ok = warp_all(mbar_wait(bar_s_full(c), (uint32_t)tile & 1u, ab)))) break;
@@ -237,27 +244,33 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
 #pragma unroll
                     for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e >> 6][e & 63]);
                 }
-                const int kbase = j * BN;
-                if ((p.causal && j == it.qt) || kbase + BN > it.len) {
-                    int lim = p.causal ? min(qi + 1, it.len) : it.len;
-                    lim -= kbase;
+                // keys < lim(j) of tile j are visible (all of them off the diagonal and the sequence end)
+                auto lim_of = [&](int jj) {
+                    const bool masked = (p.causal && jj == it.qt) || jj * BN + BN > it.len;
+                    return masked ? (p.causal ? min(qi + 1, it.len) : it.len) - jj * BN : BN;
+                };
+                if ((p.causal && j == it.qt) || j * BN + BN > it.len) {
+                    const int lim = lim_of(j);
 #pragma unroll
                     for (int e = 0; e < BN; ++e)
                         if (e >= lim) x[e] = -INFINITY;
                 }
-                float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]), mx3 = fmaxf(x[6], x[7]);
-#pragma unroll
-                for (int e = 8; e < BN; e += 8) {
-                    mx0 = fmax3(mx0, x[e], x[e + 1]);
-                    mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
-                    mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
-                    mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
-                }
-                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
                 float alpha = 1.f;
-                if (m_tile > m + RESCALE_THRESHOLD) {
-                    alpha = ex2_approx(m - m_tile);
-                    m = m_tile;
+                if (j == 0) {
+                    float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]),
+                          mx3 = fmaxf(x[6], x[7]);
+#pragma unroll
+                    for (int e = 8; e < BN; e += 8) {
+                        mx0 = fmax3(mx0, x[e], x[e + 1]);
+                        mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
+                        mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
+                        mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
+                    }
+                    const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+                    if (m_tile > m + RESCALE_THRESHOLD) {
+                        alpha = ex2_approx(m - m_tile);
+                        m = m_tile;
+                    }
                 }
                 const uint64_t nmp = f2_pack(-m, -m);
                 uint64_t sa = 0, sb = 0;
@@ -280,22 +293,34 @@ diffattn_fwd_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, co
                     tmem_st16(t_s + ch * 16, pk);
                 }
                 const float2 sab = f2_unpack(fadd2(sa, sb));
-                l = __fmaf_rn(l, alpha, __fadd_rn(sab.x, sab.y));
-                // O_c holds this item's sum through tile j-1 (S_c(j) was issued after PV_c(j-1))
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                float sum = __fadd_rn(sab.x, sab.y);
+                // A row sum above 2^32 (or not finite): the warp takes the tile maximum-first
+                // and O_c (this item's sum through tile j-1) moves to the new reference. Rows
+                // past the sequence end take no part in the choice.
+                if (j > 0 && __any_sync(0xffffffffu, qi < it.len && !(sum <= EXACT_SUM))) {
+                    const volatile Item* iv = &ms.work[slot];
+                    const int hv = iv->h, g = hv / (p.H / p.Hkv);
+                    sum = softmax_exact_tile<BN>(
+                        t_s, sq(items & 1) + (uint32_t)c * BOX_BYTES + (uint32_t)r * 128u, r,
+                        reinterpret_cast<const __nv_bfloat16*>(p.k) + ((size_t)(iv->start + j * BN) * p.Hkv + g) * (2 * HD) +
+                            c * HD,
+                        (size_t)p.Hkv * (2 * HD), lim_of(j), sl2, RESCALE_THRESHOLD, m, alpha);
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                        for (int ch = 0; ch < DV / 32; ++ch) {
+                            uint32_t o[32];
+                            tmem_ld32(t_o + ch * 32, o);
+                            tmem_wait_ld();
 #pragma unroll
-                    for (int ch = 0; ch < DV / 32; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld32(t_o + ch * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(t_o + ch * 32, o);
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(t_o + ch * 32, o);
+                        }
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar_p_ready(c));
+                l = __fmaf_rn(l, alpha, sum);
             }
             if (!ok) break;
             // Training outputs: lse_c = m_c + log2(l_c), so that P_c = 2^(S_c scale log2(e) - lse_c).

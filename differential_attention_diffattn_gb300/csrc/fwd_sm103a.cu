@@ -41,6 +41,7 @@
 #include "rope_q.cuh"
 #include "lambda_warp.cuh"
 #include "sm103a_ptx.cuh"
+#include "softmax_exact.cuh"
 
 namespace diffattn {
 namespace {
@@ -75,9 +76,11 @@ constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ uint32_t col_s(int c) { return (uint32_t)c * 128u; }        // S_c / P_c
 __device__ __forceinline__ uint32_t col_o(int c) { return 256u + (uint32_t)c * 128u; } // O_c
 
-// Rescale the running output only when the row maximum grew by more than 2^8
-// (in log2 units); otherwise keep the stale maximum, which bounds P by 256.
+// A maximum-first tile (the first, or the rare exact step) moves the reference maximum
+// only when its own maximum is more than 2^8 above it (in log2 units).
 constexpr float RESCALE_THRESHOLD = 8.0f;
+// Past the first tile, the row sum of a tile above which the warp takes it maximum-first.
+constexpr float EXACT_SUM = 4294967296.0f;  // 2^32
 
 struct Misc {  // lives at OFF_MISC
     uint64_t q_full;
@@ -372,6 +375,11 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
             fence_proxy_async_smem();  // the rotated rows, visible to the MMAs
             mbar_arrive(bar_q_rot);
         }
+        // The reference maximum m is the first tile's: later tiles are exponentiated with it
+        // at once (no maximum pass ahead of the exponentials), P staying below 2^32 unless
+        // a tile's scores rise that far above it; then the warp takes that tile
+        // maximum-first (softmax_exact.cuh). O_c / l_c and lse do not depend on the
+        // reference, and relative precision does not depend on the magnitude.
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = warp_all(mbar_wait(bar_s_full(c), (uint32_t)j & 1u, ab)))) break;
             tc_fence_after();
@@ -385,27 +393,30 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
                 for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(sr[e]);
             }
             const int kbase = j * BN;
-            if ((p.causal && j == qt) || kbase + BN > len) {
-                int lim = p.causal ? min(qi + 1, len) : len;  // keys < lim are visible
-                lim -= kbase;
+            const bool masked = (p.causal && j == qt) || kbase + BN > len;
+            // keys < lim of this tile are visible
+            const int lim = masked ? (p.causal ? min(qi + 1, len) : len) - kbase : BN;
+            if (masked) {
 #pragma unroll
                 for (int e = 0; e < BN; ++e)
                     if (e >= lim) x[e] = -INFINITY;
             }
-            float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]),
-                  mx3 = fmaxf(x[6], x[7]);
-#pragma unroll
-            for (int e = 8; e < BN; e += 8) {
-                mx0 = fmax3(mx0, x[e], x[e + 1]);
-                mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
-                mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
-                mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
-            }
-            const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
             float alpha = 1.f;
-            if (m_tile > m + RESCALE_THRESHOLD) {
-                alpha = ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
-                m = m_tile;
+            if (j == 0) {
+                float mx0 = fmaxf(x[0], x[1]), mx1 = fmaxf(x[2], x[3]), mx2 = fmaxf(x[4], x[5]),
+                      mx3 = fmaxf(x[6], x[7]);
+#pragma unroll
+                for (int e = 8; e < BN; e += 8) {
+                    mx0 = fmax3(mx0, x[e], x[e + 1]);
+                    mx1 = fmax3(mx1, x[e + 2], x[e + 3]);
+                    mx2 = fmax3(mx2, x[e + 4], x[e + 5]);
+                    mx3 = fmax3(mx3, x[e + 6], x[e + 7]);
+                }
+                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sl2;
+                if (m_tile > m + RESCALE_THRESHOLD) {
+                    alpha = ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
+                    m = m_tile;
+                }
             }
             // x * scale * log2(e) - m and the row sum as packed fp32 pairs (half the
             // instructions of the scalar forms)
@@ -432,22 +443,33 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
                 tmem_st16(t_s + ch * 16, pk);
             }
             const float2 sab = f2_unpack(fadd2(sa, sb));
-            l = __fmaf_rn(l, alpha, __fadd_rn(sab.x, sab.y));
-            // O_c holds the sum through tile j-1 here: S_c(j) was issued after PV_c(j-1).
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            float sum = __fadd_rn(sab.x, sab.y);
+            // A row sum above 2^32 (or not finite) means a maximum far above m: the warp takes
+            // the tile maximum-first, and O_c (the sum through tile j-1: S_c(j) was issued after
+            // PV_c(j-1)) moves to the new reference. Rows past the sequence end (never stored)
+            // take no part in the choice, so that it depends on the item's own rows alone.
+            if (j > 0 && __any_sync(0xffffffffu, qi < len && !(sum <= EXACT_SUM))) {
+                sum = softmax_exact_tile<BN>(
+                    t_s, sq + (uint32_t)c * BOX_BYTES + (uint32_t)r * 128u, r,
+                    reinterpret_cast<const __nv_bfloat16*>(p.k) + ((size_t)(start + kbase) * p.Hkv + g) * (2 * HD) +
+                        c * HD,
+                    (size_t)p.Hkv * (2 * HD), lim, sl2, RESCALE_THRESHOLD, m, alpha);
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < DV / 32; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + ch * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-                for (int ch = 0; ch < DV / 32; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + ch * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(t_o + ch * 32, o);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_o + ch * 32, o);
+                    }
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar_p_ready(c));
+            l = __fmaf_rn(l, alpha, sum);
         }
 
         // Training outputs: log2-sum-exp of the scaled scores per component,
@@ -455,10 +477,11 @@ __device__ __forceinline__ void fwd_bf16_body(const CUtensorMap& tm_q, const CUt
         if (ok && p.lse != nullptr && qi < len) p.lse[((size_t)(start + qi) * p.H + h) * 2 + c] = m + __log2f(l);
         // ---- epilogue, split by columns: warpgroup c handles values [64c, 64c + 64)
         // of every row. 1/l_c and the partial sums of squares cross between the two
-        // warpgroups through the Q1 box (2 KB of it): every MMA reading Q1 has
-        // retired once either warpgroup has left its loop (the tensor pipe
-        // completes in issue order and S_2 of the last tile follows S_1).
+        // warpgroups through the Q1 box (2 KB of it), once every softmax warp has left
+        // its loop: every MMA reading Q has retired then (the tensor pipe completes in
+        // issue order), and so has every maximum-first step, which reads Q rows.
         float* xch = reinterpret_cast<float*>(smem + OFF_Q);  // [0,256): 1/l_c, [256,512): sum D^2
+        named_barrier_sync(1, 256);
         xch[c * BM + r] = 1.f / l;
         named_barrier_sync(1, 256);
         ok = warp_all(ok && mbar_wait(bar_o_full, 0, ab));

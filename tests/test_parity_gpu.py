@@ -200,13 +200,24 @@ def test_batch_equals_separate_calls_bitwise():
 
 
 # 3 x 1000 tokens, 16 / 4 heads (8 key tiles an item); 3 x 8192 tokens, 2 heads
-# (items of up to 64 key tiles, the longest the persistent kernel takes)
-@pytest.mark.parametrize("T,H,Hkv", [(1000, 16, 4), (8192, 2, 2)])
-def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv):
+# (items of up to 64 key tiles, the longest the persistent kernel takes); q and k
+# scaled by 6 (scores of a few hundred: rows whose maximum rises past the rescale
+# threshold after the first tile, where the one-item-per-CTA kernel redoes the
+# tile maximum-first)
+@pytest.mark.parametrize("T,H,Hkv,qk_scale", [(1000, 16, 4, 1.0), (8192, 2, 2, 1.0), (1000, 16, 4, 6.0)])
+def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv, qk_scale):
     """An unpacked batch of three sequences runs on the persistent kernel, each
     sequence alone on the one-item-per-CTA kernel: the same bits."""
     wl = W.with_overrides(BF, num_heads=H, num_kv_heads=Hkv)
-    inp = W.generate(wl, seed=32, seq_lens=[T] * 3)
+
+    def gen():
+        g = W.generate(wl, seed=32, seq_lens=[T] * 3)
+        if qk_scale != 1.0:
+            g.q = (g.q.float() * qk_scale).to(torch.bfloat16)
+            g.k = (g.k.float() * qk_scale).to(torch.bfloat16)
+        return g
+
+    inp = gen()
     B = 3
     sh = lambda x: x.cuda().view(B, T, *x.shape[1:])  # noqa: E731
     lam = torch.ones(1, dtype=torch.float32, device="cuda")
@@ -214,7 +225,7 @@ def test_persistent_and_per_tile_kernels_agree_bitwise(T, H, Hkv):
                                   inp.subln_w.cuda()) == "diffattn_fwd_bf16_persistent_kernel"
     full = run_gpu(inp, packed=False)
     for s in range(3):
-        one = W.generate(wl, seed=32, seq_lens=[T] * 3)
+        one = gen()
         a, b = s * T, (s + 1) * T
         one.q, one.k, one.v = one.q[a:b], one.k[a:b], one.v[a:b]
         one.seq_lens, one.cu_seqlens = [T], torch.tensor([0, T], dtype=torch.int32)
