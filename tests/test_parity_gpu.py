@@ -156,6 +156,22 @@ def test_bf16_persistent_kernel(B, T, H, Hkv, causal, per_head):
     compare(run_gpu(inp, packed=False), oracle_out(inp), "bf16")
 
 
+def test_bf16_persistent_kernel_packed_large_scores():
+    """Packed sequences on the persistent kernel with q and k scaled by 6 (scores of a
+    few hundred): later tiles whose row sums pass 2^32 are taken maximum-first from
+    scores recomputed on the CUDA cores, with keys at each sequence's own offset."""
+    wl = W.with_overrides(BF, num_heads=16, num_kv_heads=4)
+    lens = [700, 130, 1024, 257, 900, 64, 511, 1000, 384, 777]
+    inp = W.generate(wl, seed=41, seq_lens=lens)
+    inp.q = (inp.q.float() * 6).to(torch.bfloat16)
+    inp.k = (inp.k.float() * 6).to(torch.bfloat16)
+    t = inp.cu_seqlens.cuda()
+    lam = torch.ones(1, dtype=torch.float32, device="cuda")
+    assert da.diffattn_fwd_kernel(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), lam, inp.subln_w.cuda(), cu_seqlens=t,
+                                  max_seqlen=max(lens)) == "diffattn_fwd_bf16_persistent_kernel"
+    compare(run_gpu(inp), oracle_out(inp), "bf16")
+
+
 def test_bf16_persistent_kernel_longest_items_sampled():
     """2 x 8192 tokens (items of up to 64 key tiles, the longest the persistent
     kernel takes), 16 / 4 heads, against the oracle on sampled rows."""
